@@ -1,0 +1,246 @@
+"""Plain CPU oracle for the quantized-weight matvec path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline / reference leg of ``bench.py`` may import this package.
+The product library (``quantized_weight_matvec_gb300``) never imports it,
+and this package never imports the product library.
+
+The arithmetic lives in ``oracle.c`` (float64, ``-ffp-contract=off``); this
+module only builds it with gcc and marshals numpy arrays through ctypes.
+Every function cites the page section it follows:
+
+* ``needle-2`` -- needle.js tutorial "Inference engine, part 2: kernels and
+  token step": section 1 (FWHT), section 2 (prepare), section 3 (packed-row
+  dot) and "Row gather" (dequantizeRow).
+* ``needle-1`` -- needle.js tutorial "Inference engine, part 1: loader and
+  tokenizer": section 3 (FP16 decode) and section 4 (CqMatrix).
+* ``ds4f-6`` -- ds4f-disk issue #6 "attention + tokenizer + sampling",
+  work item 1 / step 1 (F8 E4M3 + E8M0 block-scaled matvec).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+against values the pages fix, closed forms, library routines (numpy float16,
+torch float8 decode, numpy matmul) or brute force.  None is unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc into liboracle.so next to it."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-fvisibility=hidden", "-o", tmp, _SRC,
+           "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _CQ(ctypes.Structure):
+    _fields_ = [("output", ctypes.c_int64), ("input", ctypes.c_int64),
+                ("input_padded", ctypes.c_int64), ("group", ctypes.c_int64),
+                ("bits", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("row_bytes", ctypes.c_int64),
+                ("packed", ctypes.c_void_p), ("norms", ctypes.c_void_p),
+                ("codebook", ctypes.c_void_p)]
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P, I64, I32, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+    lib.orc_f16_to_f32.argtypes, lib.orc_f16_to_f32.restype = [ctypes.c_uint16], F
+    lib.orc_e4m3_to_f32.argtypes, lib.orc_e4m3_to_f32.restype = [ctypes.c_uint8], F
+    lib.orc_e8m0_to_f32.argtypes, lib.orc_e8m0_to_f32.restype = [ctypes.c_uint8], F
+    lib.orc_fwht_f64.argtypes, lib.orc_fwht_f64.restype = [P, I64], None
+    lib.orc_fwht_f32.argtypes, lib.orc_fwht_f32.restype = [P, I64], None
+    lib.orc_cq_index.argtypes, lib.orc_cq_index.restype = [P, I64, I32, I64, I64], I32
+    lib.orc_cq_prepare.argtypes = [P, I64, I64, I64, I64, ctypes.c_int, P, P]
+    lib.orc_cq_prepare.restype = ctypes.c_int
+    lib.orc_cq_matvec.argtypes = [ctypes.POINTER(_CQ), P, I64, P, P, I64, I64]
+    lib.orc_cq_matvec.restype = ctypes.c_int
+    lib.orc_cq_matvec_mt.argtypes = [ctypes.POINTER(_CQ), P, I64, P, P, I64, I64, ctypes.c_int]
+    lib.orc_cq_matvec_mt.restype = ctypes.c_int
+    lib.orc_cq_dequantize_row.argtypes = [ctypes.POINTER(_CQ), P, I64, P]
+    lib.orc_cq_dequantize_row.restype = ctypes.c_int
+    lib.orc_f8_matvec.argtypes = [P, I64, I64, P, I64, I64, P, I64, P, P, I64, I64]
+    lib.orc_f8_matvec.restype = ctypes.c_int
+    lib.orc_f8_matvec_mt.argtypes = [P, I64, I64, P, I64, I64, P, I64, P, P, I64, I64,
+                                     ctypes.c_int]
+    lib.orc_f8_matvec_mt.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --------------------------------------------------------------------------
+# scalar decodes
+# --------------------------------------------------------------------------
+
+def f16_to_f32(codes) -> np.ndarray:
+    """IEEE binary16 bit patterns -> float32 values (needle-1 section 3)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint16).ravel()
+    return np.array([lib.orc_f16_to_f32(int(h)) for h in c], dtype=np.float32).reshape(
+        np.shape(codes))
+
+
+def e4m3_to_f32(codes) -> np.ndarray:
+    """F8 E4M3 bytes -> float32 values, e=0 subnormal, clamp at 448 (ds4f-6 item 1)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.orc_e4m3_to_f32(int(b)) for b in c], dtype=np.float32).reshape(
+        np.shape(codes))
+
+
+def e8m0_to_f32(codes) -> np.ndarray:
+    """E8M0 bytes -> 2^(e-127) as float32; 255 read as NaN (ds4f-6 step 1)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.orc_e8m0_to_f32(int(b)) for b in c], dtype=np.float32).reshape(
+        np.shape(codes))
+
+
+# --------------------------------------------------------------------------
+# FWHT and prepare
+# --------------------------------------------------------------------------
+
+def fwht_f64(x) -> np.ndarray:
+    """Unnormalised Walsh-Hadamard transform in float64 (needle-2 section 1)."""
+    v = _c(x, np.float64).copy()
+    _load().orc_fwht_f64(_ptr(v), v.size)
+    return v
+
+
+def fwht_f32(x) -> np.ndarray:
+    """The same transform with every butterfly result stored as float32."""
+    v = _c(x, np.float32).copy()
+    _load().orc_fwht_f32(_ptr(v), v.size)
+    return v
+
+
+def cq_prepare(x, input_padded: int, group: int, mode: str = "f32") -> np.ndarray:
+    """prepare(): pad, per-group FWHT, times 1/sqrt(group) (needle-2 section 2).
+
+    ``x`` is [batch, input] float32.  mode "f32" reproduces the page's float32
+    staging exactly (bit-exact target); mode "f64" stays in float64."""
+    x = _c(np.atleast_2d(x), np.float32)
+    batch, inp = x.shape
+    if mode == "f32":
+        out = np.empty((batch, input_padded), dtype=np.float32)
+        _load().orc_cq_prepare(_ptr(x), batch, inp, input_padded, group, 0, _ptr(out), None)
+    elif mode == "f64":
+        out = np.empty((batch, input_padded), dtype=np.float64)
+        _load().orc_cq_prepare(_ptr(x), batch, inp, input_padded, group, 1, None, _ptr(out))
+    else:
+        raise ValueError(mode)
+    return out
+
+
+# --------------------------------------------------------------------------
+# CQ matrix
+# --------------------------------------------------------------------------
+
+class CQMatrix:
+    """The page's CqMatrix (needle-1 section 4) over numpy arrays."""
+
+    def __init__(self, output, input, input_padded, group, bits, packed, norms, codebook):
+        self.output, self.input = int(output), int(input)
+        self.input_padded, self.group, self.bits = int(input_padded), int(group), int(bits)
+        self.packed = _c(packed, np.uint8)
+        self.norms = _c(norms, np.uint16)
+        self.codebook = _c(codebook, np.float32)
+        self.row_bytes = self.packed.shape[1] if self.packed.ndim == 2 else \
+            (self.input_padded * self.bits + 7) // 8
+        self._s = _CQ(self.output, self.input, self.input_padded, self.group, self.bits, 0,
+                      self.row_bytes, _ptr(self.packed), _ptr(self.norms),
+                      _ptr(self.codebook))
+
+    def index(self, r: int, k: int) -> int:
+        """Codebook index of column k in row r (little-endian bit stream)."""
+        return int(_load().orc_cq_index(_ptr(self.packed), self.row_bytes, self.bits, r, k))
+
+    def matvec(self, prepared, rows=None, threads: int = 1, with_mag: bool = True):
+        """cqMatvec (needle-2 section 3) in float64.
+
+        ``prepared`` is [batch, input_padded] (float32 or float64, read as
+        float64).  Returns (y, mag), both [batch, output] float64 (only the
+        rows in ``rows=(r0, r1)`` are filled when given)."""
+        p = _c(np.atleast_2d(prepared), np.float64)
+        batch = p.shape[0]
+        r0, r1 = (0, self.output) if rows is None else rows
+        y = np.zeros((batch, self.output), dtype=np.float64)
+        mag = np.zeros((batch, self.output), dtype=np.float64) if with_mag else None
+        lib = _load()
+        if threads > 1:
+            lib.orc_cq_matvec_mt(ctypes.byref(self._s), _ptr(p), batch, _ptr(y),
+                                 _ptr(mag) if with_mag else None, r0, r1, threads)
+        else:
+            lib.orc_cq_matvec(ctypes.byref(self._s), _ptr(p), batch, _ptr(y),
+                              _ptr(mag) if with_mag else None, r0, r1)
+        return y, mag
+
+    def dequantize_rows(self, rows):
+        """dequantizeRow (needle-2 "Row gather") for each id: [n, input] float32.
+
+        Returns (out, bad) where bad is True if any id was out of range (its
+        row is zeros)."""
+        ids = _c(np.atleast_1d(rows), np.int32)
+        out = np.empty((ids.size, self.input), dtype=np.float32)
+        bad = _load().orc_cq_dequantize_row(ctypes.byref(self._s), _ptr(ids), ids.size,
+                                            _ptr(out))
+        if bad < 0:
+            raise MemoryError("oracle dequantize_row")
+        return out, bool(bad)
+
+
+# --------------------------------------------------------------------------
+# F8 E4M3 + E8M0
+# --------------------------------------------------------------------------
+
+def f8_matvec(w, scale, x, rows=None, threads: int = 1, with_mag: bool = True):
+    """Block-scaled F8 matvec (ds4f-6 step 1) in float64.
+
+    ``w`` [R, C] uint8 E4M3, ``scale`` [SR, SC] uint8 E8M0, ``x`` [batch, C]
+    float32.  Returns (y, mag) [batch, R] float64; only rows in
+    ``rows=(r0, r1)`` are filled when given."""
+    w = _c(w, np.uint8)
+    scale = _c(scale, np.uint8)
+    x = _c(np.atleast_2d(x), np.float32)
+    R, C = w.shape
+    SR, SC = scale.shape
+    batch = x.shape[0]
+    r0, r1 = (0, R) if rows is None else rows
+    y = np.zeros((batch, R), dtype=np.float64)
+    mag = np.zeros((batch, R), dtype=np.float64) if with_mag else None
+    lib = _load()
+    args = (_ptr(w), R, C, _ptr(scale), SR, SC, _ptr(x), batch, _ptr(y),
+            _ptr(mag) if with_mag else None, r0, r1)
+    if threads > 1:
+        lib.orc_f8_matvec_mt(*args, threads)
+    else:
+        lib.orc_f8_matvec(*args)
+    return y, mag

@@ -1,0 +1,365 @@
+/*
+ * oracle.c -- plain, slow CPU oracle for the quantized-weight matvec path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the bench's CPU
+ * baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA library; the two meet only through the seeded input generators.
+ *
+ * Arithmetic is float64 unless the page being followed fixes float32
+ * staging (the CQ activation preparation and dense row gather, whose
+ * reference implementation stores every butterfly result in a
+ * Float32Array).  Build with -O2 -ffp-contract=off and no fast-math so
+ * that every float expression below is one IEEE operation, rounded to
+ * nearest-even, on every host architecture.
+ *
+ * Citations name the page and its section:
+ *   [needle-2] "Inference engine, part 2: kernels and token step"
+ *              (needle.js tutorial), sections 1-3 and "Row gather".
+ *   [needle-1] "Inference engine, part 1: loader and tokenizer"
+ *              (needle.js tutorial), sections 3-4.
+ *   [ds4f-6]   "attention + tokenizer + sampling: the path to real text
+ *              (milestone 6)" (ds4f-disk issue #6), work item 1, step 1
+ *              and step 4.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_API __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------------ */
+/* Scalar decodes                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE binary16 -> value, [needle-1] section 3 "Decode FP16 control
+ * tensors".  Written from the format's definition as a value (sign,
+ * 5-bit biased exponent, 10-bit fraction): exponent 0 is subnormal
+ * (fraction * 2^-24), exponent 31 is inf (fraction 0) or NaN. */
+ORC_API float orc_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return (float)(sign ? -v : v);
+}
+
+/* F8 E4M3 -> value, [ds4f-6] work item 1 and step 1 ("E4M3 LUT decode (e=0
+ * subnormal, e=15 clamp to 448)").  Byte = s eeee mmm.  e=0: m * 2^-9;
+ * otherwise (8+m) * 2^(e-10).  The clamp is read as saturation at 448: it
+ * only changes the codes 0x7F / 0xFF (which would be 480) to +/-448. */
+ORC_API float orc_e4m3_to_f32(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 15;
+    int m = b & 7;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    if (v > 448.0)
+        v = 448.0;
+    return (float)(sign ? -v : v);
+}
+
+/* E8M0 block scale -> value: 2^(e-127).  The pages give the formula and no
+ * exception; code 255 is read as NaN (the OCP microscaling convention for
+ * this format), every other code is exact in float32 (e=0 is the
+ * subnormal 2^-127). */
+ORC_API float orc_e8m0_to_f32(uint8_t e)
+{
+    if (e == 255)
+        return NAN;
+    return (float)ldexp(1.0, (int)e - 127);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Walsh-Hadamard transform, [needle-2] section 1.                           */
+/* Unnormalised, in place, strides 1, 2, 4, ... in increasing order; at each */
+/* stride h the pair (i, i+h) with bit h clear in i becomes (a+b, a-b).      */
+/* ------------------------------------------------------------------------ */
+
+ORC_API void orc_fwht_f64(double *v, int64_t n)
+{
+    for (int64_t h = 1; h < n; h <<= 1)
+        for (int64_t i = 0; i < n; i++)
+            if ((i & h) == 0) {
+                double a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+}
+
+/* Same transform with every intermediate stored as float32, as the page's
+ * implementation does (its buffer is a Float32Array). */
+ORC_API void orc_fwht_f32(float *v, int64_t n)
+{
+    for (int64_t h = 1; h < n; h <<= 1)
+        for (int64_t i = 0; i < n; i++)
+            if ((i & h) == 0) {
+                float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+}
+
+/* ------------------------------------------------------------------------ */
+/* CQ matrix and packed indices, [needle-1] section 4 and [needle-2] 3.      */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int64_t output, input, input_padded, group;
+    int32_t bits, pad_;
+    int64_t row_bytes;
+    const uint8_t *packed;   /* [output, row_bytes]                      */
+    const uint16_t *norms;   /* [output, input_padded / group] binary16  */
+    const float *codebook;   /* [2^bits]                                 */
+} orc_cq;
+
+/* Index of column k in row r: bits [k*bits, k*bits+bits) of the row's
+ * little-endian bit stream, read one bit at a time.  With 2 bits this is
+ * the page's "(byte >> (crumb*2)) & 3" with the low crumb first. */
+ORC_API int32_t orc_cq_index(const uint8_t *packed, int64_t row_bytes, int32_t bits,
+                             int64_t r, int64_t k)
+{
+    const uint8_t *row = packed + r * row_bytes;
+    int32_t idx = 0;
+    for (int32_t i = 0; i < bits; i++) {
+        int64_t t = k * bits + i;
+        int bit = (row[t / 8] >> (t % 8)) & 1;
+        idx |= bit << i;
+    }
+    return idx;
+}
+
+static double inv_sqrt_group(int64_t group)
+{
+    return 1.0 / sqrt((double)group);
+}
+
+/* prepare(), [needle-2] section 2: zero-pad x to input_padded, then per
+ * group the unnormalised FWHT followed by multiplication by 1/sqrt(group).
+ * mode 0: the page's exact float32 staging: butterflies in float32 and the
+ *         scale applied as a float64 product rounded to float32.
+ * mode 1: float64 throughout (used for tolerance-based checks).
+ * x is [batch, input]; out32 / out64 are [batch, input_padded]. */
+ORC_API int orc_cq_prepare(const float *x, int64_t batch, int64_t input,
+                           int64_t input_padded, int64_t group, int mode,
+                           float *out32, double *out64)
+{
+    double s = inv_sqrt_group(group);
+    for (int64_t v = 0; v < batch; v++) {
+        const float *xv = x + v * input;
+        if (mode == 0) {
+            float *o = out32 + v * input_padded;
+            for (int64_t k = 0; k < input_padded; k++)
+                o[k] = (k < input) ? xv[k] : 0.0f;
+            for (int64_t g0 = 0; g0 < input_padded; g0 += group) {
+                orc_fwht_f32(o + g0, group);
+                for (int64_t k = 0; k < group; k++)
+                    o[g0 + k] = (float)((double)o[g0 + k] * s);
+            }
+        } else {
+            double *o = out64 + v * input_padded;
+            for (int64_t k = 0; k < input_padded; k++)
+                o[k] = (k < input) ? (double)xv[k] : 0.0;
+            for (int64_t g0 = 0; g0 < input_padded; g0 += group) {
+                orc_fwht_f64(o + g0, group);
+                for (int64_t k = 0; k < group; k++)
+                    o[g0 + k] *= s;
+            }
+        }
+    }
+    return 0;
+}
+
+/* cqMatvec, [needle-2] section 3:
+ *   y[v,r] = sum_g norm[r,g] * sum_{k in g} codebook[index(r,k)] * p[v,k]
+ * in float64 for rows [r0, r1).  mag[v,r] receives the magnitude sum
+ * sum_g |norm| * sum_k |codebook * p| of exactly the terms added.
+ * prepared is [batch, input_padded] float64, y and mag are [batch, output]. */
+ORC_API int orc_cq_matvec(const orc_cq *m, const double *prepared, int64_t batch,
+                          double *y, double *mag, int64_t r0, int64_t r1)
+{
+    int64_t ngroups = m->input_padded / m->group;
+    for (int64_t r = r0; r < r1; r++)
+        for (int64_t v = 0; v < batch; v++) {
+            const double *p = prepared + v * m->input_padded;
+            double sum = 0.0, abs_sum = 0.0;
+            for (int64_t g = 0; g < ngroups; g++) {
+                double n = orc_f16_to_f32(m->norms[r * ngroups + g]);
+                double part = 0.0, abs_part = 0.0;
+                for (int64_t k = g * m->group; k < (g + 1) * m->group; k++) {
+                    double level = m->codebook[orc_cq_index(m->packed, m->row_bytes, m->bits, r, k)];
+                    part += level * p[k];
+                    abs_part += fabs(level * p[k]);
+                }
+                sum += n * part;
+                abs_sum += fabs(n) * abs_part;
+            }
+            y[v * m->output + r] = sum;
+            if (mag)
+                mag[v * m->output + r] = abs_sum;
+        }
+    return 0;
+}
+
+/* dequantizeRow, [needle-2] "Row gather": per group, each level times the
+ * group's norm (one float32 product), then the normalised FWHT (butterflies
+ * in float32, then 1/sqrt(group) as in prepare), keeping only the first
+ * `input` columns.  rows holds n row ids; out is [n, input].  A row id
+ * outside [0, output) yields a row of zeros and a return value of 1. */
+ORC_API int orc_cq_dequantize_row(const orc_cq *m, const int32_t *rows, int64_t n, float *out)
+{
+    int64_t P = m->input_padded, G = m->group, ngroups = P / G;
+    double s = inv_sqrt_group(G);
+    float *dense = (float *)malloc(sizeof(float) * (size_t)P);
+    int bad = 0;
+    if (!dense)
+        return -1;
+    for (int64_t i = 0; i < n; i++) {
+        int64_t r = rows[i];
+        float *o = out + i * m->input;
+        if (r < 0 || r >= m->output) {
+            bad = 1;
+            for (int64_t k = 0; k < m->input; k++)
+                o[k] = 0.0f;
+            continue;
+        }
+        for (int64_t g = 0; g < ngroups; g++) {
+            float n_g = orc_f16_to_f32(m->norms[r * ngroups + g]);
+            for (int64_t k = g * G; k < (g + 1) * G; k++)
+                dense[k] = m->codebook[orc_cq_index(m->packed, m->row_bytes, m->bits, r, k)] * n_g;
+            orc_fwht_f32(dense + g * G, G);
+            for (int64_t k = g * G; k < (g + 1) * G; k++)
+                dense[k] = (float)((double)dense[k] * s);
+        }
+        memcpy(o, dense, sizeof(float) * (size_t)m->input);
+    }
+    free(dense);
+    return bad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* F8 E4M3 matvec with E8M0 block scales, [ds4f-6] step 1: weight [R, C],    */
+/* scale [SR, SC]; element (r, c) uses scale[r*SR/R][c*SC/C] (integer floor).*/
+/*   y[v,r] = sum_c e4m3(w[r,c]) * e8m0(scale[..][..]) * x[v,c]              */
+/* in float64 for rows [r0, r1); mag = sum_c |w * s * x|.                    */
+/* ------------------------------------------------------------------------ */
+
+ORC_API int orc_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                          int64_t SR, int64_t SC, const float *x, int64_t batch,
+                          double *y, double *mag, int64_t r0, int64_t r1)
+{
+    for (int64_t r = r0; r < r1; r++) {
+        int64_t rb = r * SR / R;
+        for (int64_t v = 0; v < batch; v++) {
+            const float *xv = x + v * C;
+            double sum = 0.0, abs_sum = 0.0;
+            for (int64_t c = 0; c < C; c++) {
+                int64_t cb = c * SC / C;
+                double term = (double)orc_e4m3_to_f32(w[r * C + c]) *
+                              (double)orc_e8m0_to_f32(scale[rb * SC + cb]) * (double)xv[c];
+                sum += term;
+                abs_sum += fabs(term);
+            }
+            y[v * R + r] = sum;
+            if (mag)
+                mag[v * R + r] = abs_sum;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Row-range threading for timing the oracle on many host cores.  Each       */
+/* thread runs the single-threaded function above on its own row range.      */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int kind; /* 0 = cq, 1 = f8 */
+    const orc_cq *m;
+    const double *prepared;
+    const uint8_t *w, *scale;
+    int64_t R, C, SR, SC;
+    const float *x;
+    int64_t batch;
+    double *y, *mag;
+    int64_t r0, r1;
+} orc_job;
+
+static void *orc_run_job(void *arg)
+{
+    orc_job *j = (orc_job *)arg;
+    if (j->kind == 0)
+        orc_cq_matvec(j->m, j->prepared, j->batch, j->y, j->mag, j->r0, j->r1);
+    else
+        orc_f8_matvec(j->w, j->R, j->C, j->scale, j->SR, j->SC, j->x, j->batch, j->y, j->mag,
+                      j->r0, j->r1);
+    return NULL;
+}
+
+static int orc_run_threads(orc_job proto, int64_t r0, int64_t r1, int nthreads)
+{
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    pthread_t tid[256];
+    orc_job jobs[256];
+    int64_t rows = r1 - r0;
+    int started = 0;
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t] = proto;
+        jobs[t].r0 = r0 + rows * t / nthreads;
+        jobs[t].r1 = r0 + rows * (t + 1) / nthreads;
+        if (t == nthreads - 1 || pthread_create(&tid[t], NULL, orc_run_job, &jobs[t]) != 0) {
+            orc_run_job(&jobs[t]); /* last range (or a failed spawn) runs here */
+        } else {
+            started = t + 1;
+        }
+    }
+    for (int t = 0; t < started; t++)
+        pthread_join(tid[t], NULL);
+    return 0;
+}
+
+ORC_API int orc_cq_matvec_mt(const orc_cq *m, const double *prepared, int64_t batch,
+                             double *y, double *mag, int64_t r0, int64_t r1, int nthreads)
+{
+    orc_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 0;
+    j.m = m;
+    j.prepared = prepared;
+    j.batch = batch;
+    j.y = y;
+    j.mag = mag;
+    return orc_run_threads(j, r0, r1, nthreads);
+}
+
+ORC_API int orc_f8_matvec_mt(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                             int64_t SR, int64_t SC, const float *x, int64_t batch,
+                             double *y, double *mag, int64_t r0, int64_t r1, int nthreads)
+{
+    orc_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 1;
+    j.w = w;
+    j.R = R;
+    j.C = C;
+    j.scale = scale;
+    j.SR = SR;
+    j.SC = SC;
+    j.x = x;
+    j.batch = batch;
+    j.y = y;
+    j.mag = mag;
+    return orc_run_threads(j, r0, r1, nthreads);
+}
