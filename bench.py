@@ -1,0 +1,476 @@
+"""Bench of the quantized-weight matvec path on GB300.
+
+One step = one pass of the whole path over one batch-1 decode-shaped input,
+with every input already resident in HBM:
+
+  1. cq_prepare        x[500] -> prepared[512]        (CQ 2-bit vocabulary matrix)
+  2. cq_matvec         32768 x 512, 2-bit, group 128  -> logits[32768]
+  3. cq_dequantize_row 64 row ids                     -> embeddings[64, 500]
+  4. f8_matvec         245760 x 4096 E4M3, E8M0 scales [1920, 32] -> head[245760]
+
+metric: weight GB/s (algorithmic bytes: packed weights + norms / scales +
+codebook + activations in + results out) per second, plus microseconds per
+matvec and the fraction of HBM bandwidth of the dominant kernel.  Each step
+streams ~1.01 GB, more than the 129 MB L2, so every step starts L2-cold for
+the weights.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) each rank runs an independent replica on its own GPU
+(the matvec has no exchange step); the time is the max over ranks and the
+value counts the bytes of all ranks.  --impl reference times the CPU oracle
+on the host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 quantized matvec: weight GB/s and % of GB300 HBM peak; µs per matvec"
+WORKLOAD = ("decode pair, batch 1: CQ 2-bit vocabulary projection 32768x512 (input 500, "
+            "group 128) with prepare and a 64-row gather + F8 E4M3 head 245760x4096 "
+            "(E8M0 scales [1920,32])")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes
+# --------------------------------------------------------------------------
+
+def cq_matvec_bytes(out, P, G, bits, batch=1):
+    rb = (P * bits + 7) // 8
+    return out * rb + out * (P // G) * 2 + (1 << bits) * 4 + batch * P * 4 + batch * out * 4
+
+
+def cq_prepare_bytes(inp, P, batch=1):
+    return batch * (inp + P) * 4
+
+
+def cq_gather_bytes(n, inp, P, G, bits):
+    rb = (P * bits + 7) // 8
+    return n * 4 + n * (rb + (P // G) * 2) + (1 << bits) * 4 + n * inp * 4
+
+
+def f8_bytes(R, C, SR, SC, batch=1):
+    return R * C + SR * SC + batch * C * 4 + batch * R * 4
+
+
+def step_bytes(cq, f8):
+    return {
+        "cq_prepare": cq_prepare_bytes(cq.input, cq.input_padded),
+        "cq_matvec": cq_matvec_bytes(cq.output, cq.input_padded, cq.group, cq.bits),
+        "cq_dequantize_row": cq_gather_bytes(len(cq.rows), cq.input, cq.input_padded, cq.group,
+                                             cq.bits),
+        "f8_matvec": f8_bytes(f8.R, f8.C, f8.SR, f8.SC),
+    }
+
+
+def make_inputs():
+    from quantized_weight_matvec_gb300 import synth
+    cq = synth.workload_inputs("cq2_vocab")
+    f8 = synth.workload_inputs("f8_head", batch=1)
+    return cq, f8
+
+
+# --------------------------------------------------------------------------
+# distributed helpers (replicas)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(d):
+    if d is not None:
+        d.barrier()
+
+
+def max_over_ranks(value: float, d) -> float:
+    """Max of a float over all ranks (identity on one rank)."""
+    if d is None:
+        return value
+    import torch
+    dev = "cuda" if d.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    d.all_reduce(t, op=d.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="qmv_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 active=parts[4], hw=parts[5], hwt=parts[6], swt=parts[7],
+                                 pcap=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 200] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(load),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# --------------------------------------------------------------------------
+# roofline inputs
+# --------------------------------------------------------------------------
+
+def measured_hbm_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("f8_kernels.cu", "qmv_internal.h"):
+        with open(os.path.join(ROOT, "quantized_weight_matvec_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic():
+    """DRAM bytes per f8_matvec launch from the committed ncu summary, or None
+    if the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "f8_head_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    from quantized_weight_matvec_gb300 import qmv
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    d = init_dist(world, "nccl")
+    qmv.load()
+    cq, f8 = make_inputs()
+    nbytes = step_bytes(cq, f8)
+    total_bytes = sum(nbytes.values())
+
+    dev = torch.device("cuda", local)
+    m = qmv.CQMatrix.from_numpy(cq, device=dev)
+    x3 = torch.from_numpy(cq.x).to(dev)
+    ids = torch.from_numpy(cq.rows).to(dev)
+    w5 = torch.from_numpy(f8.w).to(dev)
+    s5 = torch.from_numpy(f8.scale).to(dev)
+    x5 = torch.from_numpy(f8.x).to(dev)
+    prepared = torch.empty((1, cq.input_padded), dtype=torch.float32, device=dev)
+    logits = torch.empty((1, cq.output), dtype=torch.float32, device=dev)
+    emb = torch.empty((len(cq.rows), cq.input), dtype=torch.float32, device=dev)
+    head = torch.empty((1, f8.R), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    names = ["cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec"]
+
+    def check(st, name):
+        if st != 0:
+            raise RuntimeError("%s failed: %s" % (name, qmv.status_string(st)))
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        check(qmv.cq_prepare(m.struct, x3.data_ptr(), 1, prepared.data_ptr(), sh), names[0])
+        if ev is not None:
+            ev[1].record(stream)
+        check(qmv.cq_matvec(m.struct, prepared.data_ptr(), 1, logits.data_ptr(), sh), names[1])
+        if ev is not None:
+            ev[2].record(stream)
+        check(qmv.cq_dequantize_row(m.struct, ids.data_ptr(), ids.numel(), emb.data_ptr(), 0, sh),
+              names[2])
+        if ev is not None:
+            ev[3].record(stream)
+        check(qmv.f8_matvec(w5.data_ptr(), f8.R, f8.C, s5.data_ptr(), f8.SR, f8.SC, x5.data_ptr(),
+                            1, head.data_ptr(), sh), names[3])
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(d)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(d)
+    clock_info = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    per_kernel_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                     for i, n in enumerate(names)}
+
+    # end to end through the C-ABI from pinned host buffers: activations in,
+    # results out, weights resident
+    hx3 = torch.from_numpy(cq.x).pin_memory()
+    hids = torch.from_numpy(cq.rows).pin_memory()
+    hx5 = torch.from_numpy(f8.x).pin_memory()
+    hlog = torch.empty(logits.shape, dtype=torch.float32).pin_memory()
+    hemb = torch.empty(emb.shape, dtype=torch.float32).pin_memory()
+    hhead = torch.empty(head.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        x3.copy_(hx3, non_blocking=True)
+        ids.copy_(hids, non_blocking=True)
+        x5.copy_(hx5, non_blocking=True)
+        step()
+        hlog.copy_(logits, non_blocking=True)
+        hemb.copy_(emb, non_blocking=True)
+        hhead.copy_(head, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(d)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(d)
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = hx3.numel() * 4 + hids.numel() * 4 + hx5.numel() * 4
+    d2h = (hlog.numel() + hemb.numel() + hhead.numel()) * 4
+
+    # correctness spot check of this run's outputs (cheap, outside timing)
+    assert torch.isfinite(head).all() and torch.isfinite(logits).all()
+
+    elapsed_s = max_over_ranks(elapsed_ms / 1e3, d)
+    e2e_s = max_over_ranks(e2e_ms / 1e3, d)
+    f8_s = max_over_ranks(per_kernel_ms["f8_matvec"] / 1e3, d)
+    cpu = cpu_baseline(cq, f8) if (rank == 0 and world == 1) else None
+    if rank != 0:
+        if d is not None:
+            d.destroy_process_group()
+        return
+    peak, peak_kind = measured_hbm_gbs()
+    f8_achieved = nbytes["f8_matvec"] / f8_s / 1e9
+    value = world * total_bytes * args.steps / elapsed_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed_s * 1e3 / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; weights resident in HBM)",
+        "config": {"workload": WORKLOAD, "batch": 1,
+                   "bytes_per_step": total_bytes,
+                   "l2": "inputs larger than L2: each step streams %.2f GB" % (total_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_matvec": {k: round(v * 1e3, 3) for k, v in per_kernel_ms.items()},
+        "gbs_per_kernel": {k: round(nbytes[k] / (per_kernel_ms[k] / 1e3) / 1e9, 1)
+                           for k in names},
+        "hbm_frac_of_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {"kernel": "f8_matvec (245760x4096, batch 1)", "bound": "hbm",
+                     "achieved": round(f8_achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind + " copy bandwidth", "unit": "GB/s",
+                     "frac": round(f8_achieved / peak, 4), "traffic": ncu_traffic(),
+                     "algorithmic_bytes": nbytes["f8_matvec"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * total_bytes * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clock_info,
+        "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if d is not None:
+        d.destroy_process_group()
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample(cq, f8, frac, threads):
+    """Run the oracle over the first `frac` of the rows of both matrices (plus
+    prepare and the full gather); return (seconds, algorithmic bytes)."""
+    import oracle
+    om = oracle.CQMatrix(cq.output, cq.input, cq.input_padded, cq.group, cq.bits, cq.packed,
+                         cq.norms, cq.codebook)
+    r3 = max(1, int(cq.output * frac))
+    r5 = max(1, int(f8.R * frac))
+    t = time.perf_counter()
+    p = oracle.cq_prepare(cq.x, cq.input_padded, cq.group, mode="f32")
+    om.matvec(p, rows=(0, r3), threads=threads, with_mag=False)
+    om.dequantize_rows(cq.rows)
+    oracle.f8_matvec(f8.w, f8.scale, f8.x, rows=(0, r5), threads=threads, with_mag=False)
+    dt = time.perf_counter() - t
+    b = (cq_prepare_bytes(cq.input, cq.input_padded)
+         + cq_matvec_bytes(r3, cq.input_padded, cq.group, cq.bits)
+         + cq_gather_bytes(len(cq.rows), cq.input, cq.input_padded, cq.group, cq.bits)
+         + f8_bytes(r5, f8.C, f8.SR, f8.SC))
+    return dt, b, r3, r5
+
+
+def calibrate(cq, f8, threads, target_s):
+    """Fraction of the workload the oracle covers in about target_s seconds."""
+    oracle_sample(cq, f8, 1.0 / 8192, threads)  # first call: library load, first touches
+    frac = 1.0 / 1024
+    for _ in range(8):
+        dt, b, r3, r5 = oracle_sample(cq, f8, frac, threads)
+        if dt >= 0.2 * target_s or frac >= 1.0:
+            break
+        frac = min(1.0, frac * 8)
+    return min(1.0, frac * target_s / max(dt, 1e-6))
+
+
+def cpu_baseline(cq, f8, target_s=2.0):
+    threads = os.cpu_count() or 1
+    frac = calibrate(cq, f8, threads, target_s)
+    dt, b, r3, r5 = oracle_sample(cq, f8, frac, threads)
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "float64 C oracle, %d threads: prepare + 64-row gather + first %d of 32768 "
+                      "CQ rows + first %d of 245760 F8 rows (%.3f%% of the step), %.2f s" % (
+                          threads, r3, r5, 100 * frac, dt)}
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if world > 1 and rank != 0:
+        return
+    cq, f8 = make_inputs()
+    threads = os.cpu_count() or 1
+    frac = calibrate(cq, f8, threads, 1.0)
+    for _ in range(args.warmup):
+        oracle_sample(cq, f8, frac, threads)
+    total_t, total_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, b, r3, r5 = oracle_sample(cq, f8, frac, threads)
+        total_t += dt
+        total_b += b
+    value = total_b / total_t / 1e9
+    sample = ("float64 C oracle, %d threads, per step: prepare + 64-row gather + first %d of "
+              "32768 CQ rows + first %d of 245760 F8 rows (%.3f%% of the workload)" % (
+                  threads, r3, r5, 100 * frac))
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_t * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": WORKLOAD, "batch": 1, "sample_fraction": frac},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

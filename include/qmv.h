@@ -1,0 +1,188 @@
+/*
+ * qmv.h -- C ABI of libqmv, the GB300 (sm_103a) quantized-weight matvec.
+ *
+ * Two weight formats, each applied to 1..8 activation vectors at once:
+ *
+ *   CQ  (needle.js tutorial "Inference engine, part 2: kernels and token
+ *        step", sections 1-3 and "Row gather"; matrix layout from "part 1:
+ *        loader and tokenizer", section 4 "Retain packed matrices"):
+ *        activations are zero-padded and rotated by a per-group Walsh-
+ *        Hadamard transform; weights are 2/3/4/5-bit codebook indices with
+ *        one binary16 norm per (row, group).
+ *   F8  (ds4f-disk issue #6 "attention + tokenizer + sampling", work item 1
+ *        and step 1): E4M3 weight bytes with E8M0 block scales.
+ *
+ * Conventions shared by every entry point
+ *   - All array pointers are DEVICE pointers, owned by the caller.  The
+ *     library allocates nothing, never synchronises the device and never
+ *     reads device memory on the host.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream of the current device).
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns its status and launches nothing.  Outputs are
+ *     then left untouched.
+ *   - Arrays are dense and row-major, batch-major for activations:
+ *     x[v][k] lives at x + v * width + k.
+ *   - Outputs are fully overwritten and must not overlap any input
+ *     (QMV_ERR_ALIAS).  Repeated calls on equal inputs give bitwise equal
+ *     outputs (fixed reduction order, no floating-point atomics).
+ *   - float pointers must be 4-byte aligned, binary16 pointers 2-byte
+ *     aligned, int32 pointers 4-byte aligned (QMV_ERR_ALIGN).  Wider
+ *     alignment and shapes that are multiples of 16 bytes let the library
+ *     pick its vectorised kernels; other layouts take a general kernel
+ *     with the same results.
+ *   - Errors of the CUDA runtime at launch are reported as QMV_ERR_CUDA.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QMV_API __attribute__((visibility("default")))
+#else
+#define QMV_API
+#endif
+
+/* Same handle type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *qmv_stream;
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_ERR_NULL = 1,      /* a required pointer is NULL                         */
+    QMV_ERR_SHAPE = 2,     /* a size is out of range or inconsistent             */
+    QMV_ERR_BITS = 3,      /* CQ bits not in {2, 3, 4, 5}                        */
+    QMV_ERR_GROUP = 4,     /* CQ group not a power of two in [2, min(P, 32768)]   */
+    QMV_ERR_BATCH = 5,     /* batch not in [1, 8]                                */
+    QMV_ERR_ALIGN = 6,     /* a pointer is not aligned to its element type        */
+    QMV_ERR_OVERFLOW = 7,  /* a size product does not fit the library's limits  */
+    QMV_ERR_ALIAS = 8,     /* an output overlaps an input                        */
+    QMV_ERR_CUDA = 9,      /* the CUDA runtime reported an error at launch       */
+    QMV_ERR_ROW_ID = 10    /* (device status) a gathered row id was out of range */
+} qmv_status;
+
+/* Largest group the CQ kernels transform (one group must fit in shared
+ * memory as float32). */
+#define QMV_MAX_GROUP 32768
+/* Largest activation batch per call. */
+#define QMV_MAX_BATCH 8
+
+/*
+ * A CQ matrix, the page's CqMatrix record ("part 1", section 4): fields
+ * output, input, inputPadded, group, bits, rowBytes, packed, norms and the
+ * codebook for this bit width.
+ *
+ *   output        rows (>= 0)
+ *   input         logical columns, 1 <= input <= input_padded
+ *   input_padded  stored columns P, a multiple of group
+ *   group         FWHT group G, a power of two, 2 <= G <= min(P, 32768)
+ *   bits          index width b in {2, 3, 4, 5}
+ *   row_bytes     must equal ceil(P * b / 8) (the record-length rule of
+ *                 "part 1", "Minimal tests")
+ *   packed        [output, row_bytes] bytes.  Column k of row r is the
+ *                 integer formed by bits [k*b, k*b + b) of the row's
+ *                 little-endian bit stream (bit t = byte t/8, bit t%8).  For
+ *                 b = 2 this is four codes per byte, low crumb first
+ *                 ("part 2", section 3); for b = 4 two codes, low nibble
+ *                 first.
+ *   norms         [output, P / G] IEEE binary16 bit patterns
+ *   codebook      [2^b] float32 levels
+ */
+typedef struct {
+    int64_t output;
+    int64_t input;
+    int64_t input_padded;
+    int64_t group;
+    int32_t bits;
+    int32_t reserved; /* must be 0 */
+    int64_t row_bytes;
+    const uint8_t *packed;
+    const uint16_t *norms;
+    const float *codebook;
+} qmv_cq_matrix;
+
+/*
+ * cq_prepare -- "part 2", section 2 "Prepare an activation for CQ".
+ *
+ * For each of `batch` vectors: copy x[v][0..input) into a zero-padded row of
+ * input_padded floats, apply the unnormalised FWHT to every group of G
+ * consecutive columns (butterfly strides 1, 2, 4, ... in that order, each
+ * result rounded to float32, pair (i, i+h) -> (a+b, a-b)), then multiply
+ * each element by s = 1/sqrt(G) computed in float64, the product taken in
+ * float64 and rounded to float32.  The result is bit-exact to that
+ * definition.
+ *
+ *   m         matrix whose input, input_padded and group are used (its
+ *             data pointers are not read and may be NULL)
+ *   x         [batch, input] float32
+ *   prepared  [batch, input_padded] float32, written
+ */
+QMV_API qmv_status cq_prepare(const qmv_cq_matrix *m, const float *x, int32_t batch,
+                      float *prepared, qmv_stream stream);
+
+/*
+ * cq_matvec -- "part 2", section 3 "Dot packed rows directly":
+ *
+ *   y[v][r] = sum_g f16(norms[r][g]) * sum_{k in group g} codebook[idx(r,k)] * prepared[v][k]
+ *
+ * accumulated in float32 (fixed order).  Accuracy: within
+ * 1e-4 * sum_g |norm| sum_k |codebook * prepared| + 1e-6 of the exact value.
+ *
+ *   prepared  [batch, input_padded] float32 (normally cq_prepare's output)
+ *   y         [batch, output] float32, written
+ */
+QMV_API qmv_status cq_matvec(const qmv_cq_matrix *m, const float *prepared, int32_t batch,
+                     float *y, qmv_stream stream);
+
+/*
+ * cq_dequantize_row -- "part 2", "Row gather" (the embedding lookup of
+ * section 5).  For each id: per group, every level times the group's norm
+ * (one float32 product), the unnormalised FWHT as in cq_prepare, then the
+ * 1/sqrt(G) scale as in cq_prepare; the first `input` columns are written.
+ * Bit-exact to that definition.
+ *
+ *   rows        [n] int32 row ids (n >= 0)
+ *   out         [n, input] float32, written
+ *   dev_status  optional device int32.  An id outside [0, output) gives a
+ *               row of zeros and stores QMV_ERR_ROW_ID here (the value is
+ *               never reset by the library: the caller zeroes it).
+ */
+QMV_API qmv_status cq_dequantize_row(const qmv_cq_matrix *m, const int32_t *rows, int64_t n,
+                             float *out, int32_t *dev_status, qmv_stream stream);
+
+/*
+ * f8_matvec -- ds4f-disk issue #6, step 1 (the F8 matvec with per-block
+ * E8M0 scales; the head of work item 3 has this shape):
+ *
+ *   y[v][r] = sum_c e4m3(w[r][c]) * e8m0(scale[r*SR/R][c*SC/C]) * x[v][c]
+ *
+ * with integer floor division.  E4M3: e=0 subnormal m*2^-9, otherwise
+ * (1+m/8)*2^(e-7), saturated at 448 (so 0x7F / 0xFF read as +/-448).  E8M0:
+ * 2^(e-127); code 255 is NaN.  Accumulated in float32; accuracy within
+ * 1e-4 * sum_c |w * s * x| + 1e-6 of the exact value.
+ *
+ *   w      [R, C] E4M3 bytes, R >= 0, C >= 1
+ *   scale  [SR, SC] E8M0 bytes, 1 <= SR <= max(R, 1), 1 <= SC <= C
+ *   x      [batch, C] float32
+ *   y      [batch, R] float32, written
+ */
+QMV_API qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                     int64_t SR, int64_t SC, const float *x, int32_t batch, float *y,
+                     qmv_stream stream);
+
+/* Human-readable name of a status code (static storage). */
+QMV_API const char *qmv_status_string(qmv_status status);
+
+/* ABI version of this header: 1. */
+QMV_API int32_t qmv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

@@ -1,0 +1,292 @@
+// f8_kernels.cu -- block-scaled F8 E4M3 matvec for sm_103a.
+//
+// Method: ds4f-disk issue #6 "attention + tokenizer + sampling" -- work item 1
+// and step 1 (ds4f_f8_matvec: E4M3 decode with e=0 subnormal and the e=15
+// clamp at 448; E8M0 block scales, scale [SR x SC] over weight [R x C], element
+// (r, c) -> scale[r*SR/R][c*SC/C]), work item 3 (the ~246k x 4096 head, the
+// largest matvec, kept resident).  The page's kernels are scalar / NEON / AVX2
+// loops with a byte lookup table; here the weight stream is the whole cost,
+// so the fast kernel is built around 128-bit streaming loads and keeps every
+// other operand on chip.
+//
+//   y[v][r] = sum_c E4M3(w[r][c]) * E8M0(scale[r*SR/R][c*SC/C]) * x[v][c]
+//
+// E8M0 code 255 is read as NaN (OCP microscaling); every other code is
+// 2^(e-127), exact in float32 (e = 0 is the subnormal 2^-127).
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "qmv_internal.h"
+
+namespace qmv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+struct F8Args {
+    const uint8_t *w;
+    const uint8_t *scale;
+    const float *x;
+    float *y;
+    int64_t R, C, SR, SC;
+};
+
+// E4M3 byte -> float32 from its fields, with the saturation at 448 (so the
+// codes 0x7F / 0xFF, NaN in the OCP "fn" variant, read as +/-448).
+__device__ __forceinline__ float e4m3_exact(unsigned b) {
+    const unsigned e = (b >> 3) & 15u, m = b & 7u;
+    float mag;
+    if (e == 0) {
+        mag = float(m) * 0.001953125f;  // m * 2^-9, exact
+    } else {
+        mag = __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) * 2^(e-7)
+        mag = fminf(mag, 448.0f);
+    }
+    return (b & 0x80u) ? -mag : mag;
+}
+
+// E8M0 byte -> 2^(e-127) as float32; 255 -> NaN.
+__device__ __forceinline__ float e8m0_value(unsigned e) {
+    if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, subnormal
+    if (e == 255) return __uint_as_float(0x7fc00000u);
+    return __uint_as_float(e << 23);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;  // every lane holds the same bits (a + b == b + a)
+}
+
+// Exact per-element evaluation of one output, shared by the general kernel
+// and by the fast kernel's fix-up of rows that hit a saturated code.  The
+// whole warp calls it.
+__device__ float f8_row_exact(const F8Args &a, int64_t r, int v, const float *lut) {
+    const int64_t rb = r * a.SR / a.R;
+    const uint8_t *wr = a.w + r * a.C;
+    const uint8_t *sr = a.scale + rb * a.SC;
+    const float *xv = a.x + int64_t(v) * a.C;
+    float acc = 0.0f;
+    for (int64_t c = threadIdx.x & 31; c < a.C; c += 32) {
+        const float wv = lut ? lut[__ldg(wr + c)] : e4m3_exact(__ldg(wr + c));
+        const float sv = e8m0_value(__ldg(sr + c * a.SC / a.C));
+        acc = fmaf(wv * sv, __ldg(xv + c), acc);
+    }
+    return warp_sum(acc);
+}
+
+// ---------------------------------------------------------------------------
+// General kernel: any C, any scale blocking, any alignment.  One warp per
+// row, a shared-memory table of the 256 exact E4M3 values.
+// ---------------------------------------------------------------------------
+template <int B>
+__global__ void __launch_bounds__(256) f8_general_kernel(F8Args a) {
+    __shared__ float lut[256];
+    lut[threadIdx.x] = e4m3_exact(threadIdx.x);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < a.R; r += nwarps) {
+#pragma unroll 1
+        for (int v = 0; v < B; v++) {
+            const float val = f8_row_exact(a, r, v, lut);
+            if (lane == 0) a.y[int64_t(v) * a.R + r] = val;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fast kernel.  Requirements (checked by the launcher): C % 16 == 0, w and x
+// 16-byte aligned, and every 16-column chunk inside one scale block.
+//
+// Each warp owns an even share of the rows and walks it in tiles of T rows.
+// Lane l takes the 16-byte chunks l, l+32, ... of every row in the tile, so
+// one warp-wide load streams 512 contiguous bytes of a row and the T loads of
+// a chunk are independent (T * 512 bytes in flight per warp).  For a tile
+// whose rows share one scale row, x is multiplied by the chunk's E8M0 scale
+// once and reused for all T rows.  Decode: cvt.rn.f16x2.e4m3x2 (exact) then
+// f16 -> f32 (exact), one FMA per weight and vector, float32 accumulation and
+// a fixed-order warp reduction.  The hardware conversion maps 0x7F / 0xFF to
+// NaN; a row whose sum comes out NaN is recomputed exactly (saturating
+// decode), which also keeps NaN scales and non-finite x consistent with the
+// per-element definition.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
+    uint4 d;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+                 : "l"(p));
+    return d;
+}
+
+__device__ __forceinline__ void decode4(unsigned word, float (&f)[4]) {
+    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(word & 0xffffu), __NV_E4M3);
+    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(word >> 16), __NV_E4M3);
+    float2 a = __half22float2(__half2(lo));
+    float2 b = __half22float2(__half2(hi));
+    f[0] = a.x;
+    f[1] = a.y;
+    f[2] = b.x;
+    f[3] = b.y;
+}
+
+__device__ __forceinline__ unsigned word_of(const uint4 &d, int q) {
+    return q == 0 ? d.x : q == 1 ? d.y : q == 2 ? d.z : d.w;
+}
+
+template <int B, int T>
+__device__ __forceinline__ void f8_tile(const F8Args &a, int64_t r0, int rows, int64_t rb,
+                                        const int *chunk_cb) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunk = a.C >> 4;
+    const uint8_t *base = a.w + r0 * a.C;
+    const uint8_t *srow = a.scale + rb * a.SC;
+    float acc[T][B];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int v = 0; v < B; v++) acc[t][v] = 0.0f;
+
+    for (int64_t ch = lane; ch < nchunk; ch += 32) {
+        uint4 d[T];
+#pragma unroll
+        for (int t = 0; t < T; t++)
+            d[t] = (t < rows) ? ld_stream(base + int64_t(t) * a.C + ch * 16) : make_uint4(0, 0, 0, 0);
+        const float s = e8m0_value(__ldg(srow + chunk_cb[ch]));
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float xs[B][4];
+#pragma unroll
+            for (int v = 0; v < B; v++) {
+                const float4 xv = __ldg(reinterpret_cast<const float4 *>(a.x + v * a.C + ch * 16 + 4 * q));
+                xs[v][0] = xv.x * s;
+                xs[v][1] = xv.y * s;
+                xs[v][2] = xv.z * s;
+                xs[v][3] = xv.w * s;
+            }
+#pragma unroll
+            for (int t = 0; t < T; t++) {
+                float f[4];
+                decode4(word_of(d[t], q), f);
+#pragma unroll
+                for (int v = 0; v < B; v++) {
+                    acc[t][v] = fmaf(f[0], xs[v][0], acc[t][v]);
+                    acc[t][v] = fmaf(f[1], xs[v][1], acc[t][v]);
+                    acc[t][v] = fmaf(f[2], xs[v][2], acc[t][v]);
+                    acc[t][v] = fmaf(f[3], xs[v][3], acc[t][v]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+#pragma unroll
+        for (int v = 0; v < B; v++) {
+            float val = warp_sum(acc[t][v]);
+            if (t < rows) {
+                if (isnan(val)) val = f8_row_exact(a, r0 + t, v, nullptr);
+                if (lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
+            }
+        }
+    }
+}
+
+template <int B, int T>
+__global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
+    extern __shared__ int chunk_cb[];
+    const int64_t nchunk = a.C >> 4;
+    for (int64_t ch = threadIdx.x; ch < nchunk; ch += blockDim.x)
+        chunk_cb[ch] = int((ch * 16 * a.SC) / a.C);
+    __syncthreads();
+
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t row_begin = a.R * wid / nwarps, row_end = a.R * (wid + 1) / nwarps;
+    for (int64_t r0 = row_begin; r0 < row_end; r0 += T) {
+        const int rows = int(min(int64_t(T), row_end - r0));
+        const int64_t rb0 = r0 * a.SR / a.R, rb1 = (r0 + rows - 1) * a.SR / a.R;
+        if (rb0 == rb1) {
+            f8_tile<B, T>(a, r0, rows, rb0, chunk_cb);
+        } else {
+            for (int t = 0; t < rows; t++) f8_tile<B, 1>(a, r0 + t, 1, (r0 + t) * a.SR / a.R, chunk_cb);
+        }
+    }
+}
+
+// True when every 16-column chunk maps to a single scale block: the first
+// column of each block b, ceil(b*C/SC), is a multiple of 16.
+bool chunks_uniform(int64_t C, int64_t SC) {
+    for (int64_t b = 1; b < SC; b++) {
+        const int64_t start = (b * C + SC - 1) / SC;
+        if (start % 16 != 0) return false;
+    }
+    return true;
+}
+
+int grid_for(const void *kernel, int threads, size_t smem, int64_t warps_wanted) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = int64_t(per_sm) * sm_count();
+    int64_t need = (warps_wanted * 32 + threads - 1) / threads;
+    if (need < 1) need = 1;
+    return int(need < cap ? need : cap);
+}
+
+template <int B>
+qmv_status launch_fast(const F8Args &a, cudaStream_t s) {
+    constexpr int T = (B <= 4) ? 8 : 4;
+    const size_t smem = size_t(a.C >> 4) * sizeof(int);
+    auto kern = f8_fast_kernel<B, T>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return QMV_ERR_CUDA;
+    }
+    const int blocks = grid_for(reinterpret_cast<const void *>(kern), 256, smem, (a.R + T - 1) / T);
+    kern<<<blocks, 256, smem, s>>>(a);
+    return from_cuda(cudaGetLastError());
+}
+
+template <int B>
+qmv_status launch_general(const F8Args &a, cudaStream_t s) {
+    const int blocks = grid_for(reinterpret_cast<const void *>(f8_general_kernel<B>), 256, 0, a.R);
+    f8_general_kernel<B><<<blocks, 256, 0, s>>>(a);
+    return from_cuda(cudaGetLastError());
+}
+
+}  // namespace
+
+qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
+                            int64_t SC, const float *x, int batch, float *y, cudaStream_t s) {
+    F8Args a{w, scale, x, y, R, C, SR, SC};
+    const bool fast = (C % 16 == 0) && (reinterpret_cast<uintptr_t>(w) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (C / 16) * 4 <= 200 * 1024 &&
+                      chunks_uniform(C, SC);
+    if (fast) {
+        switch (batch) {
+            case 1: return launch_fast<1>(a, s);
+            case 2: return launch_fast<2>(a, s);
+            case 3: return launch_fast<3>(a, s);
+            case 4: return launch_fast<4>(a, s);
+            case 5: return launch_fast<5>(a, s);
+            case 6: return launch_fast<6>(a, s);
+            case 7: return launch_fast<7>(a, s);
+            default: return launch_fast<8>(a, s);
+        }
+    }
+    switch (batch) {
+        case 1: return launch_general<1>(a, s);
+        case 2: return launch_general<2>(a, s);
+        case 3: return launch_general<3>(a, s);
+        case 4: return launch_general<4>(a, s);
+        case 5: return launch_general<5>(a, s);
+        case 6: return launch_general<6>(a, s);
+        case 7: return launch_general<7>(a, s);
+        default: return launch_general<8>(a, s);
+    }
+}
+
+}  // namespace qmv

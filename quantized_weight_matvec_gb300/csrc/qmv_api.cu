@@ -1,0 +1,207 @@
+// qmv_api.cu -- the extern "C" boundary of libqmv: argument validation,
+// alias and overflow checks, then dispatch to the kernel launchers.
+//
+// Validation follows the loader discipline of the needle.js tutorial
+// "Inference engine, part 1" (section 2 "Make bounds checks boring": check
+// before every read, multiply shapes with overflow checks, never size work
+// from unvalidated products; "Minimal tests": CQ packed length plus norm
+// length must equal the record) and ds4f-disk issue #6, step 3 (refuse
+// misaligned layouts).  No check reads device memory.
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "qmv_internal.h"
+
+namespace qmv {
+
+int sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace qmv
+
+namespace {
+
+// Sizes are capped well inside int64 so that every index product inside the
+// kernels stays exact.
+constexpr int64_t kMaxDim = int64_t(1) << 40;
+constexpr int64_t kMaxBytes = int64_t(1) << 46;
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out) {
+    if (a < 0 || b < 0) return false;
+    if (__builtin_mul_overflow(a, b, out)) return false;
+    return *out <= kMaxBytes;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Half-open byte ranges [a, a+na) and [b, b+nb) intersect.
+bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
+    if (!a || !b || na <= 0 || nb <= 0) return false;
+    uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + uint64_t(nb) && pb < pa + uint64_t(na);
+}
+
+bool is_pow2(int64_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// Shape checks shared by the three CQ entry points.
+qmv_status check_cq_shape(const qmv_cq_matrix *m) {
+    if (!m) return QMV_ERR_NULL;
+    if (m->reserved != 0) return QMV_ERR_SHAPE;
+    if (m->bits < 2 || m->bits > 5) return QMV_ERR_BITS;
+    if (m->output < 0 || m->output > kMaxDim) return QMV_ERR_SHAPE;
+    if (m->input_padded < 2 || m->input_padded > kMaxDim) return QMV_ERR_SHAPE;
+    if (m->input < 1 || m->input > m->input_padded) return QMV_ERR_SHAPE;
+    if (!is_pow2(m->group) || m->group < 2 || m->group > QMV_MAX_GROUP ||
+        m->group > m->input_padded)
+        return QMV_ERR_GROUP;
+    if (m->input_padded % m->group != 0) return QMV_ERR_SHAPE;
+    int64_t bits_total = 0;
+    if (!mul_ok(m->input_padded, m->bits, &bits_total)) return QMV_ERR_OVERFLOW;
+    if (m->row_bytes != (bits_total + 7) / 8) return QMV_ERR_SHAPE;
+    int64_t tmp = 0;
+    if (!mul_ok(m->output, m->row_bytes, &tmp)) return QMV_ERR_OVERFLOW;
+    if (!mul_ok(m->output, (m->input_padded / m->group) * 2, &tmp)) return QMV_ERR_OVERFLOW;
+    return QMV_OK;
+}
+
+qmv_status check_batch(int32_t batch) {
+    return (batch < 1 || batch > QMV_MAX_BATCH) ? QMV_ERR_BATCH : QMV_OK;
+}
+
+// Byte sizes of the matrix arrays.
+struct CqBytes {
+    int64_t packed, norms, codebook;
+};
+CqBytes cq_bytes(const qmv_cq_matrix *m) {
+    CqBytes b;
+    b.packed = m->output * m->row_bytes;
+    b.norms = m->output * (m->input_padded / m->group) * 2;
+    b.codebook = (int64_t(1) << m->bits) * 4;
+    return b;
+}
+
+qmv_status check_cq_data(const qmv_cq_matrix *m) {
+    if (m->output > 0 && (!m->packed || !m->norms || !m->codebook)) return QMV_ERR_NULL;
+    if (!aligned(m->norms, 2) || !aligned(m->codebook, 4)) return QMV_ERR_ALIGN;
+    return QMV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qmv_status_string(qmv_status s) {
+    switch (s) {
+        case QMV_OK: return "QMV_OK";
+        case QMV_ERR_NULL: return "QMV_ERR_NULL: a required pointer is NULL";
+        case QMV_ERR_SHAPE: return "QMV_ERR_SHAPE: a size is out of range or inconsistent";
+        case QMV_ERR_BITS: return "QMV_ERR_BITS: CQ bits must be 2, 3, 4 or 5";
+        case QMV_ERR_GROUP:
+            return "QMV_ERR_GROUP: CQ group must be a power of two in [2, min(input_padded, 32768)]";
+        case QMV_ERR_BATCH: return "QMV_ERR_BATCH: batch must be in [1, 8]";
+        case QMV_ERR_ALIGN: return "QMV_ERR_ALIGN: a pointer is not aligned to its element type";
+        case QMV_ERR_OVERFLOW: return "QMV_ERR_OVERFLOW: a size product exceeds the library's limits";
+        case QMV_ERR_ALIAS: return "QMV_ERR_ALIAS: an output overlaps an input";
+        case QMV_ERR_CUDA: return "QMV_ERR_CUDA: the CUDA runtime reported an error";
+        case QMV_ERR_ROW_ID: return "QMV_ERR_ROW_ID: a gathered row id was out of range";
+    }
+    return "unknown qmv_status";
+}
+
+int32_t qmv_abi_version(void) { return 1; }
+
+qmv_status cq_prepare(const qmv_cq_matrix *m, const float *x, int32_t batch, float *prepared,
+                      qmv_stream stream) {
+    qmv_status st = check_cq_shape(m);
+    if (st != QMV_OK) return st;
+    if ((st = check_batch(batch)) != QMV_OK) return st;
+    if (!x || !prepared) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(prepared, 4)) return QMV_ERR_ALIGN;
+    int64_t xb = 0, pb = 0;
+    if (!mul_ok(int64_t(batch) * 4, m->input, &xb) || !mul_ok(int64_t(batch) * 4, m->input_padded, &pb))
+        return QMV_ERR_OVERFLOW;
+    if (overlaps(prepared, pb, x, xb)) return QMV_ERR_ALIAS;
+    return qmv::launch_cq_prepare(*m, x, batch, prepared, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status cq_matvec(const qmv_cq_matrix *m, const float *prepared, int32_t batch, float *y,
+                     qmv_stream stream) {
+    qmv_status st = check_cq_shape(m);
+    if (st != QMV_OK) return st;
+    if ((st = check_batch(batch)) != QMV_OK) return st;
+    if ((st = check_cq_data(m)) != QMV_OK) return st;
+    if (!prepared || !y) return QMV_ERR_NULL;
+    if (!aligned(prepared, 4) || !aligned(y, 4)) return QMV_ERR_ALIGN;
+    int64_t pb = 0, yb = 0;
+    if (!mul_ok(int64_t(batch) * 4, m->input_padded, &pb) || !mul_ok(int64_t(batch) * 4, m->output, &yb))
+        return QMV_ERR_OVERFLOW;
+    CqBytes b = cq_bytes(m);
+    if (overlaps(y, yb, prepared, pb) || overlaps(y, yb, m->packed, b.packed) ||
+        overlaps(y, yb, m->norms, b.norms) || overlaps(y, yb, m->codebook, b.codebook))
+        return QMV_ERR_ALIAS;
+    if (m->output == 0) return QMV_OK;
+    return qmv::launch_cq_matvec(*m, prepared, batch, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status cq_dequantize_row(const qmv_cq_matrix *m, const int32_t *rows, int64_t n, float *out,
+                             int32_t *dev_status, qmv_stream stream) {
+    qmv_status st = check_cq_shape(m);
+    if (st != QMV_OK) return st;
+    if (n < 0 || n > kMaxDim) return QMV_ERR_SHAPE;
+    if (n == 0) return QMV_OK;
+    if ((st = check_cq_data(m)) != QMV_OK) return st;
+    if (!rows || !out) return QMV_ERR_NULL;
+    if (!aligned(rows, 4) || !aligned(out, 4) || !aligned(dev_status, 4)) return QMV_ERR_ALIGN;
+    int64_t ob = 0;
+    if (!mul_ok(n * 4, m->input, &ob)) return QMV_ERR_OVERFLOW;
+    CqBytes b = cq_bytes(m);
+    if (overlaps(out, ob, rows, n * 4) || overlaps(out, ob, m->packed, b.packed) ||
+        overlaps(out, ob, m->norms, b.norms) || overlaps(out, ob, m->codebook, b.codebook) ||
+        overlaps(out, ob, dev_status, 4))
+        return QMV_ERR_ALIAS;
+    if (dev_status && (overlaps(dev_status, 4, rows, n * 4) ||
+                       overlaps(dev_status, 4, m->packed, b.packed) ||
+                       overlaps(dev_status, 4, m->norms, b.norms) ||
+                       overlaps(dev_status, 4, m->codebook, b.codebook)))
+        return QMV_ERR_ALIAS;
+    return qmv::launch_cq_dequantize_row(*m, rows, n, out, dev_status,
+                                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
+                     int64_t SC, const float *x, int32_t batch, float *y, qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (R < 0 || R > kMaxDim || C < 1 || C > kMaxDim) return QMV_ERR_SHAPE;
+    if (SR < 1 || SR > (R > 0 ? R : 1) || SC < 1 || SC > C) return QMV_ERR_SHAPE;
+    int64_t wb = 0, sb = 0, xb = 0, yb = 0, t = 0;
+    if (!mul_ok(R, C, &wb) || !mul_ok(SR, SC, &sb) || !mul_ok(int64_t(batch) * 4, C, &xb) ||
+        !mul_ok(int64_t(batch) * 4, R, &yb))
+        return QMV_ERR_OVERFLOW;
+    // the kernels form r * SR and c * SC in 64 bits
+    if (!mul_ok(R, SR, &t) || !mul_ok(C, SC, &t)) return QMV_ERR_OVERFLOW;
+    if (!x || !scale) return QMV_ERR_NULL;
+    if (R > 0 && (!w || !y)) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(y, 4)) return QMV_ERR_ALIGN;
+    if (overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb) || overlaps(y, yb, x, xb))
+        return QMV_ERR_ALIAS;
+    if (R == 0) return QMV_OK;
+    return qmv::launch_f8_matvec(w, R, C, scale, SR, SC, x, batch, y,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// qmv_internal.h -- host-side interfaces between the C-ABI layer (qmv_api.cu)
+// and the kernel translation units (cq_kernels.cu, f8_kernels.cu).
+// Arguments reaching these launchers are already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qmv.h"
+
+namespace qmv {
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Fills a cudaError_t into a qmv_status.
+inline qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ERR_CUDA; }
+
+// ---- CQ ------------------------------------------------------------------
+qmv_status launch_cq_prepare(const qmv_cq_matrix &m, const float *x, int batch, float *prepared,
+                             cudaStream_t s);
+qmv_status launch_cq_dequantize_row(const qmv_cq_matrix &m, const int32_t *rows, int64_t n,
+                                    float *out, int32_t *dev_status, cudaStream_t s);
+qmv_status launch_cq_matvec(const qmv_cq_matrix &m, const float *prepared, int batch, float *y,
+                            cudaStream_t s);
+
+// ---- F8 ------------------------------------------------------------------
+qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                            int64_t SR, int64_t SC, const float *x, int batch, float *y,
+                            cudaStream_t s);
+
+}  // namespace qmv

@@ -1,0 +1,235 @@
+"""ctypes binding of libqmv (include/qmv.h): argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module only
+checks tensor dtypes / devices / contiguity, passes ``data_ptr()`` values and
+torch's current CUDA stream, and turns status codes into exceptions.  There
+is no CPU fallback: if the library cannot be loaded, import fails loudly.
+
+Raw entry points with the C names (``cq_prepare``, ``cq_matvec``,
+``cq_dequantize_row``, ``f8_matvec``) take integer device pointers exactly as
+the C-ABI does; the ``*_t`` helpers take torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build_lib
+
+QMV_OK = 0
+STATUS_NAMES = {0: "QMV_OK", 1: "QMV_ERR_NULL", 2: "QMV_ERR_SHAPE", 3: "QMV_ERR_BITS",
+                4: "QMV_ERR_GROUP", 5: "QMV_ERR_BATCH", 6: "QMV_ERR_ALIGN",
+                7: "QMV_ERR_OVERFLOW", 8: "QMV_ERR_ALIAS", 9: "QMV_ERR_CUDA",
+                10: "QMV_ERR_ROW_ID"}
+MAX_BATCH = 8
+MAX_GROUP = 32768
+
+
+class QmvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+class CQMatrixStruct(ctypes.Structure):
+    """Mirror of qmv_cq_matrix."""
+    _fields_ = [("output", ctypes.c_int64), ("input", ctypes.c_int64),
+                ("input_padded", ctypes.c_int64), ("group", ctypes.c_int64),
+                ("bits", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("row_bytes", ctypes.c_int64),
+                ("packed", ctypes.c_void_p), ("norms", ctypes.c_void_p),
+                ("codebook", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return build_lib.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libqmv.so, building it first if it is missing or stale and nvcc exists."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = build_lib.LIB
+    if not build_lib.up_to_date():
+        try:
+            build_lib.build()
+        except Exception as e:  # no toolkit: fail loudly unless a library is present
+            if not os.path.exists(path):
+                raise RuntimeError("libqmv.so is not built and cannot be built: %s" % e) from e
+    lib = ctypes.CDLL(path)
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    CQP = ctypes.POINTER(CQMatrixStruct)
+    lib.cq_prepare.argtypes = [CQP, P, I32, P, P]
+    lib.cq_matvec.argtypes = [CQP, P, I32, P, P]
+    lib.cq_dequantize_row.argtypes = [CQP, P, I64, P, P, P]
+    lib.f8_matvec.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P]
+    for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.f8_matvec):
+        fn.restype = ctypes.c_int
+    lib.qmv_status_string.argtypes = [ctypes.c_int]
+    lib.qmv_status_string.restype = ctypes.c_char_p
+    lib.qmv_abi_version.argtypes = []
+    lib.qmv_abi_version.restype = I32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().qmv_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(load().qmv_abi_version())
+
+
+# --------------------------------------------------------------------------
+# raw C-ABI calls (integer pointers), returning the status code
+# --------------------------------------------------------------------------
+
+def cq_struct(output, input, input_padded, group, bits, row_bytes, packed=0, norms=0,
+              codebook=0, reserved=0) -> CQMatrixStruct:
+    return CQMatrixStruct(int(output), int(input), int(input_padded), int(group), int(bits),
+                          int(reserved), int(row_bytes), int(packed) or None, int(norms) or None,
+                          int(codebook) or None)
+
+
+def cq_prepare(m: CQMatrixStruct, x: int, batch: int, prepared: int, stream: int = 0) -> int:
+    return load().cq_prepare(ctypes.byref(m), x or None, batch, prepared or None, stream or None)
+
+
+def cq_matvec(m: CQMatrixStruct, prepared: int, batch: int, y: int, stream: int = 0) -> int:
+    return load().cq_matvec(ctypes.byref(m), prepared or None, batch, y or None, stream or None)
+
+
+def cq_dequantize_row(m: CQMatrixStruct, rows: int, n: int, out: int, dev_status: int = 0,
+                      stream: int = 0) -> int:
+    return load().cq_dequantize_row(ctypes.byref(m), rows or None, n, out or None,
+                                    dev_status or None, stream or None)
+
+
+def f8_matvec(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: int, batch: int, y: int,
+              stream: int = 0) -> int:
+    return load().f8_matvec(w or None, R, C, scale or None, SR, SC, x or None, batch, y or None,
+                            stream or None)
+
+
+# --------------------------------------------------------------------------
+# torch helpers
+# --------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev(t, dtype, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != QMV_OK:
+        raise QmvError(status, where)
+
+
+class CQMatrix:
+    """A CQ matrix whose arrays live on the GPU (the page's CqMatrix record)."""
+
+    def __init__(self, output, input, input_padded, group, bits, packed, norms, codebook):
+        torch = _torch()
+        self.output, self.input, self.input_padded = int(output), int(input), int(input_padded)
+        self.group, self.bits = int(group), int(bits)
+        self.row_bytes = (self.input_padded * self.bits + 7) // 8
+        self.packed = _dev(packed, torch.uint8, "packed")
+        self.norms = _dev(norms, (torch.int16, torch.uint16), "norms")
+        self.codebook = _dev(codebook, torch.float32, "codebook")
+        self.struct = cq_struct(self.output, self.input, self.input_padded, self.group, self.bits,
+                                self.row_bytes, self.packed.data_ptr(), self.norms.data_ptr(),
+                                self.codebook.data_ptr())
+
+    @classmethod
+    def from_numpy(cls, c, device="cuda"):
+        """Upload a synth.CQInputs (or any object with the same fields)."""
+        torch = _torch()
+        return cls(c.output, c.input, c.input_padded, c.group, c.bits,
+                   torch.from_numpy(c.packed).to(device),
+                   torch.from_numpy(c.norms.view("int16")).to(device),
+                   torch.from_numpy(c.codebook).to(device))
+
+
+def cq_prepare_t(m: CQMatrix, x, out=None, stream=None):
+    """prepared[B, P] = cq_prepare(x[B, input])."""
+    torch = _torch()
+    x = _dev(x, torch.float32, "x")
+    batch = x.shape[0] if x.dim() == 2 else 1
+    if out is None:
+        out = torch.empty((batch, m.input_padded), dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(cq_prepare(m.struct, x.data_ptr(), batch, out.data_ptr(), _stream(stream)), "cq_prepare")
+    return out
+
+
+def cq_matvec_t(m: CQMatrix, prepared, out=None, stream=None):
+    """y[B, output] = cq_matvec(prepared[B, P])."""
+    torch = _torch()
+    prepared = _dev(prepared, torch.float32, "prepared")
+    batch = prepared.shape[0] if prepared.dim() == 2 else 1
+    if out is None:
+        out = torch.empty((batch, m.output), dtype=torch.float32, device=prepared.device)
+    _dev(out, torch.float32, "out")
+    _check(cq_matvec(m.struct, prepared.data_ptr(), batch, out.data_ptr(), _stream(stream)),
+           "cq_matvec")
+    return out
+
+
+def cq_dequantize_row_t(m: CQMatrix, rows, out=None, status=None, stream=None):
+    """out[n, input] = dense rows of the given ids."""
+    torch = _torch()
+    rows = _dev(rows, torch.int32, "rows")
+    n = rows.numel()
+    if out is None:
+        out = torch.empty((n, m.input), dtype=torch.float32, device=rows.device)
+    _dev(out, torch.float32, "out")
+    sp = 0
+    if status is not None:
+        sp = _dev(status, torch.int32, "status").data_ptr()
+    _check(cq_dequantize_row(m.struct, rows.data_ptr(), n, out.data_ptr(), sp, _stream(stream)),
+           "cq_dequantize_row")
+    return out
+
+
+def f8_matvec_t(w, scale, x, out=None, stream=None):
+    """y[B, R] = f8_matvec(w[R, C], scale[SR, SC], x[B, C])."""
+    torch = _torch()
+    w = _dev(w, torch.uint8, "w")
+    scale = _dev(scale, torch.uint8, "scale")
+    x = _dev(x, torch.float32, "x")
+    R, C = w.shape
+    SR, SC = scale.shape
+    batch = x.shape[0] if x.dim() == 2 else 1
+    if out is None:
+        out = torch.empty((batch, R), dtype=torch.float32, device=w.device)
+    _dev(out, torch.float32, "out")
+    _check(f8_matvec(w.data_ptr(), R, C, scale.data_ptr(), SR, SC, x.data_ptr(), batch,
+                     out.data_ptr(), _stream(stream)), "f8_matvec")
+    return out

@@ -1,0 +1,116 @@
+"""CPU checks of the C-ABI library: it loads, exports every declared symbol,
+and rejects invalid arguments on the host before any launch.
+
+Nothing here touches a GPU: every call below fails validation, and the
+library returns its status before calling the CUDA runtime.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from quantized_weight_matvec_gb300 import build_lib, qmv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmv.h")
+
+# a fake, 256-byte aligned, never dereferenced device address
+FAKE = 0x7F0000000000
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"QMV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec",
+              "qmv_status_string", "qmv_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    path = build_lib.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+    lib = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(lib, name)
+
+
+def test_only_the_abi_is_exported():
+    out = subprocess.run(["nm", "-D", "--defined-only", build_lib.build()], capture_output=True,
+                         text=True, check=True).stdout
+    funcs = {l.split()[-1] for l in out.splitlines() if l.split() and l.split()[-2] == "T"}
+    assert funcs == set(declared_functions())
+
+
+def test_status_strings_and_version():
+    assert qmv.abi_version() == 1
+    for code, name in qmv.STATUS_NAMES.items():
+        assert qmv.status_string(code).startswith(name)
+
+
+def _m(**kw):
+    f = dict(output=64, input=500, input_padded=512, group=128, bits=2, row_bytes=128,
+             packed=FAKE, norms=FAKE, codebook=FAKE)
+    f.update(kw)
+    return qmv.cq_struct(**f)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=1), 3), (dict(bits=6), 3),
+    (dict(group=96), 4), (dict(group=1), 4), (dict(group=1024), 4), (dict(group=65536), 4),
+    (dict(input=0), 2), (dict(input=513), 2),
+    (dict(row_bytes=125), 2), (dict(input_padded=500, row_bytes=125), 2),
+    (dict(output=-1), 2), (dict(reserved=1), 2),
+])
+def test_cq_shape_rejections(kw, code):
+    m = _m(**kw)
+    assert qmv.cq_prepare(m, FAKE, 1, FAKE + 65536) == code
+    assert qmv.cq_matvec(m, FAKE, 1, FAKE + 65536) == code
+    assert qmv.cq_dequantize_row(m, FAKE, 1, FAKE + 65536) == code
+
+
+def test_cq_batch_null_align_alias():
+    m = _m()
+    assert qmv.cq_prepare(m, FAKE, 0, FAKE + 65536) == 5
+    assert qmv.cq_prepare(m, FAKE, 9, FAKE + 65536) == 5
+    assert qmv.cq_prepare(m, 0, 1, FAKE + 65536) == 1
+    assert qmv.cq_matvec(m, FAKE, 1, 0) == 1
+    assert qmv.cq_matvec(_m(packed=0), FAKE, 1, FAKE + 65536) == 1
+    assert qmv.cq_matvec(m, FAKE + 2, 1, FAKE + 65536) == 6
+    assert qmv.cq_matvec(_m(norms=FAKE + 1), FAKE, 1, FAKE + 65536) == 6
+    # y overlapping the prepared vector, or the packed rows
+    assert qmv.cq_matvec(m, FAKE, 1, FAKE + 1024) == 8
+    assert qmv.cq_matvec(_m(packed=FAKE + (1 << 20)), FAKE, 1, FAKE + (1 << 20) + 64) == 8
+    assert qmv.cq_prepare(m, FAKE, 1, FAKE + 512) == 8
+    assert qmv.cq_dequantize_row(m, FAKE, -1, FAKE + 65536) == 2
+    assert qmv.cq_dequantize_row(m, FAKE, 0, FAKE + 65536) == 0  # empty: nothing to do
+    assert qmv.cq_dequantize_row(m, FAKE + 2, 3, FAKE + 65536) == 6
+    # empty matrix: valid, nothing launched
+    assert qmv.cq_matvec(_m(output=0), FAKE, 1, FAKE + 65536) == 0
+
+
+def test_f8_rejections():
+    W, S, X, Y = FAKE, FAKE + (1 << 30), FAKE + (1 << 31), FAKE + (1 << 32)
+    assert qmv.f8_matvec(W, 16, 16, S, 1, 1, X, 0, Y) == 5
+    assert qmv.f8_matvec(W, 16, 0, S, 1, 1, X, 1, Y) == 2
+    assert qmv.f8_matvec(W, 16, 16, S, 17, 1, X, 1, Y) == 2
+    assert qmv.f8_matvec(W, 16, 16, S, 1, 17, X, 1, Y) == 2
+    assert qmv.f8_matvec(W, 16, 16, S, 0, 1, X, 1, Y) == 2
+    assert qmv.f8_matvec(W, -1, 16, S, 1, 1, X, 1, Y) == 2
+    assert qmv.f8_matvec(W, 1 << 41, 16, S, 1, 1, X, 1, Y) == 2
+    assert qmv.f8_matvec(W, 1 << 39, 1 << 39, S, 1, 1, X, 1, Y) == 7
+    assert qmv.f8_matvec(0, 16, 16, S, 1, 1, X, 1, Y) == 1
+    assert qmv.f8_matvec(W, 16, 16, 0, 1, 1, X, 1, Y) == 1
+    assert qmv.f8_matvec(W, 16, 16, S, 1, 1, X + 2, 1, Y) == 6
+    assert qmv.f8_matvec(W, 16, 16, S, 1, 1, X, 1, W + 8) == 8
+    assert qmv.f8_matvec(W, 16, 16, S, 1, 1, X, 1, X + 16) == 8
+    assert qmv.f8_matvec(W, 0, 16, S, 1, 1, X, 1, 0) == 0  # R = 0: nothing to do
