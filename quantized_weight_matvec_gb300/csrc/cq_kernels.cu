@@ -210,9 +210,7 @@ qmv_status launch_group(const GroupArgs &a, cudaStream_t s) {
         }
     } else {
         size_t smem = size_t(a.G) * sizeof(float);
-        cudaError_t e = cudaFuncSetAttribute(group_block_kernel<M>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return QMV_ERR_CUDA;
+        if (!allow_smem(reinterpret_cast<const void *>(group_block_kernel<M>), smem)) return QMV_ERR_CUDA;
         group_block_kernel<M><<<dim3(unsigned(jobs)), 1024, smem, s>>>(a);
     }
     return from_cuda(cudaGetLastError());
@@ -296,7 +294,21 @@ __global__ void __launch_bounds__(256) cq_matvec_general_kernel(qmv_cq_matrix m,
 // ---------------------------------------------------------------------------
 
 template <int CPR>
-__global__ void __launch_bounds__(256) cq2_table_kernel(qmv_cq_matrix m, const float *p, float *y) {
+__device__ __forceinline__ void cq2_load(uint4 &d, float &n, const qmv_cq_matrix &m, int64_t r, int q,
+                                         int g, int64_t nG) {
+    d = make_uint4(0, 0, 0, 0);
+    n = 0.0f;
+    if (r < m.output) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(m.packed + r * m.row_bytes) + q;
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+                     : "l"(src));
+        n = half_bits_to_float(__ldg(m.norms + r * nG + g));
+    }
+}
+
+template <int CPR>
+__global__ void __launch_bounds__(1024, 1) cq2_table_kernel(qmv_cq_matrix m, const float *p, float *y) {
     constexpr int RPW = 32 / CPR;
     constexpr int P = CPR * 64;
     constexpr int NIB_STRIDE = 4 * P;  // bytes per nibble block
@@ -305,6 +317,19 @@ __global__ void __launch_bounds__(256) cq2_table_kernel(qmv_cq_matrix m, const f
     extern __shared__ __align__(16) unsigned char table_raw[];
     float *table = reinterpret_cast<float *>(table_raw);
 
+    const int lane = threadIdx.x & 31;
+    const int rho = lane / CPR, q = lane % CPR;
+    const int64_t nG = P / m.group;
+    const int g = (q * 64) / int(m.group);
+    const int64_t ngroups_rows = (m.output + RPW - 1) / RPW;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    int64_t rg = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+
+    // the first rows' loads go out before the table is built
+    uint4 d;
+    float n;
+    cq2_load<CPR>(d, n, m, rg * RPW + rho, q, g, nG);
+
     // ---- build the table (one pass per block) ----
     {
         const float c0 = __ldg(m.codebook + 0), c1 = __ldg(m.codebook + 1);
@@ -312,43 +337,31 @@ __global__ void __launch_bounds__(256) cq2_table_kernel(qmv_cq_matrix m, const f
         for (int u = threadIdx.x; u < 16 * CPR * 32; u += blockDim.x) {
             const int nib = u / (CPR * 32);
             const int rest = u - nib * (CPR * 32);
-            const int q = rest >> 5, j = rest & 31;
+            const int qq = rest >> 5, j = rest & 31;
             const int lo = nib & 3, hi = nib >> 2;
             const float cl = lo == 0 ? c0 : lo == 1 ? c1 : lo == 2 ? c2 : c3;
-            const float ch = hi == 0 ? c0 : hi == 1 ? c1 : hi == 2 ? c2 : c3;
-            const int col = q * 64 + 2 * j;
-            const float v = fmaf(ch, __ldg(p + col + 1), cl * __ldg(p + col));
-            const int slot = (j + RPW * q) & 31;
-            float *blk = table + (nib * NIB_STRIDE + q * 256) / 4;
+            const float chv = hi == 0 ? c0 : hi == 1 ? c1 : hi == 2 ? c2 : c3;
+            const int col = qq * 64 + 2 * j;
+            const float v = fmaf(chv, __ldg(p + col + 1), cl * __ldg(p + col));
+            const int slot = (j + RPW * qq) & 31;
+            float *blk = table + (nib * NIB_STRIDE + qq * 256) / 4;
             blk[slot] = v;
             blk[slot + 32] = v;
         }
     }
     __syncthreads();
 
-    const int lane = threadIdx.x & 31;
-    const int rho = lane / CPR, q = lane % CPR;
     const unsigned lane_part = unsigned(q * 256 + 4 * (rho + RPW * q));
-    const int64_t nG = P / m.group;
-    const int g = (q * 64) / int(m.group);
-    const int64_t ngroups_rows = (m.output + RPW - 1) / RPW;
-    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
     const unsigned tbase = unsigned(__cvta_generic_to_shared(table_raw));
+    const unsigned sh = 4u * unsigned(rho);
 
-    for (int64_t rg = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; rg < ngroups_rows;
-         rg += nwarps) {
+    for (; rg < ngroups_rows; rg += nwarps) {
         const int64_t r = rg * RPW + rho;
-        uint4 d = make_uint4(0, 0, 0, 0);
-        float n = 0.0f;
-        if (r < m.output) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(m.packed + r * m.row_bytes) + q;
-            asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
-                         : "l"(src));
-            n = half_bits_to_float(__ldg(m.norms + r * nG + g));
-        }
+        // next rows' loads before this row's lookups
+        uint4 dn;
+        float nn;
+        cq2_load<CPR>(dn, nn, m, (rg + nwarps) * RPW + rho, q, g, nG);
         // rotate the 128-bit chunk right by 4*rho bits
-        const unsigned sh = 4u * unsigned(rho);
         unsigned w[4];
         w[0] = __funnelshift_r(d.x, d.y, sh);
         w[1] = __funnelshift_r(d.y, d.z, sh);
@@ -369,35 +382,26 @@ __global__ void __launch_bounds__(256) cq2_table_kernel(qmv_cq_matrix m, const f
 #pragma unroll
         for (int dd = CPR / 2; dd >= 1; dd >>= 1) acc += __shfl_xor_sync(kFull, acc, dd);
         if (q == 0 && r < m.output) y[r] = acc;
+        d = dn;
+        n = nn;
     }
-}
-
-int blocks_for(const void *kernel, int threads, size_t smem, int64_t warps_needed) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    int64_t cap = int64_t(per_sm) * sm_count();
-    int64_t need = (warps_needed * 32 + threads - 1) / threads;
-    if (need < 1) need = 1;
-    return int(need < cap ? need : cap);
 }
 
 template <int CPR>
 qmv_status launch_cq2_table(const qmv_cq_matrix &m, const float *p, float *y, cudaStream_t s) {
     const size_t smem = size_t(64) * CPR * 64;
-    cudaError_t e = cudaFuncSetAttribute(cq2_table_kernel<CPR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return QMV_ERR_CUDA;
+    const void *kp = reinterpret_cast<const void *>(cq2_table_kernel<CPR>);
+    if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
     const int64_t rgroups = (m.output + (32 / CPR) - 1) / (32 / CPR);
-    int blocks = blocks_for(reinterpret_cast<const void *>(cq2_table_kernel<CPR>), 256, smem, rgroups);
-    cq2_table_kernel<CPR><<<blocks, 256, smem, s>>>(m, p, y);
+    int64_t blocks = (rgroups + 31) / 32;  // 32 warps per block
+    if (blocks > sm_count()) blocks = sm_count();
+    cq2_table_kernel<CPR><<<int(blocks), 1024, smem, s>>>(m, p, y);
     return from_cuda(cudaGetLastError());
 }
 
 template <int B>
 qmv_status launch_cq_general(const qmv_cq_matrix &m, const float *p, float *y, cudaStream_t s) {
-    int blocks = blocks_for(reinterpret_cast<const void *>(cq_matvec_general_kernel<B>), 256, 0, m.output);
+    int blocks = grid_blocks(reinterpret_cast<const void *>(cq_matvec_general_kernel<B>), 256, 0, m.output);
     cq_matvec_general_kernel<B><<<blocks, 256, 0, s>>>(m, p, y);
     return from_cuda(cudaGetLastError());
 }

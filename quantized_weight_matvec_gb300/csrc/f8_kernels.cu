@@ -103,21 +103,29 @@ __global__ void __launch_bounds__(256) f8_general_kernel(F8Args a) {
 // Each warp owns an even share of the rows and walks it in tiles of T rows.
 // Lane l takes the 16-byte chunks l, l+32, ... of every row in the tile, so
 // one warp-wide load streams 512 contiguous bytes of a row and the T loads of
-// a chunk are independent (T * 512 bytes in flight per warp).  For a tile
-// whose rows share one scale row, x is multiplied by the chunk's E8M0 scale
-// once and reused for all T rows.  Decode: cvt.rn.f16x2.e4m3x2 (exact) then
-// f16 -> f32 (exact), one FMA per weight and vector, float32 accumulation and
-// a fixed-order warp reduction.  The hardware conversion maps 0x7F / 0xFF to
+// a chunk are independent.  The (tile, chunk) loop is flattened and, with PF,
+// the T loads of the next step (the next chunk, or the first chunk of the
+// next tile) are issued before the current step is decoded, so every warp
+// keeps 2 * T * 512 bytes of the weight stream in flight.
+//
+// For a tile whose rows share one scale row, x is multiplied by the chunk's
+// E8M0 scale once and reused by all T rows; a tile straddling two scale rows
+// scales x per row.  Decode: cvt.rn.f16x2.e4m3x2 (exact) then f16 -> f32
+// (exact), one FMA per weight and vector, float32 accumulation and a
+// fixed-order warp reduction.  The hardware conversion maps 0x7F / 0xFF to
 // NaN; a row whose sum comes out NaN is recomputed exactly (saturating
 // decode), which also keeps NaN scales and non-finite x consistent with the
 // per-element definition.
 // ---------------------------------------------------------------------------
 
+// Streaming 16-byte load of read-only weights, not kept in L1.  Not volatile:
+// the weights are never written while a matvec runs, so the compiler may
+// schedule these loads freely.
 __device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
     uint4 d;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
-                 : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+        : "l"(p));
     return d;
 }
 
@@ -136,64 +144,67 @@ __device__ __forceinline__ unsigned word_of(const uint4 &d, int q) {
     return q == 0 ? d.x : q == 1 ? d.y : q == 2 ? d.z : d.w;
 }
 
-template <int B, int T>
-__device__ __forceinline__ void f8_tile(const F8Args &a, int64_t r0, int rows, int64_t rb,
-                                        const int *chunk_cb) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nchunk = a.C >> 4;
-    const uint8_t *base = a.w + r0 * a.C;
-    const uint8_t *srow = a.scale + rb * a.SC;
-    float acc[T][B];
+// The T weight chunks of one step: rows r0 .. r0+rows-1, chunk ch.  Rows past
+// the tile's end re-read its last row and chunks past the row's end re-read
+// its last chunk (in bounds, results unused), so no load is predicated.
+template <int T>
+__device__ __forceinline__ void load_step(uint4 (&d)[T], const F8Args &a, int64_t r0, int rows,
+                                          int64_t ch, int64_t nchunk) {
+    const int64_t chc = ch < nchunk ? ch : nchunk - 1;
+    const uint8_t *p = a.w + r0 * a.C + chc * 16;
 #pragma unroll
-    for (int t = 0; t < T; t++)
-#pragma unroll
-        for (int v = 0; v < B; v++) acc[t][v] = 0.0f;
+    for (int t = 0; t < T; t++) d[t] = ld_stream(p + int64_t(t < rows ? t : rows - 1) * a.C);
+}
 
-    for (int64_t ch = lane; ch < nchunk; ch += 32) {
-        uint4 d[T];
+// acc[t][v] += sum over the 16 columns of chunk ch of w[t] * s * x[v].
+// UNIFORM: every row of the tile uses the scale row srow0; otherwise row t
+// uses srow0 + ((dpack >> 4t) & 15) * SC.
+template <int B, int T, bool UNIFORM>
+__device__ __forceinline__ void compute_step(float (&acc)[T][B], const uint4 (&d)[T], const F8Args &a,
+                                             const uint8_t *srow0, uint32_t dpack, int cb, int64_t ch) {
+    float s0 = 0.0f;
+    if (UNIFORM) s0 = e8m0_value(__ldg(srow0 + cb));
 #pragma unroll
-        for (int t = 0; t < T; t++)
-            d[t] = (t < rows) ? ld_stream(base + int64_t(t) * a.C + ch * 16) : make_uint4(0, 0, 0, 0);
-        const float s = e8m0_value(__ldg(srow + chunk_cb[ch]));
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            float xs[B][4];
-#pragma unroll
-            for (int v = 0; v < B; v++) {
-                const float4 xv = __ldg(reinterpret_cast<const float4 *>(a.x + v * a.C + ch * 16 + 4 * q));
-                xs[v][0] = xv.x * s;
-                xs[v][1] = xv.y * s;
-                xs[v][2] = xv.z * s;
-                xs[v][3] = xv.w * s;
-            }
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-                float f[4];
-                decode4(word_of(d[t], q), f);
-#pragma unroll
-                for (int v = 0; v < B; v++) {
-                    acc[t][v] = fmaf(f[0], xs[v][0], acc[t][v]);
-                    acc[t][v] = fmaf(f[1], xs[v][1], acc[t][v]);
-                    acc[t][v] = fmaf(f[2], xs[v][2], acc[t][v]);
-                    acc[t][v] = fmaf(f[3], xs[v][3], acc[t][v]);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < T; t++) {
+    for (int q = 0; q < 4; q++) {
+        float xv[B][4];
 #pragma unroll
         for (int v = 0; v < B; v++) {
-            float val = warp_sum(acc[t][v]);
-            if (t < rows) {
-                if (isnan(val)) val = f8_row_exact(a, r0 + t, v, nullptr);
-                if (lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
+            const float4 x4 = __ldg(reinterpret_cast<const float4 *>(a.x + v * a.C + ch * 16 + 4 * q));
+            xv[v][0] = x4.x;
+            xv[v][1] = x4.y;
+            xv[v][2] = x4.z;
+            xv[v][3] = x4.w;
+        }
+        float xs[B][4];
+        if (UNIFORM) {
+#pragma unroll
+            for (int v = 0; v < B; v++)
+#pragma unroll
+                for (int k = 0; k < 4; k++) xs[v][k] = xv[v][k] * s0;
+        }
+#pragma unroll
+        for (int t = 0; t < T; t++) {
+            if (!UNIFORM) {
+                const float st = e8m0_value(__ldg(srow0 + int64_t((dpack >> (4 * t)) & 15u) * a.SC + cb));
+#pragma unroll
+                for (int v = 0; v < B; v++)
+#pragma unroll
+                    for (int k = 0; k < 4; k++) xs[v][k] = xv[v][k] * st;
+            }
+            float f[4];
+            decode4(word_of(d[t], q), f);
+#pragma unroll
+            for (int v = 0; v < B; v++) {
+                acc[t][v] = fmaf(f[0], xs[v][0], acc[t][v]);
+                acc[t][v] = fmaf(f[1], xs[v][1], acc[t][v]);
+                acc[t][v] = fmaf(f[2], xs[v][2], acc[t][v]);
+                acc[t][v] = fmaf(f[3], xs[v][3], acc[t][v]);
             }
         }
     }
 }
 
-template <int B, int T>
+template <int B, int T, bool PF, bool GS>
 __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
     extern __shared__ int chunk_cb[];
     const int64_t nchunk = a.C >> 4;
@@ -201,17 +212,92 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
         chunk_cb[ch] = int((ch * 16 * a.SC) / a.C);
     __syncthreads();
 
+    const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
     const int64_t wid = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t row_begin = a.R * wid / nwarps, row_end = a.R * (wid + 1) / nwarps;
-    for (int64_t r0 = row_begin; r0 < row_end; r0 += T) {
-        const int rows = int(min(int64_t(T), row_end - r0));
+    // GS: tiles in grid-stride order (all warps sweep one region of the
+    // matrix together); otherwise each warp owns an even contiguous share.
+    const int64_t row_end = GS ? a.R : a.R * (wid + 1) / nwarps;
+    int64_t r0 = GS ? wid * T : a.R * wid / nwarps;
+    const int64_t tile_stride = GS ? nwarps * T : T;
+    if (r0 >= row_end) return;
+    const int iters = int((nchunk + 31) >> 5);
+
+    int rows = int(min(int64_t(T), row_end - r0));
+    int j = 0;
+    uint4 cur[T];
+    load_step<T>(cur, a, r0, rows, lane, nchunk);
+
+    float acc[T][B];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int v = 0; v < B; v++) acc[t][v] = 0.0f;
+
+    static_assert(T <= 8, "per-row scale deltas are packed in 4 bits");
+    const uint8_t *srow0 = a.scale;
+    uint32_t dpack = 0;
+    bool uniform = true;
+    auto setup_tile = [&]() {
+        // rows of one tile span at most T + 1 scale rows (SR <= R), so each
+        // row's offset from the first fits in 4 bits
         const int64_t rb0 = r0 * a.SR / a.R, rb1 = (r0 + rows - 1) * a.SR / a.R;
-        if (rb0 == rb1) {
-            f8_tile<B, T>(a, r0, rows, rb0, chunk_cb);
-        } else {
-            for (int t = 0; t < rows; t++) f8_tile<B, 1>(a, r0 + t, 1, (r0 + t) * a.SR / a.R, chunk_cb);
+        uniform = (rb0 == rb1);
+        srow0 = a.scale + rb0 * a.SC;
+        dpack = 0;
+        if (!uniform) {
+            for (int t = 1; t < rows; t++) dpack |= uint32_t((r0 + t) * a.SR / a.R - rb0) << (4 * t);
         }
+    };
+    setup_tile();
+
+    while (true) {
+        // position of the next step
+        int jn = j + 1;
+        int64_t r0n = r0;
+        int rowsn = rows;
+        if (jn == iters) {
+            jn = 0;
+            r0n = r0 + tile_stride;
+            rowsn = int(min(int64_t(T), row_end - r0n));
+        }
+        const bool has_next = r0n < row_end;
+        uint4 nxt[T];
+        if (PF && has_next) load_step<T>(nxt, a, r0n, rowsn, lane + 32 * int64_t(jn), nchunk);
+
+        const int64_t ch = lane + 32 * int64_t(j);
+        if (ch < nchunk) {
+            if (uniform)
+                compute_step<B, T, true>(acc, cur, a, srow0, dpack, chunk_cb[ch], ch);
+            else
+                compute_step<B, T, false>(acc, cur, a, srow0, dpack, chunk_cb[ch], ch);
+        }
+        if (j == iters - 1) {  // tile done: reduce, store, restart the sums
+#pragma unroll
+            for (int t = 0; t < T; t++) {
+#pragma unroll
+                for (int v = 0; v < B; v++) {
+                    float val = warp_sum(acc[t][v]);
+                    acc[t][v] = 0.0f;
+                    if (t < rows) {
+                        if (isnan(val)) val = f8_row_exact(a, r0 + t, v, nullptr);
+                        if (lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
+                    }
+                }
+            }
+        }
+        if (!has_next) break;
+        if (PF) {
+#pragma unroll
+            for (int t = 0; t < T; t++) cur[t] = nxt[t];
+        } else {
+            load_step<T>(cur, a, r0n, rowsn, lane + 32 * int64_t(jn), nchunk);
+        }
+        const bool new_tile = (jn == 0);
+        j = jn;
+        r0 = r0n;
+        rows = rowsn;
+        if (new_tile) setup_tile();
     }
 }
 
@@ -225,34 +311,20 @@ bool chunks_uniform(int64_t C, int64_t SC) {
     return true;
 }
 
-int grid_for(const void *kernel, int threads, size_t smem, int64_t warps_wanted) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    const int64_t cap = int64_t(per_sm) * sm_count();
-    int64_t need = (warps_wanted * 32 + threads - 1) / threads;
-    if (need < 1) need = 1;
-    return int(need < cap ? need : cap);
-}
-
-template <int B>
+template <int B, int T = (B <= 4) ? 8 : 4, bool PF = false, bool GS = true>
 qmv_status launch_fast(const F8Args &a, cudaStream_t s) {
-    constexpr int T = (B <= 4) ? 8 : 4;
     const size_t smem = size_t(a.C >> 4) * sizeof(int);
-    auto kern = f8_fast_kernel<B, T>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return QMV_ERR_CUDA;
-    }
-    const int blocks = grid_for(reinterpret_cast<const void *>(kern), 256, smem, (a.R + T - 1) / T);
+    auto kern = f8_fast_kernel<B, T, PF, GS>;
+    const void *kp = reinterpret_cast<const void *>(kern);
+    if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
+    const int blocks = grid_blocks(kp, 256, smem, (a.R + T - 1) / T);
     kern<<<blocks, 256, smem, s>>>(a);
     return from_cuda(cudaGetLastError());
 }
 
 template <int B>
 qmv_status launch_general(const F8Args &a, cudaStream_t s) {
-    const int blocks = grid_for(reinterpret_cast<const void *>(f8_general_kernel<B>), 256, 0, a.R);
+    const int blocks = grid_blocks(reinterpret_cast<const void *>(f8_general_kernel<B>), 256, 0, a.R);
     f8_general_kernel<B><<<blocks, 256, 0, s>>>(a);
     return from_cuda(cudaGetLastError());
 }

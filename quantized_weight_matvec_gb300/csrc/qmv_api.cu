@@ -10,7 +10,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "qmv_internal.h"
 
@@ -29,6 +31,44 @@ int sm_count() {
         cache[dev] = n;
     }
     return cache[dev];
+}
+
+int occupancy(const void *kernel, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, int, size_t>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    const auto key = std::make_tuple(kernel, dev, threads, smem);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+        per_sm < 1) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = per_sm;
+    return per_sm;
+}
+
+bool allow_smem(const void *kernel, size_t smem) {
+    if (smem <= 48 * 1024) return true;
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, size_t> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(std::make_pair(kernel, dev));
+    if (it != done.end() && it->second >= smem) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
+        return false;
+    done[std::make_pair(kernel, dev)] = smem;
+    return true;
 }
 
 }  // namespace qmv
@@ -144,7 +184,7 @@ qmv_status cq_matvec(const qmv_cq_matrix *m, const float *prepared, int32_t batc
     if (st != QMV_OK) return st;
     if ((st = check_batch(batch)) != QMV_OK) return st;
     if ((st = check_cq_data(m)) != QMV_OK) return st;
-    if (!prepared || !y) return QMV_ERR_NULL;
+    if (!prepared || (m->output > 0 && !y)) return QMV_ERR_NULL;
     if (!aligned(prepared, 4) || !aligned(y, 4)) return QMV_ERR_ALIGN;
     int64_t pb = 0, yb = 0;
     if (!mul_ok(int64_t(batch) * 4, m->input_padded, &pb) || !mul_ok(int64_t(batch) * 4, m->output, &yb))

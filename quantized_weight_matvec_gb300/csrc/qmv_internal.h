@@ -13,6 +13,23 @@ namespace qmv {
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Resident blocks per SM of `kernel` at (threads, dynamic smem) on the
+// current device; cached per (kernel, device, threads, smem).  Returns >= 1.
+int occupancy(const void *kernel, int threads, size_t smem);
+
+// Raises the kernel's dynamic shared-memory limit to `smem` bytes once per
+// (kernel, device).  Returns false if the runtime refuses.
+bool allow_smem(const void *kernel, size_t smem);
+
+// Blocks for a grid of `threads`-thread blocks that covers `warps_wanted`
+// warps, capped at resident_per_sm * SMs.
+inline int grid_blocks(const void *kernel, int threads, size_t smem, int64_t warps_wanted) {
+    const int64_t cap = int64_t(occupancy(kernel, threads, smem)) * sm_count();
+    int64_t need = (warps_wanted * 32 + threads - 1) / threads;
+    if (need < 1) need = 1;
+    return int(need < cap ? need : cap);
+}
+
 // Fills a cudaError_t into a qmv_status.
 inline qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ERR_CUDA; }
 

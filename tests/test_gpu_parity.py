@@ -318,5 +318,5 @@ def test_alias_rejected_on_device():
     f = synth.f8_inputs(3, 64, 64, 1, 1, 127, 127)
     w = dev(f.w)
     with pytest.raises(qmv.QmvError) as e:
-        qmv.f8_matvec_t(w, dev(f.scale), dev(f.x), out=w.view(torch.float32)[:64].view(1, 64))
+        qmv.f8_matvec_t(w, dev(f.scale), dev(f.x), out=w.view(-1).view(torch.float32)[:64].view(1, 64))
     assert e.value.status == 8
