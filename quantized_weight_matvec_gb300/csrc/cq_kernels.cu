@@ -98,20 +98,38 @@ struct GroupArgs {
     int32_t *status;
 };
 
-// The value entering the transform at column `col` of job `j`, and whether
-// the job's row id is out of range (gather only).
+// Per-thread copy of the codebook for the gather: lane l holds level l
+// (2^bits <= 32), so a level is one warp shuffle away once the index is known.
 template <GMode M>
-__device__ __forceinline__ float group_load(const GroupArgs &a, int64_t j, int64_t col, bool &bad) {
+__device__ __forceinline__ float codebook_lane(const GroupArgs &a, int lane) {
+    if (M == GMode::Prepare) return 0.0f;
+    return lane < (1 << a.bits) ? __ldg(a.codebook + lane) : 0.0f;
+}
+
+// The value entering the transform at column `col` of job `j` (`valid`
+// false: a padding lane of a partial warp, value 0), and whether the job's
+// row id is out of range (gather only).  Every lane of the warp must call it
+// together: the gather's level lookup is a warp shuffle.
+template <GMode M>
+__device__ __forceinline__ float group_load(const GroupArgs &a, int64_t j, int64_t col, bool valid,
+                                            float cb_lane, bool &bad) {
     if (M == GMode::Prepare) {
         bad = false;
-        return col < a.input ? __ldg(a.x + j * a.input + col) : 0.0f;
+        return (valid && col < a.input) ? __ldg(a.x + j * a.input + col) : 0.0f;
     } else {
-        int64_t r = __ldg(a.rows + j);
-        bad = (r < 0 || r >= a.output);
-        if (bad) return 0.0f;
-        float n = half_bits_to_float(__ldg(a.norms + r * a.nG + col / a.G));
-        float level = __ldg(a.codebook + cq_index(a.packed + r * a.row_bytes, col, a.bits));
-        return __fmul_rn(level, n);
+        int idx = 0;
+        float n = 0.0f;
+        bad = false;
+        if (valid) {
+            const int64_t r = __ldg(a.rows + j);
+            bad = (r < 0 || r >= a.output);
+            if (!bad) {
+                n = half_bits_to_float(__ldg(a.norms + r * a.nG + col / a.G));
+                idx = cq_index(a.packed + r * a.row_bytes, col, a.bits);
+            }
+        }
+        const float level = __shfl_sync(kFull, cb_lane, idx);
+        return (valid && !bad) ? __fmul_rn(level, n) : 0.0f;
     }
 }
 
@@ -130,18 +148,17 @@ __device__ __forceinline__ void group_store(const GroupArgs &a, int64_t j, int64
 // (groups never straddle a warp since G divides 32 and P).
 template <GMode M>
 __global__ void __launch_bounds__(256) group_small_kernel(GroupArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t flat = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x);
     const int64_t total = a.njobs * a.P;
     const bool valid = flat < total;
-    int64_t j = 0, col = 0;
+    const int64_t j = valid ? flat / a.P : 0;
+    const int64_t col = valid ? flat - j * a.P : 0;
     bool bad = false;
-    float v[1] = {0.0f};
-    if (valid) {
-        j = flat / a.P;
-        col = flat - j * a.P;
-        v[0] = group_load<M>(a, j, col, bad);
-    }
+    float v[1];
+    v[0] = group_load<M>(a, j, col, valid, codebook_lane<M>(a, lane), bad);
     fwht_warp<1>(v, int(a.G), lane);
     if (valid) group_store<M>(a, j, col, scale_f64(v[0], a.s), bad);
 }
@@ -149,15 +166,18 @@ __global__ void __launch_bounds__(256) group_small_kernel(GroupArgs a) {
 // 64 <= G <= 1024: one warp per group job, E = G/32 elements per lane.
 template <GMode M, int E>
 __global__ void __launch_bounds__(256) group_warp_kernel(GroupArgs a) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t job = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (job >= a.njobs * a.nG) return;  // whole warp leaves together
     const int64_t j = job / a.nG, g = job - j * a.nG;
     const int64_t col0 = g * a.G + int64_t(lane) * E;
+    const float cbl = codebook_lane<M>(a, lane);
     float v[E];
     bool bad = false;
 #pragma unroll
-    for (int e = 0; e < E; e++) v[e] = group_load<M>(a, j, col0 + e, bad);
+    for (int e = 0; e < E; e++) v[e] = group_load<M>(a, j, col0 + e, true, cbl, bad);
     fwht_warp<E>(v, int(a.G), lane);
 #pragma unroll
     for (int e = 0; e < E; e++) group_store<M>(a, j, col0 + e, scale_f64(v[e], a.s), bad);
@@ -168,11 +188,16 @@ __global__ void __launch_bounds__(256) group_warp_kernel(GroupArgs a) {
 template <GMode M>
 __global__ void __launch_bounds__(1024) group_block_kernel(GroupArgs a) {
     extern __shared__ float sm[];
+    pdl_wait();
+    pdl_trigger();
     const int64_t job = blockIdx.x;
     const int64_t j = job / a.nG, g = job - j * a.nG;
     const int G = int(a.G);
+    const float cbl = codebook_lane<M>(a, threadIdx.x & 31);
     bool bad = false;
-    for (int i = threadIdx.x; i < G; i += blockDim.x) sm[i] = group_load<M>(a, j, g * a.G + i, bad);
+    // G is a multiple of blockDim, so every lane runs the same iterations
+    for (int i = threadIdx.x; i < G; i += blockDim.x)
+        sm[i] = group_load<M>(a, j, g * a.G + i, true, cbl, bad);
     for (int h = 1; h < G; h <<= 1) {
         __syncthreads();
         for (int t = threadIdx.x; t < G / 2; t += blockDim.x) {
@@ -194,26 +219,27 @@ qmv_status launch_group(const GroupArgs &a, cudaStream_t s) {
     if ((a.G <= 32 && (a.njobs * a.P + 255) / 256 > kMaxGrid) ||
         (a.G > 32 && a.G <= 1024 && (jobs * 32 + 255) / 256 > kMaxGrid) || jobs > kMaxGrid)
         return QMV_ERR_OVERFLOW;
+    cudaError_t e = cudaSuccess;
     if (a.G <= 32) {
         int64_t threads = a.njobs * a.P;
         int64_t blocks = (threads + 255) / 256;
-        group_small_kernel<M><<<dim3(unsigned(blocks)), 256, 0, s>>>(a);
+        e = launch_pdl(group_small_kernel<M>, dim3(unsigned(blocks)), dim3(256), 0, s, a);
     } else if (a.G <= 1024) {
         int64_t blocks = (jobs * 32 + 255) / 256;
         const dim3 grid{unsigned(blocks)};
         switch (a.G) {
-            case 64: group_warp_kernel<M, 2><<<grid, 256, 0, s>>>(a); break;
-            case 128: group_warp_kernel<M, 4><<<grid, 256, 0, s>>>(a); break;
-            case 256: group_warp_kernel<M, 8><<<grid, 256, 0, s>>>(a); break;
-            case 512: group_warp_kernel<M, 16><<<grid, 256, 0, s>>>(a); break;
-            default: group_warp_kernel<M, 32><<<grid, 256, 0, s>>>(a); break;
+            case 64: e = launch_pdl(group_warp_kernel<M, 2>, grid, dim3(256), 0, s, a); break;
+            case 128: e = launch_pdl(group_warp_kernel<M, 4>, grid, dim3(256), 0, s, a); break;
+            case 256: e = launch_pdl(group_warp_kernel<M, 8>, grid, dim3(256), 0, s, a); break;
+            case 512: e = launch_pdl(group_warp_kernel<M, 16>, grid, dim3(256), 0, s, a); break;
+            default: e = launch_pdl(group_warp_kernel<M, 32>, grid, dim3(256), 0, s, a); break;
         }
     } else {
         size_t smem = size_t(a.G) * sizeof(float);
         if (!allow_smem(reinterpret_cast<const void *>(group_block_kernel<M>), smem)) return QMV_ERR_CUDA;
-        group_block_kernel<M><<<dim3(unsigned(jobs)), 1024, smem, s>>>(a);
+        e = launch_pdl(group_block_kernel<M>, dim3(unsigned(jobs)), dim3(1024), smem, s, a);
     }
-    return from_cuda(cudaGetLastError());
+    return from_cuda(e);
 }
 
 GroupArgs group_args(const qmv_cq_matrix &m) {
@@ -243,6 +269,8 @@ template <int B>
 __global__ void __launch_bounds__(256) cq_matvec_general_kernel(qmv_cq_matrix m, const float *p,
                                                                 float *y) {
     __shared__ float cb[32];
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x < (1 << m.bits)) cb[threadIdx.x] = m.codebook[threadIdx.x];
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -317,6 +345,8 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(qmv_cq_matrix m, con
     extern __shared__ __align__(16) unsigned char table_raw[];
     float *table = reinterpret_cast<float *>(table_raw);
 
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int rho = lane / CPR, q = lane % CPR;
     const int64_t nG = P / m.group;
@@ -395,15 +425,13 @@ qmv_status launch_cq2_table(const qmv_cq_matrix &m, const float *p, float *y, cu
     const int64_t rgroups = (m.output + (32 / CPR) - 1) / (32 / CPR);
     int64_t blocks = (rgroups + 31) / 32;  // 32 warps per block
     if (blocks > sm_count()) blocks = sm_count();
-    cq2_table_kernel<CPR><<<int(blocks), 1024, smem, s>>>(m, p, y);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(launch_pdl(cq2_table_kernel<CPR>, dim3(unsigned(blocks)), dim3(1024), smem, s, m, p, y));
 }
 
 template <int B>
 qmv_status launch_cq_general(const qmv_cq_matrix &m, const float *p, float *y, cudaStream_t s) {
     int blocks = grid_blocks(reinterpret_cast<const void *>(cq_matvec_general_kernel<B>), 256, 0, m.output);
-    cq_matvec_general_kernel<B><<<blocks, 256, 0, s>>>(m, p, y);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(launch_pdl(cq_matvec_general_kernel<B>, dim3(unsigned(blocks)), dim3(256), 0, s, m, p, y));
 }
 
 }  // namespace

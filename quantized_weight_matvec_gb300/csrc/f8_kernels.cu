@@ -84,6 +84,8 @@ template <int B>
 __global__ void __launch_bounds__(256) f8_general_kernel(F8Args a) {
     __shared__ float lut[256];
     lut[threadIdx.x] = e4m3_exact(threadIdx.x);
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -208,8 +210,11 @@ template <int B, int T, bool PF, bool GS>
 __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
     extern __shared__ int chunk_cb[];
     const int64_t nchunk = a.C >> 4;
+    // (depends only on the shapes: runs before the wait)
     for (int64_t ch = threadIdx.x; ch < nchunk; ch += blockDim.x)
         chunk_cb[ch] = int((ch * 16 * a.SC) / a.C);
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -318,15 +323,13 @@ qmv_status launch_fast(const F8Args &a, cudaStream_t s) {
     const void *kp = reinterpret_cast<const void *>(kern);
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
     const int blocks = grid_blocks(kp, 256, smem, (a.R + T - 1) / T);
-    kern<<<blocks, 256, smem, s>>>(a);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(256), smem, s, a));
 }
 
 template <int B>
 qmv_status launch_general(const F8Args &a, cudaStream_t s) {
     const int blocks = grid_blocks(reinterpret_cast<const void *>(f8_general_kernel<B>), 256, 0, a.R);
-    f8_general_kernel<B><<<blocks, 256, 0, s>>>(a);
-    return from_cuda(cudaGetLastError());
+    return from_cuda(launch_pdl(f8_general_kernel<B>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
 }
 
 }  // namespace

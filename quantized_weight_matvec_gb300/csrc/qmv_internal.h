@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/qmv.h"
 
 namespace qmv {
@@ -28,6 +30,32 @@ inline int grid_blocks(const void *kernel, int threads, size_t smem, int64_t war
     int64_t need = (warps_wanted * 32 + threads - 1) / threads;
     if (need < 1) need = 1;
     return int(need < cap ? need : cap);
+}
+
+// Programmatic dependent launch.  Every kernel of the library starts with
+// pdl_wait(), which returns once all work that precedes it in the stream has
+// completed and its memory is visible, and only then touches global memory;
+// so stream order is preserved whatever the preceding kernel is.  Launched
+// with launch_pdl(), a kernel may be scheduled while the previous kernel in
+// the stream is still running (that kernel calls pdl_trigger()), which hides
+// the launch latency between the back-to-back calls of a decode step.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Fills a cudaError_t into a qmv_status.
