@@ -474,15 +474,133 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------
+# per-workload sweep (--configs): every workload and batch of the pages'
+# shapes, one JSON line each; not the default bench line
+# --------------------------------------------------------------------------
+
+def _graph_time(torch, calls, reps=20):
+    """Median microseconds per call of a CUDA graph holding `calls`."""
+    def checked(c):
+        def run(sh):
+            st = c(sh)
+            if st != 0:
+                raise RuntimeError("call failed with status %d" % st)
+        return run
+    calls = [checked(c) for c in calls]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for c in calls[:4]:
+            c(s.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for c in calls:
+            c(s.cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / len(calls))
+    return statistics.median(ts), min(ts)
+
+
+def run_configs(args):
+    import torch
+    from quantized_weight_matvec_gb300 import qmv, synth
+    qmv.load()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    peak, peak_kind = measured_hbm_gbs()
+    dev = torch.device("cuda", 0)
+
+    def copies_for(nbytes):
+        return max(1, min(4096, -(-2 * l2 // max(nbytes, 1))))
+
+    def emit(name, batch, op, nbytes, us_med, us_best, ncopies):
+        print(json.dumps({"workload": name, "batch": batch, "op": op, "bytes": nbytes,
+                          "us_median": round(us_med, 3), "us_best": round(us_best, 3),
+                          "gbs": round(nbytes / us_med / 1e3, 1),
+                          "frac_of_measured_hbm": round(nbytes / us_med / 1e3 / peak, 4),
+                          "frac_of_8tbs": round(nbytes / us_med / 1e3 / NOMINAL_HBM_GBS, 4),
+                          "l2_cold_copies": ncopies}), flush=True)
+
+    for name, wl in synth.WORKLOADS.items():
+        for batch in wl["batch"]:
+            if wl["kind"] == "cq":
+                for bits in wl["bits"]:
+                    c = synth.workload_inputs(name, bits=bits, batch=batch)
+                    nb = cq_matvec_bytes(c.output, c.input_padded, c.group, c.bits, batch)
+                    k = copies_for(c.output * (c.row_bytes + 2 * (c.input_padded // c.group)))
+                    packed = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(
+                        c.packed, (k,) + c.packed.shape))).to(dev)
+                    norms = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(
+                        c.norms.view(np.int16), (k,) + c.norms.shape))).to(dev)
+                    cb = torch.from_numpy(c.codebook).to(dev)
+                    mats = [qmv.CQMatrix(c.output, c.input, c.input_padded, c.group, c.bits,
+                                         packed[i], norms[i], cb) for i in range(k)]
+                    x = torch.from_numpy(c.x).to(dev)
+                    p = qmv.cq_prepare_t(mats[0], x)
+                    y = torch.empty((batch, c.output), device=dev)
+                    calls = [(lambda m: lambda sh: qmv.cq_matvec(m.struct, p.data_ptr(), batch,
+                                                                  y.data_ptr(), sh))(m)
+                             for m in mats]
+                    med, best = _graph_time(torch, calls)
+                    emit("%s/%dbit" % (name, bits), batch, "cq_matvec", nb, med, best, k)
+                    pc = [lambda sh: qmv.cq_prepare(mats[0].struct, x.data_ptr(), batch,
+                                                    p.data_ptr(), sh)] * 64
+                    med, best = _graph_time(torch, pc)
+                    emit("%s/%dbit" % (name, bits), batch, "cq_prepare",
+                         cq_prepare_bytes(c.input, c.input_padded, batch), med, best, 1)
+                    if wl.get("gather"):
+                        ids = torch.from_numpy(c.rows).to(dev)
+                        emb = torch.empty((len(c.rows), c.input), device=dev)
+                        gc = [(lambda m: lambda sh: qmv.cq_dequantize_row(
+                            m.struct, ids.data_ptr(), ids.numel(), emb.data_ptr(), 0, sh))(m)
+                            for m in mats]
+                        med, best = _graph_time(torch, gc)
+                        emit("%s/%dbit" % (name, bits), len(c.rows), "cq_dequantize_row",
+                             cq_gather_bytes(len(c.rows), c.input, c.input_padded, c.group,
+                                             c.bits), med, best, k)
+                    del packed, norms, mats
+            else:
+                f = synth.workload_inputs(name, batch=batch)
+                nb = f8_bytes(f.R, f.C, f.SR, f.SC, batch)
+                k = copies_for(f.R * f.C)
+                w = torch.from_numpy(f.w).to(dev)
+                ws = [w] + [w.clone() for _ in range(k - 1)]
+                s5 = torch.from_numpy(f.scale).to(dev)
+                x = torch.from_numpy(f.x).to(dev)
+                y = torch.empty((batch, f.R), device=dev)
+                calls = [(lambda wi: lambda sh: qmv.f8_matvec(
+                    wi.data_ptr(), f.R, f.C, s5.data_ptr(), f.SR, f.SC, x.data_ptr(), batch,
+                    y.data_ptr(), sh))(wi) for wi in ws]
+                if k == 1:
+                    calls = calls * 8
+                med, best = _graph_time(torch, calls, reps=10)
+                emit(name, batch, "f8_matvec", nb, med, best, k)
+                del ws, w
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--configs", action="store_true",
+                    help="per-workload sweep (one JSON line per workload, batch and op)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.configs:
+        run_configs(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -158,52 +158,115 @@ __device__ __forceinline__ void load_step(uint4 (&d)[T], const F8Args &a, int64_
     for (int t = 0; t < T; t++) d[t] = ld_stream(p + int64_t(t < rows ? t : rows - 1) * a.C);
 }
 
-// acc[t][v] += sum over the 16 columns of chunk ch of w[t] * s * x[v].
+// Accumulators: batch 1 keeps one float per row and folds the chunk's scale
+// into x (one multiply shared by the T rows); larger batches keep an
+// (even column, odd column) pair per row and vector, fold the scale into the
+// decoded weight pair (one packed multiply shared by the B vectors) and use
+// one packed FMA (fma.rn.f32x2) per weight pair and vector.
+template <int B>
+struct AccOf {
+    typedef float2 type;
+};
+template <>
+struct AccOf<1> {
+    typedef float type;
+};
+__device__ __forceinline__ float acc_total(float v) { return v; }
+__device__ __forceinline__ float acc_total(float2 v) { return v.x + v.y; }
+__device__ __forceinline__ void acc_zero(float &v) { v = 0.0f; }
+__device__ __forceinline__ void acc_zero(float2 &v) { v = make_float2(0.0f, 0.0f); }
+
+__device__ __forceinline__ void decode_pairs(unsigned word, float2 &w01, float2 &w23) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(word & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(word >> 16), __NV_E4M3);
+    w01 = __half22float2(__half2(lo));
+    w23 = __half22float2(__half2(hi));
+}
+
+// acc[t][v] += sum over the 16 columns of chunk ch of w[t] * s_t * x[v].
 // UNIFORM: every row of the tile uses the scale row srow0; otherwise row t
 // uses srow0 + ((dpack >> 4t) & 15) * SC.
 template <int B, int T, bool UNIFORM>
-__device__ __forceinline__ void compute_step(float (&acc)[T][B], const uint4 (&d)[T], const F8Args &a,
-                                             const uint8_t *srow0, uint32_t dpack, int cb, int64_t ch) {
-    float s0 = 0.0f;
-    if (UNIFORM) s0 = e8m0_value(__ldg(srow0 + cb));
+__device__ __forceinline__ void compute_step(typename AccOf<B>::type (&acc)[T][B], const uint4 (&d)[T],
+                                             const F8Args &a, const uint8_t *srow0, uint32_t dpack, int cb,
+                                             int64_t ch) {
+    // scale of row t for this chunk
+    const float s0 = e8m0_value(__ldg(srow0 + cb));
+    auto scale_of = [&](int t) -> float {
+        return UNIFORM ? s0 : e8m0_value(__ldg(srow0 + int64_t((dpack >> (4 * t)) & 15u) * a.SC + cb));
+    };
 #pragma unroll
     for (int q = 0; q < 4; q++) {
-        float xv[B][4];
+        float4 xv[B];
 #pragma unroll
-        for (int v = 0; v < B; v++) {
-            const float4 x4 = __ldg(reinterpret_cast<const float4 *>(a.x + v * a.C + ch * 16 + 4 * q));
-            xv[v][0] = x4.x;
-            xv[v][1] = x4.y;
-            xv[v][2] = x4.z;
-            xv[v][3] = x4.w;
-        }
-        float xs[B][4];
-        if (UNIFORM) {
+        for (int v = 0; v < B; v++)
+            xv[v] = __ldg(reinterpret_cast<const float4 *>(a.x + v * a.C + ch * 16 + 4 * q));
+        if constexpr (B == 1) {
+            float4 xs = make_float4(xv[0].x * s0, xv[0].y * s0, xv[0].z * s0, xv[0].w * s0);
 #pragma unroll
-            for (int v = 0; v < B; v++)
-#pragma unroll
-                for (int k = 0; k < 4; k++) xs[v][k] = xv[v][k] * s0;
-        }
-#pragma unroll
-        for (int t = 0; t < T; t++) {
-            if (!UNIFORM) {
-                const float st = e8m0_value(__ldg(srow0 + int64_t((dpack >> (4 * t)) & 15u) * a.SC + cb));
-#pragma unroll
-                for (int v = 0; v < B; v++)
-#pragma unroll
-                    for (int k = 0; k < 4; k++) xs[v][k] = xv[v][k] * st;
+            for (int t = 0; t < T; t++) {
+                if (!UNIFORM) {
+                    const float st = scale_of(t);
+                    xs = make_float4(xv[0].x * st, xv[0].y * st, xv[0].z * st, xv[0].w * st);
+                }
+                float2 w01, w23;
+                decode_pairs(word_of(d[t], q), w01, w23);
+                acc[t][0] = fmaf(w01.x, xs.x, acc[t][0]);
+                acc[t][0] = fmaf(w01.y, xs.y, acc[t][0]);
+                acc[t][0] = fmaf(w23.x, xs.z, acc[t][0]);
+                acc[t][0] = fmaf(w23.y, xs.w, acc[t][0]);
             }
-            float f[4];
-            decode4(word_of(d[t], q), f);
+        } else {
 #pragma unroll
-            for (int v = 0; v < B; v++) {
-                acc[t][v] = fmaf(f[0], xs[v][0], acc[t][v]);
-                acc[t][v] = fmaf(f[1], xs[v][1], acc[t][v]);
-                acc[t][v] = fmaf(f[2], xs[v][2], acc[t][v]);
-                acc[t][v] = fmaf(f[3], xs[v][3], acc[t][v]);
+            for (int t = 0; t < T; t++) {
+                float2 w01, w23;
+                decode_pairs(word_of(d[t], q), w01, w23);
+                const float st = scale_of(t);
+                const float2 ss = make_float2(st, st);
+                w01 = __fmul2_rn(w01, ss);
+                w23 = __fmul2_rn(w23, ss);
+#pragma unroll
+                for (int v = 0; v < B; v++) {
+                    acc[t][v] = __ffma2_rn(w01, make_float2(xv[v].x, xv[v].y), acc[t][v]);
+                    acc[t][v] = __ffma2_rn(w23, make_float2(xv[v].z, xv[v].w), acc[t][v]);
+                }
             }
         }
     }
+}
+
+// Tile epilogue: reduce each row's sums across the warp (fixed order), fall
+// back to the exact per-element evaluation for rows that came out NaN, store.
+template <int B, int T>
+__device__ __forceinline__ void finish_tile(typename AccOf<B>::type (&acc)[T][B], const F8Args &a, int64_t r0,
+                                            int rows, int lane) {
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+#pragma unroll
+        for (int v = 0; v < B; v++) {
+            float val = warp_sum(acc_total(acc[t][v]));
+            acc_zero(acc[t][v]);
+            if (t < rows) {
+                if (isnan(val)) val = f8_row_exact(a, r0 + t, v, nullptr);
+                if (lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
+            }
+        }
+    }
+}
+
+// Scale rows of a tile: srow0 for its first row and, when the tile spans
+// several scale rows, 4-bit per-row offsets (rows of one tile span at most
+// T + 1 scale rows since SR <= R).
+template <int T>
+__device__ __forceinline__ bool setup_scale(const F8Args &a, int64_t r0, int rows, const uint8_t *&srow0,
+                                            uint32_t &dpack) {
+    static_assert(T <= 8, "per-row scale offsets are packed in 4 bits");
+    const int64_t rb0 = r0 * a.SR / a.R, rb1 = (r0 + rows - 1) * a.SR / a.R;
+    srow0 = a.scale + rb0 * a.SC;
+    dpack = 0;
+    if (rb0 == rb1) return true;
+    for (int t = 1; t < rows; t++) dpack |= uint32_t((r0 + t) * a.SR / a.R - rb0) << (4 * t);
+    return false;
 }
 
 template <int B, int T, bool PF, bool GS>
@@ -233,27 +296,16 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
     uint4 cur[T];
     load_step<T>(cur, a, r0, rows, lane, nchunk);
 
-    float acc[T][B];
+    typename AccOf<B>::type acc[T][B];
 #pragma unroll
     for (int t = 0; t < T; t++)
 #pragma unroll
-        for (int v = 0; v < B; v++) acc[t][v] = 0.0f;
+        for (int v = 0; v < B; v++) acc_zero(acc[t][v]);
 
-    static_assert(T <= 8, "per-row scale deltas are packed in 4 bits");
     const uint8_t *srow0 = a.scale;
     uint32_t dpack = 0;
     bool uniform = true;
-    auto setup_tile = [&]() {
-        // rows of one tile span at most T + 1 scale rows (SR <= R), so each
-        // row's offset from the first fits in 4 bits
-        const int64_t rb0 = r0 * a.SR / a.R, rb1 = (r0 + rows - 1) * a.SR / a.R;
-        uniform = (rb0 == rb1);
-        srow0 = a.scale + rb0 * a.SC;
-        dpack = 0;
-        if (!uniform) {
-            for (int t = 1; t < rows; t++) dpack |= uint32_t((r0 + t) * a.SR / a.R - rb0) << (4 * t);
-        }
-    };
+    auto setup_tile = [&]() { uniform = setup_scale<T>(a, r0, rows, srow0, dpack); };
     setup_tile();
 
     while (true) {
@@ -277,20 +329,7 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
             else
                 compute_step<B, T, false>(acc, cur, a, srow0, dpack, chunk_cb[ch], ch);
         }
-        if (j == iters - 1) {  // tile done: reduce, store, restart the sums
-#pragma unroll
-            for (int t = 0; t < T; t++) {
-#pragma unroll
-                for (int v = 0; v < B; v++) {
-                    float val = warp_sum(acc[t][v]);
-                    acc[t][v] = 0.0f;
-                    if (t < rows) {
-                        if (isnan(val)) val = f8_row_exact(a, r0 + t, v, nullptr);
-                        if (lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
-                    }
-                }
-            }
-        }
+        if (j == iters - 1) finish_tile<B, T>(acc, a, r0, rows, lane);  // tile done
         if (!has_next) break;
         if (PF) {
 #pragma unroll
@@ -306,6 +345,59 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Small-matrix kernel: when the matrix has too few rows to give every warp of
+// a full grid several tiles, each warp takes tiles of T rows and loads all
+// NSTEP chunk steps of them at once (NSTEP * 512 bytes per row in flight),
+// so the whole matrix is requested in about one wave instead of NSTEP
+// dependent round trips per warp.  Same arithmetic and order as the fast
+// kernel.
+// ---------------------------------------------------------------------------
+template <int B, int T, int NSTEP>
+__global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
+    extern __shared__ int chunk_cb[];
+    const int64_t nchunk = a.C >> 4;
+    for (int64_t ch = threadIdx.x; ch < nchunk; ch += blockDim.x)
+        chunk_cb[ch] = int((ch * 16 * a.SC) / a.C);
+    pdl_wait();
+    pdl_trigger();
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    const int64_t ntiles = (a.R + T - 1) / T;
+    typename AccOf<B>::type acc[T][B];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int v = 0; v < B; v++) acc_zero(acc[t][v]);
+
+    for (int64_t tile = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tile < ntiles;
+         tile += nwarps) {
+        const int64_t r0 = tile * T;
+        const int rows = int(min(int64_t(T), a.R - r0));
+        const uint8_t *srow0;
+        uint32_t dpack;
+        const bool uniform = setup_scale<T>(a, r0, rows, srow0, dpack);
+        for (int64_t base = 0; base < nchunk; base += 32 * NSTEP) {
+            uint4 d[NSTEP][T];
+#pragma unroll
+            for (int st = 0; st < NSTEP; st++) load_step<T>(d[st], a, r0, rows, base + lane + 32 * st, nchunk);
+#pragma unroll
+            for (int st = 0; st < NSTEP; st++) {
+                const int64_t ch = base + lane + 32 * st;
+                if (ch < nchunk) {
+                    if (uniform)
+                        compute_step<B, T, true>(acc, d[st], a, srow0, dpack, chunk_cb[ch], ch);
+                    else
+                        compute_step<B, T, false>(acc, d[st], a, srow0, dpack, chunk_cb[ch], ch);
+                }
+            }
+        }
+        finish_tile<B, T>(acc, a, r0, rows, lane);
+    }
+}
+
 // True when every 16-column chunk maps to a single scale block: the first
 // column of each block b, ceil(b*C/SC), is a multiple of 16.
 bool chunks_uniform(int64_t C, int64_t SC) {
@@ -316,12 +408,22 @@ bool chunks_uniform(int64_t C, int64_t SC) {
     return true;
 }
 
-template <int B, int T = (B <= 4) ? 8 : 4, bool PF = false, bool GS = true>
+template <int B, int T = (B <= 2) ? 8 : 4, bool PF = false, bool GS = true>
 qmv_status launch_fast(const F8Args &a, cudaStream_t s) {
     const size_t smem = size_t(a.C >> 4) * sizeof(int);
     auto kern = f8_fast_kernel<B, T, PF, GS>;
     const void *kp = reinterpret_cast<const void *>(kern);
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
+    const int64_t capacity = int64_t(occupancy(kp, 256, smem)) * sm_count() * 8;  // resident warps
+    if ((a.R + T - 1) / T < 4 * capacity) {
+        // too few tiles to keep a full grid streaming: load whole rows at once
+        constexpr int TS = 2, NSTEP = (B <= 2) ? 8 : 4;
+        auto rk = f8_rows_kernel<B, TS, NSTEP>;
+        const void *rp = reinterpret_cast<const void *>(rk);
+        if (!allow_smem(rp, smem)) return QMV_ERR_CUDA;
+        const int blocks = grid_blocks(rp, 256, smem, (a.R + TS - 1) / TS);
+        return from_cuda(launch_pdl(rk, dim3(unsigned(blocks)), dim3(256), smem, s, a));
+    }
     const int blocks = grid_blocks(kp, 256, smem, (a.R + T - 1) / T);
     return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(256), smem, s, a));
 }

@@ -259,6 +259,15 @@ def test_f8_shapes(batch, R, C, SR, SC):
     check_f8(synth.f8_inputs(R + C + SC, R, C, SR, SC, 115, 135, batch=batch))
 
 
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("R,C,SR,SC", [
+    (150001, 32, 7, 2),      # many tiles: the streaming kernel; SR does not divide R
+    (131075, 48, 40000, 3),  # tiles straddle scale rows (up to 1 per 3 rows)
+    (122881, 16, 1, 1)])     # one chunk per row: most lanes idle
+def test_f8_streaming_kernel_shapes(batch, R, C, SR, SC):
+    check_f8(synth.f8_inputs(R + C + batch, R, C, SR, SC, 110, 140, batch=batch))
+
+
 def test_f8_saturated_codes_and_nan_scale():
     f = synth.f8_inputs(77, 500, 4096, 10, 32, 120, 130, batch=2, finite_only=False)
     assert (f.w == 0x7F).any() and (f.w == 0xFF).any()
