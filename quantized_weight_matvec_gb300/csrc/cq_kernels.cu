@@ -360,29 +360,38 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(qmv_cq_matrix m, con
     float n;
     cq2_load<CPR>(d, n, m, rg * RPW + rho, q, g, nG);
 
-    // ---- build the table (one pass per block) ----
+    // ---- build the table (one pass per block): one thread per column pair
+    // (chunk q, pair j) loads p once and writes all 16 nibble entries ----
     {
-        const float c0 = __ldg(m.codebook + 0), c1 = __ldg(m.codebook + 1);
-        const float c2 = __ldg(m.codebook + 2), c3 = __ldg(m.codebook + 3);
-        for (int u = threadIdx.x; u < 16 * CPR * 32; u += blockDim.x) {
-            const int nib = u / (CPR * 32);
-            const int rest = u - nib * (CPR * 32);
-            const int qq = rest >> 5, j = rest & 31;
-            const int lo = nib & 3, hi = nib >> 2;
-            const float cl = lo == 0 ? c0 : lo == 1 ? c1 : lo == 2 ? c2 : c3;
-            const float chv = hi == 0 ? c0 : hi == 1 ? c1 : hi == 2 ? c2 : c3;
+        float cb[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) cb[i] = __ldg(m.codebook + i);
+        for (int u = threadIdx.x; u < CPR * 32; u += blockDim.x) {
+            const int qq = u >> 5, j = u & 31;
             const int col = qq * 64 + 2 * j;
-            const float v = fmaf(chv, __ldg(p + col + 1), cl * __ldg(p + col));
+            const float p0 = __ldg(p + col), p1 = __ldg(p + col + 1);
+            float lo_prod[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) lo_prod[i] = cb[i] * p0;
             const int slot = (j + RPW * qq) & 31;
-            float *blk = table + (nib * NIB_STRIDE + qq * 256) / 4;
-            blk[slot] = v;
-            blk[slot + 32] = v;
+            float *blk = table + (qq * 256) / 4 + slot;
+#pragma unroll
+            for (int hi = 0; hi < 4; hi++) {
+#pragma unroll
+                for (int lo = 0; lo < 4; lo++) {
+                    const float v = fmaf(cb[hi], p1, lo_prod[lo]);
+                    float *e = blk + (lo | (hi << 2)) * (NIB_STRIDE / 4);
+                    e[0] = v;
+                    e[32] = v;
+                }
+            }
         }
     }
     __syncthreads();
 
-    const unsigned lane_part = unsigned(q * 256 + 4 * (rho + RPW * q));
-    const unsigned tbase = unsigned(__cvta_generic_to_shared(table_raw));
+    // per-lane part of every table address (shared-window base included)
+    const unsigned lane_base = unsigned(__cvta_generic_to_shared(table_raw)) +
+                               unsigned(q * 256 + 4 * (rho + RPW * q));
     const unsigned sh = 4u * unsigned(rho);
 
     for (; rg < ngroups_rows; rg += nwarps) {
@@ -391,23 +400,31 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(qmv_cq_matrix m, con
         uint4 dn;
         float nn;
         cq2_load<CPR>(dn, nn, m, (rg + nwarps) * RPW + rho, q, g, nG);
-        // rotate the 128-bit chunk right by 4*rho bits
+        // rotate the 128-bit chunk right by 4*rho bits, then split every word
+        // into its even nibbles (one per byte) and its odd nibbles
         unsigned w[4];
         w[0] = __funnelshift_r(d.x, d.y, sh);
         w[1] = __funnelshift_r(d.y, d.z, sh);
         w[2] = __funnelshift_r(d.z, d.w, sh);
         w[3] = __funnelshift_r(d.w, d.x, sh);
-        float part = 0.0f;
+        float part0 = 0.0f, part1 = 0.0f;
 #pragma unroll
-        for (int t = 0; t < 32; t++) {
-            const unsigned word = w[t >> 3];
-            const int pos = 4 * (t & 7);
-            unsigned nb = (pos >= LG_NIB) ? (word >> (pos - LG_NIB)) : (word << (LG_NIB - pos));
-            const unsigned addr = tbase + ((nb & (15u << LG_NIB)) | lane_part) + 4u * t;
-            float tv;
-            asm("ld.shared.f32 %0, [%1];" : "=f"(tv) : "r"(addr));
-            part += tv;
+        for (int i = 0; i < 4; i++) {
+            const unsigned ev = w[i] & 0x0f0f0f0fu, od = (w[i] >> 4) & 0x0f0f0f0fu;
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                const int t = 8 * i + k;
+                const unsigned nib = __byte_perm((k & 1) ? od : ev, 0u, 0x4440u | unsigned(k >> 1));
+                const unsigned addr = nib * unsigned(NIB_STRIDE) + lane_base + 4u * unsigned(t);
+                float tv;
+                asm("ld.shared.f32 %0, [%1];" : "=f"(tv) : "r"(addr));
+                if (k & 1)
+                    part1 += tv;
+                else
+                    part0 += tv;
+            }
         }
+        const float part = part0 + part1;
         float acc = n * part;
 #pragma unroll
         for (int dd = CPR / 2; dd >= 1; dd >>= 1) acc += __shfl_xor_sync(kFull, acc, dd);
