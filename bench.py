@@ -585,6 +585,20 @@ def run_configs(args):
                     calls = calls * 8
                 med, best = _graph_time(torch, calls, reps=10)
                 emit(name, batch, "f8_matvec", nb, med, best, k)
+                # head + greedy selection (no logits stored)
+                wsp = torch.empty(qmv.f8_argmax_workspace_bytes(batch), dtype=torch.uint8,
+                                  device=dev)
+                oi = torch.empty(batch, dtype=torch.int64, device=dev)
+                ov = torch.empty(batch, device=dev)
+                acalls = [(lambda wi: lambda sh: qmv.f8_matvec_argmax(
+                    wi.data_ptr(), f.R, f.C, s5.data_ptr(), f.SR, f.SC, x.data_ptr(), batch, 0,
+                    oi.data_ptr(), ov.data_ptr(), wsp.data_ptr(), wsp.numel(), sh))(wi)
+                    for wi in ws]
+                if k == 1:
+                    acalls = acalls * 8
+                med, best = _graph_time(torch, acalls, reps=10)
+                emit(name, batch, "f8_matvec_argmax", nb - 4 * batch * f.R + 12 * batch, med,
+                     best, k)
                 del ws, w
 
 

@@ -175,6 +175,41 @@ QMV_API qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8
                      int64_t SR, int64_t SC, const float *x, int32_t batch, float *y,
                      qmv_stream stream);
 
+/* Bytes of device workspace f8_matvec_argmax needs for `batch` vectors: one
+ * (value, row) partial result per block and vector, for at most
+ * QMV_ARGMAX_MAX_BLOCKS blocks. */
+#define QMV_ARGMAX_MAX_BLOCKS 2048
+#define QMV_F8_ARGMAX_WORKSPACE_BYTES(batch) ((int64_t)QMV_ARGMAX_MAX_BLOCKS * (int64_t)(batch) * 16)
+
+/*
+ * f8_matvec_argmax -- the head matvec followed by greedy selection, fused.
+ * ds4f-disk issue #6, work item 3 ("logits = head x state" then sampling;
+ * the head is the single biggest matvec) and step 3 (head.c: F8_E4M3 +
+ * E8M0 head logits and a deterministic sampler); greedy selection is the
+ * sampler at temperature zero.
+ *
+ * Computes y = f8_matvec(w, scale, x) exactly as f8_matvec does, then for
+ * each vector v the row index r that maximises y[v][r].  Order: NaN is
+ * greater than every number (as numpy/torch argmax); among equal values
+ * (and among NaNs) the lowest row wins.  The choice is made on the float32
+ * values this call computes, so it is always the argmax of the y this call
+ * writes.
+ *
+ *   y          [batch, R] float32, written when non-NULL (else not stored)
+ *   out_index  [batch] int64, written
+ *   out_value  [batch] float32, written (y[v][out_index[v]])
+ *   workspace  device scratch of workspace_bytes >=
+ *              QMV_F8_ARGMAX_WORKSPACE_BYTES(batch), 16-byte aligned,
+ *              caller-owned; its contents on entry are ignored and on exit
+ *              are unspecified.  Calls that overlap on the GPU must not share
+ *              a workspace.
+ * R >= 1.  Other arguments and errors as f8_matvec.
+ */
+QMV_API qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                                    int64_t SR, int64_t SC, const float *x, int32_t batch, float *y,
+                                    int64_t *out_index, float *out_value, void *workspace,
+                                    int64_t workspace_bytes, qmv_stream stream);
+
 /* Human-readable name of a status code (static storage). */
 QMV_API const char *qmv_status_string(qmv_status status);
 

@@ -15,7 +15,8 @@ Every function cites the page section it follows:
 * ``needle-1`` -- needle.js tutorial "Inference engine, part 1: loader and
   tokenizer": section 3 (FP16 decode) and section 4 (CqMatrix).
 * ``ds4f-6`` -- ds4f-disk issue #6 "attention + tokenizer + sampling",
-  work item 1 / step 1 (F8 E4M3 + E8M0 block-scaled matvec).
+  work item 1 / step 1 (F8 E4M3 + E8M0 block-scaled matvec), work item 3 /
+  step 3 (head logits then sampling: greedy selection).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against values the pages fix, closed forms, library routines (numpy float16,
@@ -84,6 +85,8 @@ def _load():
     lib.orc_f8_matvec_mt.argtypes = [P, I64, I64, P, I64, I64, P, I64, P, P, I64, I64,
                                      ctypes.c_int]
     lib.orc_f8_matvec_mt.restype = ctypes.c_int
+    lib.orc_argmax_f32.argtypes = [P, I64]
+    lib.orc_argmax_f32.restype = I64
     _lib = lib
     return lib
 
@@ -244,3 +247,12 @@ def f8_matvec(w, scale, x, rows=None, threads: int = 1, with_mag: bool = True):
     else:
         lib.orc_f8_matvec(*args)
     return y, mag
+
+
+def argmax_rows(y) -> np.ndarray:
+    """Greedy selection per row of y [batch, n] float32 (ds4f-6 work item 3 /
+    step 3): NaN above every number, then the larger value, then the lower
+    index.  Returns int64 [batch]."""
+    y = _c(np.atleast_2d(y), np.float32)
+    lib = _load()
+    return np.array([lib.orc_argmax_f32(_ptr(row), row.size) for row in y], dtype=np.int64)

@@ -278,6 +278,30 @@ ORC_API int orc_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t 
 }
 
 /* ------------------------------------------------------------------------ */
+/* Greedy selection over one vector of head outputs (ds4f-6 work item 3 and  */
+/* step 3: logits = head x state, then sampling; greedy = temperature 0).    */
+/* Order: NaN above every number, larger above smaller, then the lower       */
+/* index.  Returns -1 for n == 0.                                            */
+/* ------------------------------------------------------------------------ */
+
+ORC_API int64_t orc_argmax_f32(const float *y, int64_t n)
+{
+    int64_t best = -1;
+    for (int64_t i = 0; i < n; i++) {
+        if (best < 0) {
+            best = i;
+            continue;
+        }
+        int i_nan = isnan(y[i]), b_nan = isnan(y[best]);
+        if (b_nan)
+            continue; /* an earlier NaN is never beaten */
+        if (i_nan || y[i] > y[best])
+            best = i;
+    }
+    return best;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Row-range threading for timing the oracle on many host cores.  Each       */
 /* thread runs the single-threaded function above on its own row range.      */
 /* ------------------------------------------------------------------------ */

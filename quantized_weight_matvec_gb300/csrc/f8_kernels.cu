@@ -24,13 +24,82 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// One partial argmax result: the best (value, row) a block found for a vector.
+struct ArgBest {
+    float v;
+    int32_t pad;
+    int64_t i;
+};
+
 struct F8Args {
     const uint8_t *w;
     const uint8_t *scale;
     const float *x;
-    float *y;
+    float *y;  // may be NULL for the argmax variant (then not stored)
     int64_t R, C, SR, SC;
+    ArgBest *ws;  // argmax variant: [gridDim.x, B] partial results
 };
+
+// Total order of the greedy choice: NaN above every number (as numpy and
+// torch argmax), larger values above smaller, then the lower row.
+__device__ __forceinline__ bool arg_better(float av, int64_t ai, float bv, int64_t bi) {
+    const bool an = isnan(av), bn = isnan(bv);
+    if (an != bn) return an;
+    if (!an && av != bv) return av > bv;
+    return ai < bi;
+}
+
+// Per-warp running best for each vector (every lane holds the same values).
+template <int B>
+struct WarpBest {
+    float v[B];
+    int64_t i[B];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int k = 0; k < B; k++) {
+            v[k] = -INFINITY;
+            i[k] = INT64_MAX;
+        }
+    }
+    __device__ __forceinline__ void offer(int k, float val, int64_t row) {
+        if (arg_better(val, row, v[k], i[k])) {
+            v[k] = val;
+            i[k] = row;
+        }
+    }
+};
+
+// Block-level reduction of the warps' bests, written to ws[blockIdx.x * B + k].
+// Every thread of the block must call it.
+template <int B>
+__device__ __forceinline__ void block_best_store(const WarpBest<B> &wb, ArgBest *ws) {
+    __shared__ float sv[32][B];
+    __shared__ int64_t si[32][B];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < B; k++) {
+            sv[warp][k] = wb.v[k];
+            si[warp][k] = wb.i[k];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < B) {
+        const int k = threadIdx.x;
+        float bv = sv[0][k];
+        int64_t bi = si[0][k];
+        for (int w2 = 1; w2 < nw; w2++)
+            if (arg_better(sv[w2][k], si[w2][k], bv, bi)) {
+                bv = sv[w2][k];
+                bi = si[w2][k];
+            }
+        ArgBest r;
+        r.v = bv;
+        r.pad = 0;
+        r.i = bi;
+        ws[int64_t(blockIdx.x) * B + k] = r;
+    }
+}
 
 // E4M3 byte -> float32 from its fields, with the saturation at 448 (so the
 // codes 0x7F / 0xFF, NaN in the OCP "fn" variant, read as +/-448).
@@ -80,7 +149,7 @@ __device__ float f8_row_exact(const F8Args &a, int64_t r, int v, const float *lu
 // General kernel: any C, any scale blocking, any alignment.  One warp per
 // row, a shared-memory table of the 256 exact E4M3 values.
 // ---------------------------------------------------------------------------
-template <int B>
+template <int B, bool AM>
 __global__ void __launch_bounds__(256) f8_general_kernel(F8Args a) {
     __shared__ float lut[256];
     lut[threadIdx.x] = e4m3_exact(threadIdx.x);
@@ -89,13 +158,17 @@ __global__ void __launch_bounds__(256) f8_general_kernel(F8Args a) {
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    WarpBest<B> best;
+    best.init();
     for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < a.R; r += nwarps) {
-#pragma unroll 1
+#pragma unroll
         for (int v = 0; v < B; v++) {
             const float val = f8_row_exact(a, r, v, lut);
-            if (lane == 0) a.y[int64_t(v) * a.R + r] = val;
+            if (AM) best.offer(v, val, r);
+            if (lane == 0 && (!AM || a.y)) a.y[int64_t(v) * a.R + r] = val;
         }
     }
+    if (AM) block_best_store<B>(best, a.ws);
 }
 
 // ---------------------------------------------------------------------------
@@ -237,9 +310,9 @@ __device__ __forceinline__ void compute_step(typename AccOf<B>::type (&acc)[T][B
 
 // Tile epilogue: reduce each row's sums across the warp (fixed order), fall
 // back to the exact per-element evaluation for rows that came out NaN, store.
-template <int B, int T>
+template <int B, int T, bool AM>
 __device__ __forceinline__ void finish_tile(typename AccOf<B>::type (&acc)[T][B], const F8Args &a, int64_t r0,
-                                            int rows, int lane) {
+                                            int rows, int lane, WarpBest<B> &best) {
 #pragma unroll
     for (int t = 0; t < T; t++) {
 #pragma unroll
@@ -248,7 +321,8 @@ __device__ __forceinline__ void finish_tile(typename AccOf<B>::type (&acc)[T][B]
             acc_zero(acc[t][v]);
             if (t < rows) {
                 if (isnan(val)) val = f8_row_exact(a, r0 + t, v, nullptr);
-                if (lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
+                if (AM) best.offer(v, val, r0 + t);
+                if (lane == 0 && (!AM || a.y)) a.y[int64_t(v) * a.R + r0 + t] = val;
             }
         }
     }
@@ -269,7 +343,7 @@ __device__ __forceinline__ bool setup_scale(const F8Args &a, int64_t r0, int row
     return false;
 }
 
-template <int B, int T, bool PF, bool GS>
+template <int B, int T, bool PF, bool GS, bool AM>
 __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
     extern __shared__ int chunk_cb[];
     const int64_t nchunk = a.C >> 4;
@@ -288,7 +362,9 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
     const int64_t row_end = GS ? a.R : a.R * (wid + 1) / nwarps;
     int64_t r0 = GS ? wid * T : a.R * wid / nwarps;
     const int64_t tile_stride = GS ? nwarps * T : T;
-    if (r0 >= row_end) return;
+    WarpBest<B> best;
+    best.init();
+    if (r0 < row_end) {  // (no early return: the argmax epilogue has a barrier)
     const int iters = int((nchunk + 31) >> 5);
 
     int rows = int(min(int64_t(T), row_end - r0));
@@ -329,7 +405,7 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
             else
                 compute_step<B, T, false>(acc, cur, a, srow0, dpack, chunk_cb[ch], ch);
         }
-        if (j == iters - 1) finish_tile<B, T>(acc, a, r0, rows, lane);  // tile done
+        if (j == iters - 1) finish_tile<B, T, AM>(acc, a, r0, rows, lane, best);  // tile done
         if (!has_next) break;
         if (PF) {
 #pragma unroll
@@ -343,6 +419,8 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
         rows = rowsn;
         if (new_tile) setup_tile();
     }
+    }
+    if (AM) block_best_store<B>(best, a.ws);
 }
 
 // ---------------------------------------------------------------------------
@@ -353,7 +431,7 @@ __global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
 // dependent round trips per warp.  Same arithmetic and order as the fast
 // kernel.
 // ---------------------------------------------------------------------------
-template <int B, int T, int NSTEP>
+template <int B, int T, int NSTEP, bool AM>
 __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
     extern __shared__ int chunk_cb[];
     const int64_t nchunk = a.C >> 4;
@@ -372,6 +450,8 @@ __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
 #pragma unroll
         for (int v = 0; v < B; v++) acc_zero(acc[t][v]);
 
+    WarpBest<B> best;
+    best.init();
     for (int64_t tile = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tile < ntiles;
          tile += nwarps) {
         const int64_t r0 = tile * T;
@@ -394,7 +474,44 @@ __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
                 }
             }
         }
-        finish_tile<B, T>(acc, a, r0, rows, lane);
+        finish_tile<B, T, AM>(acc, a, r0, rows, lane, best);
+    }
+    if (AM) block_best_store<B>(best, a.ws);
+}
+
+// Final pass of the argmax: one block reduces the [nblocks, B] partials.
+__global__ void __launch_bounds__(256) argmax_reduce_kernel(const ArgBest *ws, int nblocks, int B,
+                                                            int64_t *out_index, float *out_value) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ float sv[256];
+    __shared__ int64_t si[256];
+    for (int k = 0; k < B; k++) {
+        float bv = -INFINITY;
+        int64_t bi = INT64_MAX;
+        for (int b = threadIdx.x; b < nblocks; b += blockDim.x) {
+            const ArgBest e = ws[int64_t(b) * B + k];
+            if (arg_better(e.v, e.i, bv, bi)) {
+                bv = e.v;
+                bi = e.i;
+            }
+        }
+        sv[threadIdx.x] = bv;
+        si[threadIdx.x] = bi;
+        __syncthreads();
+        for (int st = blockDim.x / 2; st > 0; st >>= 1) {
+            if (threadIdx.x < st && arg_better(sv[threadIdx.x + st], si[threadIdx.x + st], sv[threadIdx.x],
+                                               si[threadIdx.x])) {
+                sv[threadIdx.x] = sv[threadIdx.x + st];
+                si[threadIdx.x] = si[threadIdx.x + st];
+            }
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) {
+            out_index[k] = si[0];
+            out_value[k] = sv[0];
+        }
+        __syncthreads();
     }
 }
 
@@ -408,62 +525,89 @@ bool chunks_uniform(int64_t C, int64_t SC) {
     return true;
 }
 
-template <int B, int T = (B <= 2) ? 8 : 4, bool PF = false, bool GS = true>
-qmv_status launch_fast(const F8Args &a, cudaStream_t s) {
+template <int B, bool AM, int T = (B <= 2) ? 8 : 4, bool PF = false, bool GS = true>
+qmv_status launch_fast(const F8Args &a, cudaStream_t s, int &blocks_out) {
     const size_t smem = size_t(a.C >> 4) * sizeof(int);
-    auto kern = f8_fast_kernel<B, T, PF, GS>;
+    auto kern = f8_fast_kernel<B, T, PF, GS, AM>;
     const void *kp = reinterpret_cast<const void *>(kern);
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
     const int64_t capacity = int64_t(occupancy(kp, 256, smem)) * sm_count() * 8;  // resident warps
+    int blocks;
+    cudaError_t e;
     if ((a.R + T - 1) / T < 4 * capacity) {
         // too few tiles to keep a full grid streaming: load whole rows at once
         constexpr int TS = 2, NSTEP = (B <= 2) ? 8 : 4;
-        auto rk = f8_rows_kernel<B, TS, NSTEP>;
+        auto rk = f8_rows_kernel<B, TS, NSTEP, AM>;
         const void *rp = reinterpret_cast<const void *>(rk);
         if (!allow_smem(rp, smem)) return QMV_ERR_CUDA;
-        const int blocks = grid_blocks(rp, 256, smem, (a.R + TS - 1) / TS);
-        return from_cuda(launch_pdl(rk, dim3(unsigned(blocks)), dim3(256), smem, s, a));
+        blocks = grid_blocks(rp, 256, smem, (a.R + TS - 1) / TS);
+        if (AM && blocks > QMV_ARGMAX_MAX_BLOCKS) blocks = QMV_ARGMAX_MAX_BLOCKS;
+        e = launch_pdl(rk, dim3(unsigned(blocks)), dim3(256), smem, s, a);
+    } else {
+        blocks = grid_blocks(kp, 256, smem, (a.R + T - 1) / T);
+        if (AM && blocks > QMV_ARGMAX_MAX_BLOCKS) blocks = QMV_ARGMAX_MAX_BLOCKS;
+        e = launch_pdl(kern, dim3(unsigned(blocks)), dim3(256), smem, s, a);
     }
-    const int blocks = grid_blocks(kp, 256, smem, (a.R + T - 1) / T);
-    return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(256), smem, s, a));
+    blocks_out = blocks;
+    return from_cuda(e);
 }
 
-template <int B>
-qmv_status launch_general(const F8Args &a, cudaStream_t s) {
-    const int blocks = grid_blocks(reinterpret_cast<const void *>(f8_general_kernel<B>), 256, 0, a.R);
-    return from_cuda(launch_pdl(f8_general_kernel<B>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
+template <int B, bool AM>
+qmv_status launch_general(const F8Args &a, cudaStream_t s, int &blocks_out) {
+    const void *kp = reinterpret_cast<const void *>(f8_general_kernel<B, AM>);
+    int blocks = grid_blocks(kp, 256, 0, a.R);
+    if (AM && blocks > QMV_ARGMAX_MAX_BLOCKS) blocks = QMV_ARGMAX_MAX_BLOCKS;
+    blocks_out = blocks;
+    return from_cuda(launch_pdl(f8_general_kernel<B, AM>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
+}
+
+template <bool AM>
+qmv_status launch_any(const F8Args &a, int batch, cudaStream_t s, int &blocks) {
+    const bool fast = (a.C % 16 == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) && (a.C / 16) * 4 <= 200 * 1024 &&
+                      chunks_uniform(a.C, a.SC);
+    if (fast) {
+        switch (batch) {
+            case 1: return launch_fast<1, AM>(a, s, blocks);
+            case 2: return launch_fast<2, AM>(a, s, blocks);
+            case 3: return launch_fast<3, AM>(a, s, blocks);
+            case 4: return launch_fast<4, AM>(a, s, blocks);
+            case 5: return launch_fast<5, AM>(a, s, blocks);
+            case 6: return launch_fast<6, AM>(a, s, blocks);
+            case 7: return launch_fast<7, AM>(a, s, blocks);
+            default: return launch_fast<8, AM>(a, s, blocks);
+        }
+    }
+    switch (batch) {
+        case 1: return launch_general<1, AM>(a, s, blocks);
+        case 2: return launch_general<2, AM>(a, s, blocks);
+        case 3: return launch_general<3, AM>(a, s, blocks);
+        case 4: return launch_general<4, AM>(a, s, blocks);
+        case 5: return launch_general<5, AM>(a, s, blocks);
+        case 6: return launch_general<6, AM>(a, s, blocks);
+        case 7: return launch_general<7, AM>(a, s, blocks);
+        default: return launch_general<8, AM>(a, s, blocks);
+    }
 }
 
 }  // namespace
 
 qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
                             int64_t SC, const float *x, int batch, float *y, cudaStream_t s) {
-    F8Args a{w, scale, x, y, R, C, SR, SC};
-    const bool fast = (C % 16 == 0) && (reinterpret_cast<uintptr_t>(w) % 16 == 0) &&
-                      (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (C / 16) * 4 <= 200 * 1024 &&
-                      chunks_uniform(C, SC);
-    if (fast) {
-        switch (batch) {
-            case 1: return launch_fast<1>(a, s);
-            case 2: return launch_fast<2>(a, s);
-            case 3: return launch_fast<3>(a, s);
-            case 4: return launch_fast<4>(a, s);
-            case 5: return launch_fast<5>(a, s);
-            case 6: return launch_fast<6>(a, s);
-            case 7: return launch_fast<7>(a, s);
-            default: return launch_fast<8>(a, s);
-        }
-    }
-    switch (batch) {
-        case 1: return launch_general<1>(a, s);
-        case 2: return launch_general<2>(a, s);
-        case 3: return launch_general<3>(a, s);
-        case 4: return launch_general<4>(a, s);
-        case 5: return launch_general<5>(a, s);
-        case 6: return launch_general<6>(a, s);
-        case 7: return launch_general<7>(a, s);
-        default: return launch_general<8>(a, s);
-    }
+    F8Args a{w, scale, x, y, R, C, SR, SC, nullptr};
+    int blocks = 0;
+    return launch_any<false>(a, batch, s, blocks);
+}
+
+qmv_status launch_f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
+                                   int64_t SC, const float *x, int batch, float *y, int64_t *out_index,
+                                   float *out_value, void *workspace, cudaStream_t s) {
+    F8Args a{w, scale, x, y, R, C, SR, SC, reinterpret_cast<ArgBest *>(workspace)};
+    int blocks = 0;
+    qmv_status st = launch_any<true>(a, batch, s, blocks);
+    if (st != QMV_OK) return st;
+    return from_cuda(launch_pdl(argmax_reduce_kernel, dim3(1), dim3(256), 0, s,
+                                static_cast<const ArgBest *>(a.ws), blocks, batch, out_index, out_value));
 }
 
 }  // namespace qmv

@@ -222,6 +222,39 @@ qmv_status cq_dequantize_row(const qmv_cq_matrix *m, const int32_t *rows, int64_
                                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
+                            int64_t SC, const float *x, int32_t batch, float *y, int64_t *out_index,
+                            float *out_value, void *workspace, int64_t workspace_bytes,
+                            qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (R < 1 || R > kMaxDim || C < 1 || C > kMaxDim) return QMV_ERR_SHAPE;
+    if (SR < 1 || SR > R || SC < 1 || SC > C) return QMV_ERR_SHAPE;
+    int64_t wb = 0, sb = 0, xb = 0, yb = 0, t = 0;
+    if (!mul_ok(R, C, &wb) || !mul_ok(SR, SC, &sb) || !mul_ok(int64_t(batch) * 4, C, &xb) ||
+        !mul_ok(int64_t(batch) * 4, R, &yb) || !mul_ok(R, SR, &t) || !mul_ok(C, SC, &t))
+        return QMV_ERR_OVERFLOW;
+    if (!w || !scale || !x || !out_index || !out_value || !workspace) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(y, 4) || !aligned(out_index, 8) || !aligned(out_value, 4) ||
+        !aligned(workspace, 16))
+        return QMV_ERR_ALIGN;
+    if (workspace_bytes < QMV_F8_ARGMAX_WORKSPACE_BYTES(batch)) return QMV_ERR_SHAPE;
+    const int64_t ib = int64_t(batch) * 8, vb = int64_t(batch) * 4, kb = workspace_bytes;
+    // every output (and the workspace) apart from every input and each other
+    const void *outs[4] = {y, out_index, out_value, workspace};
+    const int64_t outb[4] = {y ? yb : 0, ib, vb, kb};
+    const void *ins[3] = {w, scale, x};
+    const int64_t inb[3] = {wb, sb, xb};
+    for (int i = 0; i < 4; i++) {
+        for (int j = 0; j < 3; j++)
+            if (overlaps(outs[i], outb[i], ins[j], inb[j])) return QMV_ERR_ALIAS;
+        for (int j = i + 1; j < 4; j++)
+            if (overlaps(outs[i], outb[i], outs[j], outb[j])) return QMV_ERR_ALIAS;
+    }
+    return qmv::launch_f8_matvec_argmax(w, R, C, scale, SR, SC, x, batch, y, out_index, out_value,
+                                        workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
                      int64_t SC, const float *x, int32_t batch, float *y, qmv_stream stream) {
     qmv_status st = check_batch(batch);

@@ -73,5 +73,9 @@ qmv_status launch_cq_matvec(const qmv_cq_matrix &m, const float *prepared, int b
 qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                             int64_t SR, int64_t SC, const float *x, int batch, float *y,
                             cudaStream_t s);
+qmv_status launch_f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                                   int64_t SR, int64_t SC, const float *x, int batch, float *y,
+                                   int64_t *out_index, float *out_value, void *workspace,
+                                   cudaStream_t s);
 
 }  // namespace qmv

@@ -23,6 +23,12 @@ STATUS_NAMES = {0: "QMV_OK", 1: "QMV_ERR_NULL", 2: "QMV_ERR_SHAPE", 3: "QMV_ERR_
                 10: "QMV_ERR_ROW_ID"}
 MAX_BATCH = 8
 MAX_GROUP = 32768
+ARGMAX_MAX_BLOCKS = 2048
+
+
+def f8_argmax_workspace_bytes(batch: int) -> int:
+    """QMV_F8_ARGMAX_WORKSPACE_BYTES(batch)."""
+    return ARGMAX_MAX_BLOCKS * int(batch) * 16
 
 
 class QmvError(RuntimeError):
@@ -67,7 +73,9 @@ def load() -> ctypes.CDLL:
     lib.cq_matvec.argtypes = [CQP, P, I32, P, P]
     lib.cq_dequantize_row.argtypes = [CQP, P, I64, P, P, P]
     lib.f8_matvec.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P]
-    for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.f8_matvec):
+    lib.f8_matvec_argmax.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P, I64, P]
+    for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.f8_matvec,
+               lib.f8_matvec_argmax):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
     lib.qmv_status_string.restype = ctypes.c_char_p
@@ -114,6 +122,14 @@ def f8_matvec(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: int, batc
               stream: int = 0) -> int:
     return load().f8_matvec(w or None, R, C, scale or None, SR, SC, x or None, batch, y or None,
                             stream or None)
+
+
+def f8_matvec_argmax(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: int, batch: int,
+                     y: int, out_index: int, out_value: int, workspace: int, workspace_bytes: int,
+                     stream: int = 0) -> int:
+    return load().f8_matvec_argmax(w or None, R, C, scale or None, SR, SC, x or None, batch,
+                                   y or None, out_index or None, out_value or None,
+                                   workspace or None, workspace_bytes, stream or None)
 
 
 # --------------------------------------------------------------------------
@@ -233,3 +249,29 @@ def f8_matvec_t(w, scale, x, out=None, stream=None):
     _check(f8_matvec(w.data_ptr(), R, C, scale.data_ptr(), SR, SC, x.data_ptr(), batch,
                      out.data_ptr(), _stream(stream)), "f8_matvec")
     return out
+
+
+def f8_matvec_argmax_t(w, scale, x, y=None, workspace=None, stream=None):
+    """(index[B] int64, value[B] float32) of the row maximising y = f8_matvec(...).
+
+    ``y`` (optional) receives the full [B, R] result; ``workspace`` (optional)
+    is a uint8 CUDA tensor of at least f8_argmax_workspace_bytes(B) bytes."""
+    torch = _torch()
+    w = _dev(w, torch.uint8, "w")
+    scale = _dev(scale, torch.uint8, "scale")
+    x = _dev(x, torch.float32, "x")
+    R, C = w.shape
+    SR, SC = scale.shape
+    batch = x.shape[0] if x.dim() == 2 else 1
+    if workspace is None:
+        workspace = torch.empty(f8_argmax_workspace_bytes(batch), dtype=torch.uint8, device=w.device)
+    _dev(workspace, torch.uint8, "workspace")
+    idx = torch.empty(batch, dtype=torch.int64, device=w.device)
+    val = torch.empty(batch, dtype=torch.float32, device=w.device)
+    yp = 0
+    if y is not None:
+        yp = _dev(y, torch.float32, "y").data_ptr()
+    _check(f8_matvec_argmax(w.data_ptr(), R, C, scale.data_ptr(), SR, SC, x.data_ptr(), batch, yp,
+                            idx.data_ptr(), val.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                            _stream(stream)), "f8_matvec_argmax")
+    return idx, val

@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_four_entry_points():
     names = declared_functions()
-    for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec",
+    for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec", "f8_matvec_argmax",
               "qmv_status_string", "qmv_abi_version"):
         assert n in names
 
@@ -114,3 +114,20 @@ def test_f8_rejections():
     assert qmv.f8_matvec(W, 16, 16, S, 1, 1, X, 1, W + 8) == 8
     assert qmv.f8_matvec(W, 16, 16, S, 1, 1, X, 1, X + 16) == 8
     assert qmv.f8_matvec(W, 0, 16, S, 1, 1, X, 1, 0) == 0  # R = 0: nothing to do
+
+
+def test_f8_argmax_rejections():
+    W, S, X, Y = FAKE, FAKE + (1 << 30), FAKE + (1 << 31), FAKE + (1 << 32)
+    I, V, K = FAKE + (1 << 33), FAKE + (1 << 34), FAKE + (1 << 35)
+    need = qmv.f8_argmax_workspace_bytes(2)
+    assert need == 2048 * 2 * 16
+    a = qmv.f8_matvec_argmax
+    assert a(W, 0, 16, S, 1, 1, X, 2, Y, I, V, K, need) == 2          # R >= 1
+    assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, K, need - 1) == 2     # workspace too small
+    assert a(W, 16, 16, S, 1, 1, X, 2, Y, 0, V, K, need) == 1         # out_index NULL
+    assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, 0, need) == 1         # workspace NULL
+    assert a(W, 16, 16, S, 1, 1, X, 2, Y, I + 4, V, K, need) == 6     # int64 alignment
+    assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, K + 8, need) == 6     # workspace alignment
+    assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, W, need) == 8         # workspace over weights
+    assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, Y + 4, K, need) == 8     # value inside y
+    assert a(W, 16, 16, S, 1, 1, X, 9, Y, I, V, K, need) == 5

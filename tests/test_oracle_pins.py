@@ -378,3 +378,25 @@ def test_threaded_oracle_equals_single_threaded():
     c, m = _cq(3, output=50)
     p = oracle.cq_prepare(c.x, c.input_padded, c.group)
     assert np.array_equal(m.matvec(p)[0], m.matvec(p, threads=3)[0])
+
+
+# ---------------------------------------------------------------------------
+# greedy selection over head outputs
+# ---------------------------------------------------------------------------
+
+def test_argmax_matches_numpy_including_ties_and_nans():
+    rng = np.random.default_rng(21)
+    for trial in range(200):
+        n = int(rng.integers(1, 60))
+        y = rng.integers(-3, 4, n).astype(np.float32)  # many ties
+        if trial % 3 == 0:
+            y[rng.integers(0, n, 2)] = np.nan
+        if trial % 5 == 0:
+            y[:] = -np.inf
+        assert oracle.argmax_rows(y)[0] == np.argmax(y)  # numpy: first NaN, first max
+
+
+def test_argmax_hand_cases():
+    assert list(oracle.argmax_rows(np.array([[1, 3, 3, 2], [np.nan, 5, np.nan, 9]],
+                                            np.float32))) == [1, 0]
+    assert oracle.argmax_rows(np.array([[-np.inf, -np.inf]], np.float32))[0] == 0
