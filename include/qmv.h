@@ -210,6 +210,29 @@ QMV_API qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, cons
                                     int64_t *out_index, float *out_value, void *workspace,
                                     int64_t workspace_bytes, qmv_stream stream);
 
+/*
+ * f8_matvec_argmax_noalloc -- f8_matvec_argmax without a caller workspace.
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory, for example an engine whose
+ * memory pool owns the whole device and forbids further cudaMalloc, or a
+ * plug-in interface that hands over inputs and outputs but no workspace.
+ *
+ * Same arguments, results and errors as f8_matvec_argmax, minus the
+ * workspace: the scratch is a fixed 256 KiB array inside the library (one
+ * per GPU, held until the process exits), enough for batch <= QMV_MAX_BATCH;
+ * anything beyond that returns QMV_ERR_BATCH.  The call allocates nothing.
+ * Its first call on each device looks up that array's device address (with
+ * the device current), so make that first call before any stream capture.
+ * Every call uses the same array: calls that may run at the same time on the
+ * GPU (for example on two streams) race and must be ordered by the caller.
+ * The array's previous contents never matter.
+ */
+QMV_API qmv_status f8_matvec_argmax_noalloc(const uint8_t *w, int64_t R, int64_t C,
+                                            const uint8_t *scale, int64_t SR, int64_t SC,
+                                            const float *x, int32_t batch, float *y,
+                                            int64_t *out_index, float *out_value,
+                                            qmv_stream stream);
+
 /* Human-readable name of a status code (static storage). */
 QMV_API const char *qmv_status_string(qmv_status status);
 

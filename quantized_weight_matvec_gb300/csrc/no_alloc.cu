@@ -1,0 +1,73 @@
+// no_alloc.cu -- f8_matvec_argmax_noalloc: the fused head matvec + greedy
+// selection for callers that cannot allocate device memory.
+//
+// f8_matvec_argmax needs a small scratch buffer (one partial result per
+// block and vector) that its caller provides.  Some callers have no way to
+// get one: an engine that has handed the whole device to its own memory pool
+// at start-up and treats any further cudaMalloc as an error, or a plug-in
+// interface that passes tensors in and out but offers no workspace and no
+// allocator.  For them this entry point takes its scratch from a fixed array
+// that lives in the library itself, so it never allocates.
+//
+// The array below is a file-scope __device__ variable: every GPU that loads
+// the library holds its 256 KiB until the process exits.  In host code its
+// name is only a host-side stand-in for the device symbol, not a device
+// address, so the device address is looked up once per device with
+// cudaGetSymbolAddress (while that device is current) and passed to the
+// kernels like any other workspace pointer.
+#include <mutex>
+
+#include "qmv_internal.h"
+
+namespace {
+
+// Enough for every launch the argmax kernels make: at most
+// QMV_ARGMAX_MAX_BLOCKS blocks x QMV_MAX_BATCH vectors x 16 bytes.
+constexpr size_t kScratchBytes = size_t(QMV_ARGMAX_MAX_BLOCKS) * QMV_MAX_BATCH * 16;
+
+static __device__ __align__(256) unsigned char g_argmax_scratch[kScratchBytes];
+
+// Device address of g_argmax_scratch on each device, looked up on the first
+// call made while that device is current.
+void *scratch_address(qmv_status *status) {
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = QMV_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_argmax_scratch) != cudaSuccess || !p) {
+            *status = QMV_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    *status = QMV_OK;
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" qmv_status f8_matvec_argmax_noalloc(const uint8_t *w, int64_t R, int64_t C,
+                                               const uint8_t *scale, int64_t SR, int64_t SC,
+                                               const float *x, int32_t batch, float *y,
+                                               int64_t *out_index, float *out_value,
+                                               qmv_stream stream) {
+    // The scratch holds QMV_MAX_BATCH vectors' partials; larger batches are
+    // refused (the regular entry point refuses them too).
+    if (batch < 1 || batch > QMV_MAX_BATCH ||
+        QMV_F8_ARGMAX_WORKSPACE_BYTES(batch) > int64_t(kScratchBytes))
+        return QMV_ERR_BATCH;
+    qmv_status st = QMV_OK;
+    void *ws = scratch_address(&st);
+    if (st != QMV_OK) return st;
+    // All checks of the regular entry point still apply; the scratch does not
+    // need to start at any particular value (every block writes its partial
+    // result before the final pass reads it).
+    return f8_matvec_argmax(w, R, C, scale, SR, SC, x, batch, y, out_index, out_value, ws,
+                            int64_t(kScratchBytes), stream);
+}

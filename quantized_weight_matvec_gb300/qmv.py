@@ -74,8 +74,9 @@ def load() -> ctypes.CDLL:
     lib.cq_dequantize_row.argtypes = [CQP, P, I64, P, P, P]
     lib.f8_matvec.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P]
     lib.f8_matvec_argmax.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P, I64, P]
+    lib.f8_matvec_argmax_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P]
     for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.f8_matvec,
-               lib.f8_matvec_argmax):
+               lib.f8_matvec_argmax, lib.f8_matvec_argmax_noalloc):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
     lib.qmv_status_string.restype = ctypes.c_char_p
@@ -130,6 +131,16 @@ def f8_matvec_argmax(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: in
     return load().f8_matvec_argmax(w or None, R, C, scale or None, SR, SC, x or None, batch,
                                    y or None, out_index or None, out_value or None,
                                    workspace or None, workspace_bytes, stream or None)
+
+
+def f8_matvec_argmax_noalloc(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: int,
+                             batch: int, y: int, out_index: int, out_value: int,
+                             stream: int = 0) -> int:
+    """f8_matvec_argmax using the library's own scratch: for callers that
+    cannot allocate device memory (see include/qmv.h)."""
+    return load().f8_matvec_argmax_noalloc(w or None, R, C, scale or None, SR, SC, x or None,
+                                           batch, y or None, out_index or None,
+                                           out_value or None, stream or None)
 
 
 # --------------------------------------------------------------------------
