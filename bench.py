@@ -531,6 +531,55 @@ def run_configs(args):
                           "frac_of_8tbs": round(nbytes / us_med / 1e3 / NOMINAL_HBM_GBS, 4),
                           "l2_cold_copies": ncopies}), flush=True)
 
+    # matrix sets: one activation, several matrices sharing it (needle-2
+    # sections 6-7: phiPre/phiPost/phiResidual, Q/K/V).  Per set call, three
+    # ways: prepare + one call per matrix, prepare + cq_matvec_multi, and the
+    # fused cq_prepare_matvec.
+    for label, outs, inp, group, bits in (("set3_2048x512", (2048, 2048, 2048), 512, 64, 2),
+                                          ("set3_2048x512", (2048, 2048, 2048), 512, 64, 4),
+                                          ("cq2_vocab_fused", (32768,), 500, 128, 2)):
+        cs = [synth.cq_inputs(60 + i, o, inp, group, bits, x_scale=3.0) for i, o in enumerate(outs)]
+        c0 = cs[0]
+        per = [c.output * (c.row_bytes + 2 * (c.input_padded // c.group)) for c in cs]
+        k = copies_for(sum(per))
+        cb = torch.from_numpy(c0.codebook).to(dev)
+        packs = [torch.from_numpy(np.ascontiguousarray(np.broadcast_to(c.packed, (k,) + c.packed.shape))).to(dev)
+                 for c in cs]
+        norms = [torch.from_numpy(np.ascontiguousarray(np.broadcast_to(c.norms.view(np.int16), (k,) + c.norms.shape))).to(dev)
+                 for c in cs]
+        sets = [[qmv.CQMatrix(c.output, c.input, c.input_padded, c.group, c.bits, packs[j][i],
+                              norms[j][i], cb) for j, c in enumerate(cs)] for i in range(k)]
+        x = torch.from_numpy(c0.x).to(dev)
+        p = torch.empty((1, c0.input_padded), device=dev)
+        ys = [torch.empty((1, c.output), device=dev) for c in cs]
+        yp = [y.data_ptr() for y in ys]
+        nb = cq_prepare_bytes(c0.input, c0.input_padded) + sum(
+            cq_matvec_bytes(c.output, c.input_padded, c.group, c.bits) for c in cs)
+
+        def sep(ms):
+            def run(sh):
+                st = qmv.cq_prepare(ms[0].struct, x.data_ptr(), 1, p.data_ptr(), sh)
+                for m, y in zip(ms, yp):
+                    st = st or qmv.cq_matvec(m.struct, p.data_ptr(), 1, y, sh)
+                return st
+            return run
+
+        def multi(ms):
+            def run(sh):
+                return (qmv.cq_prepare(ms[0].struct, x.data_ptr(), 1, p.data_ptr(), sh) or
+                        qmv.cq_matvec_multi([m.struct for m in ms], p.data_ptr(), 1, yp, sh))
+            return run
+
+        def fused(ms):
+            return lambda sh: qmv.cq_prepare_matvec([m.struct for m in ms], x.data_ptr(), 1, 0, yp, sh)
+
+        tag = "%s/%dbit" % (label, bits)
+        for op, mk in (("prepare+cq_matvec x%d" % len(cs), sep),
+                       ("prepare+cq_matvec_multi", multi), ("cq_prepare_matvec", fused)):
+            med, best = _graph_time(torch, [mk(ms) for ms in sets])
+            emit(tag, 1, op, nb, med, best, k)
+        del packs, norms, sets
+
     for name, wl in synth.WORKLOADS.items():
         for batch in wl["batch"]:
             if wl["kind"] == "cq":

@@ -155,6 +155,41 @@ QMV_API qmv_status cq_matvec(const qmv_cq_matrix *m, const float *prepared, int3
 QMV_API qmv_status cq_dequantize_row(const qmv_cq_matrix *m, const int32_t *rows, int64_t n,
                              float *out, int32_t *dev_status, qmv_stream stream);
 
+/* Most matrices one cq_matvec_multi / cq_prepare_matvec call takes. */
+#define QMV_MAX_MATRICES 8
+
+/*
+ * cq_matvec_multi -- several CQ matrices applied to one prepared activation
+ * in one launch.  needle.js "part 2", section 6 ("An optimized backend can
+ * reuse the prepared CQ activation for all three": phiPre, phiPost and
+ * phiResidual of one normalised input) and section 7 (the Q, K and V
+ * projections of one block input).
+ *
+ * mats[i] for i < nmats (1 <= nmats <= QMV_MAX_MATRICES) must share input,
+ * input_padded, group, bits and the codebook array (the archive keeps one
+ * codebook per bit width, "part 1" section 4); output, packed and norms are
+ * per matrix.  ys[i] (a host array of device pointers) receives matrix i's
+ * [batch, output_i] result, exactly what cq_matvec(mats[i], ...) would
+ * write.  Every ys[i] must be distinct from every input and every other
+ * ys[j] (QMV_ERR_ALIAS); a mismatch of the shared fields is QMV_ERR_SHAPE.
+ */
+QMV_API qmv_status cq_matvec_multi(const qmv_cq_matrix *mats, int32_t nmats, const float *prepared,
+                                   int32_t batch, float *const *ys, qmv_stream stream);
+
+/*
+ * cq_prepare_matvec -- cq_prepare fused into cq_matvec_multi: x is
+ * prepared ("part 2", section 2) inside the same launch and applied to
+ * every matrix.  Results are bitwise equal to cq_prepare followed by
+ * cq_matvec_multi.  `prepared` may be NULL; when given, the prepared
+ * activation [batch, input_padded] is also written there.  When
+ * batch * input_padded floats do not fit on chip (over 96 KiB) or
+ * group > 1024, the call runs cq_prepare and cq_matvec_multi as two
+ * launches instead (same results; `prepared` must then be given).
+ */
+QMV_API qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, const float *x,
+                                     int32_t batch, float *prepared, float *const *ys,
+                                     qmv_stream stream);
+
 /*
  * f8_matvec -- ds4f-disk issue #6, step 1 (the F8 matvec with per-block
  * E8M0 scales; the head of work item 3 has this shape):

@@ -259,35 +259,131 @@ GroupArgs group_args(const qmv_cq_matrix &m) {
 }
 
 // ---------------------------------------------------------------------------
-// cq_matvec, general kernel: any bits, group, width and alignment.  One warp
-// per row; lane l takes columns l, l+32, ...; each element contributes
-// (codebook level * norm) * prepared in a float32 FMA, then a fixed-order warp
-// reduction.
+// Matrix sets.  cq_matvec (one matrix), cq_matvec_multi and cq_prepare_matvec
+// (several matrices sharing input width, group, bits and codebook -- needle-2
+// section 6: one prepared activation serves phiPre, phiPost and phiResidual;
+// section 7: Q, K and V of one input) run the same kernels.  The units of all
+// matrices (rows, or groups of RPW rows for the table kernel) form one space;
+// unit u belongs to matrix i when first[i] <= u < first[i+1].  With FUSED the
+// activation is prepared inside every block (same butterflies and rounding as
+// cq_prepare, so the results are bitwise those of cq_prepare + cq_matvec).
 // ---------------------------------------------------------------------------
 
-template <int B>
-__global__ void __launch_bounds__(256) cq_matvec_general_kernel(qmv_cq_matrix m, const float *p,
-                                                                float *y) {
+struct CqSet {
+    int nmats, bits;
+    int64_t input, P, G, nG, row_bytes;
+    const float *codebook;
+    int64_t output[QMV_MAX_MATRICES];
+    const uint8_t *packed[QMV_MAX_MATRICES];
+    const uint16_t *norms[QMV_MAX_MATRICES];
+    float *y[QMV_MAX_MATRICES];
+    int64_t first[QMV_MAX_MATRICES + 1];
+    const float *p;        // prepared activation [B, P] (not FUSED)
+    const float *x;        // raw activation [B, input] (FUSED)
+    float *prepared_out;   // FUSED: block 0 also stores the prepared vector (may be NULL)
+    double s;              // RN64(1/sqrt(G))
+};
+
+// Matrix of unit u, scanning on from matrix i (units of a warp only grow).
+__device__ __forceinline__ int set_matrix(const CqSet &c, int64_t u, int i) {
+    while (i + 1 < c.nmats && u >= c.first[i + 1]) i++;
+    return i;
+}
+
+// ---- in-block prepare (FUSED): x -> sp[B][P] in shared memory -------------
+template <int E>
+__device__ __forceinline__ void prep_warp_jobs(const CqSet &c, int B, float *sp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const bool store = c.prepared_out && blockIdx.x == 0;
+    const int64_t jobs = int64_t(B) * c.nG;
+    for (int64_t job = warp; job < jobs; job += nw) {
+        const int64_t v = job / c.nG, g = job - v * c.nG;
+        const int64_t col0 = g * c.G + int64_t(lane) * E;
+        float val[E];
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const int64_t col = col0 + e;
+            val[e] = col < c.input ? __ldg(c.x + v * c.input + col) : 0.0f;
+        }
+        fwht_warp<E>(val, int(c.G), lane);
+#pragma unroll
+        for (int e = 0; e < E; e++) {
+            const float o = scale_f64(val[e], c.s);
+            sp[v * c.P + col0 + e] = o;
+            if (store) c.prepared_out[v * c.P + col0 + e] = o;
+        }
+    }
+}
+
+// G <= 32: each warp transforms 32 consecutive elements of the [B, P] space.
+__device__ __forceinline__ void prep_small(const CqSet &c, int B, float *sp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const bool store = c.prepared_out && blockIdx.x == 0;
+    const int64_t total = int64_t(B) * c.P;
+    for (int64_t chunk = warp; chunk * 32 < total; chunk += nw) {
+        const int64_t flat = chunk * 32 + lane;
+        const bool valid = flat < total;
+        const int64_t v = valid ? flat / c.P : 0, col = valid ? flat - v * c.P : 0;
+        float val[1];
+        val[0] = (valid && col < c.input) ? __ldg(c.x + v * c.input + col) : 0.0f;
+        fwht_warp<1>(val, int(c.G), lane);
+        if (valid) {
+            const float o = scale_f64(val[0], c.s);
+            sp[flat] = o;
+            if (store) c.prepared_out[flat] = o;
+        }
+    }
+}
+
+__device__ __forceinline__ void block_prepare(const CqSet &c, int B, float *sp) {
+    switch (c.G) {
+        case 64: prep_warp_jobs<2>(c, B, sp); break;
+        case 128: prep_warp_jobs<4>(c, B, sp); break;
+        case 256: prep_warp_jobs<8>(c, B, sp); break;
+        case 512: prep_warp_jobs<16>(c, B, sp); break;
+        case 1024: prep_warp_jobs<32>(c, B, sp); break;
+        default: prep_small(c, B, sp); break;  // G <= 32 (fused launches never take G > 1024)
+    }
+}
+
+// ---------------------------------------------------------------------------
+// General kernel: any bits, group, width, batch and alignment.  One warp per
+// row; lane l takes columns l, l+32, ...; each element contributes
+// (codebook level * norm) * prepared in a float32 FMA, then a fixed-order
+// warp reduction.
+// ---------------------------------------------------------------------------
+template <int B, bool FUSED>
+__global__ void __launch_bounds__(256) cq_matvec_general_kernel(CqSet c) {
     __shared__ float cb[32];
+    extern __shared__ __align__(16) float sp_dyn[];
     pdl_wait();
     pdl_trigger();
-    if (threadIdx.x < (1 << m.bits)) cb[threadIdx.x] = m.codebook[threadIdx.x];
+    if (threadIdx.x < (1 << c.bits)) cb[threadIdx.x] = c.codebook[threadIdx.x];
+    const float *p = c.p;
+    if (FUSED) {
+        block_prepare(c, B, sp_dyn);
+        p = sp_dyn;
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
-    const int64_t P = m.input_padded, nG = P / m.group;
-    const int lg = __ffsll(m.group) - 1;
-    for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < m.output;
-         r += nwarps) {
-        const uint8_t *row = m.packed + r * m.row_bytes;
+    const int64_t P = c.P, nG = c.nG;
+    const int lg = __ffsll(c.G) - 1;
+    int mi = 0;
+    for (int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; u < c.first[c.nmats];
+         u += nwarps) {
+        mi = set_matrix(c, u, mi);
+        const int64_t r = u - c.first[mi];
+        const uint8_t *row = c.packed[mi] + r * c.row_bytes;
+        const uint16_t *nrow = c.norms[mi] + r * nG;
         float acc[B];
 #pragma unroll
         for (int v = 0; v < B; v++) acc[v] = 0.0f;
         for (int64_t k = lane; k < P; k += 32) {
-            float n = half_bits_to_float(__ldg(m.norms + r * nG + (k >> lg)));
-            float wv = cb[cq_index(row, k, m.bits)] * n;
+            const float n = half_bits_to_float(__ldg(nrow + (k >> lg)));
+            const float wv = cb[cq_index(row, k, c.bits)] * n;
 #pragma unroll
-            for (int v = 0; v < B; v++) acc[v] = fmaf(wv, __ldg(p + v * P + k), acc[v]);
+            for (int v = 0; v < B; v++) acc[v] = fmaf(wv, FUSED ? p[v * P + k] : __ldg(p + v * P + k), acc[v]);
         }
 #pragma unroll
         for (int v = 0; v < B; v++) {
@@ -295,16 +391,17 @@ __global__ void __launch_bounds__(256) cq_matvec_general_kernel(qmv_cq_matrix m,
             for (int d = 16; d >= 1; d >>= 1) acc[v] += __shfl_xor_sync(kFull, acc[v], d);
         }
         if (lane == 0) {
+            const int64_t out = c.output[mi];
 #pragma unroll
-            for (int v = 0; v < B; v++) y[v * m.output + r] = acc[v];
+            for (int v = 0; v < B; v++) c.y[mi][v * out + r] = acc[v];
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// cq_matvec, 2-bit / batch-1 kernel with the activation folded into a nibble
-// table.  The page's 2-bit loop looks up four levels per byte (section 3);
-// here each table entry already holds the two products of one nibble:
+// 2-bit / batch-1 kernel with the activation folded into a nibble table.  The
+// page's 2-bit loop looks up four levels per byte (section 3); here each
+// table entry already holds the two products of one nibble:
 //   T[nib][c2] = codebook[nib & 3] * p[2*c2] + codebook[nib >> 2] * p[2*c2+1]
 // so every 4-bit code pair costs one shared-memory load and one add.
 //
@@ -316,70 +413,80 @@ __global__ void __launch_bounds__(256) cq_matvec_general_kernel(qmv_cq_matrix m,
 // (rho, q) reads slot t + rho + RPW*q: the 32 lanes of a warp always hit 32
 // distinct banks and the address is a per-lane constant plus 4*t.
 //
-// Shared memory: 16 nibbles x CPR chunks x 64 slots x 4 B = 64*P bytes.
-// Requirements (checked by the launcher): bits == 2, batch == 1,
-// P in {256, 512, 1024, 2048}, group >= 64, 16-byte aligned packed rows.
+// Shared memory: 16 nibbles x CPR chunks x 64 slots x 4 B = 64*P bytes (plus
+// 4*P for the prepared vector when FUSED).  Requirements (checked by the
+// launcher): bits == 2, batch == 1, P in {256, 512, 1024, 2048}, group >= 64,
+// 16-byte aligned packed rows.  Units are row groups of RPW rows per matrix.
 // ---------------------------------------------------------------------------
 
-template <int CPR>
-__device__ __forceinline__ void cq2_load(uint4 &d, float &n, const qmv_cq_matrix &m, int64_t r, int q,
-                                         int g, int64_t nG) {
+__device__ __forceinline__ void cq2_load(uint4 &d, float &n, const CqSet &c, int mi, int64_t r, int q, int g) {
     d = make_uint4(0, 0, 0, 0);
     n = 0.0f;
-    if (r < m.output) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(m.packed + r * m.row_bytes) + q;
+    if (r < c.output[mi]) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(c.packed[mi] + r * c.row_bytes) + q;
         asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
                      : "l"(src));
-        n = half_bits_to_float(__ldg(m.norms + r * nG + g));
+        n = half_bits_to_float(__ldg(c.norms[mi] + r * c.nG + g));
     }
 }
 
-template <int CPR>
-__global__ void __launch_bounds__(1024, 1) cq2_table_kernel(qmv_cq_matrix m, const float *p, float *y) {
+template <int CPR, bool FUSED>
+__global__ void __launch_bounds__(1024, 1) cq2_table_kernel(CqSet c) {
     constexpr int RPW = 32 / CPR;
     constexpr int P = CPR * 64;
     constexpr int NIB_STRIDE = 4 * P;  // bytes per nibble block
-    constexpr int LG_NIB = (P == 256) ? 10 : (P == 512) ? 11 : (P == 1024) ? 12 : 13;
-    static_assert((1 << LG_NIB) == NIB_STRIDE, "nibble stride");
     extern __shared__ __align__(16) unsigned char table_raw[];
     float *table = reinterpret_cast<float *>(table_raw);
+    float *sp = reinterpret_cast<float *>(table_raw + 64 * P);  // FUSED: prepared vector
 
     pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int rho = lane / CPR, q = lane % CPR;
-    const int64_t nG = P / m.group;
-    const int g = (q * 64) / int(m.group);
-    const int64_t ngroups_rows = (m.output + RPW - 1) / RPW;
+    const int g = (q * 64) / int(c.G);
+    const int64_t nunits = c.first[c.nmats];
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
-    int64_t rg = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
 
     // the first rows' loads go out before the table is built
+    int mi = set_matrix(c, u, 0);
     uint4 d;
     float n;
-    cq2_load<CPR>(d, n, m, rg * RPW + rho, q, g, nG);
+    if (u < nunits) {
+        cq2_load(d, n, c, mi, (u - c.first[mi]) * RPW + rho, q, g);
+    } else {
+        d = make_uint4(0, 0, 0, 0);
+        n = 0.0f;
+    }
 
+    const float *pv = c.p;
+    if (FUSED) {
+        block_prepare(c, 1, sp);
+        __syncthreads();
+        pv = sp;
+    }
     // ---- build the table (one pass per block): one thread per column pair
     // (chunk q, pair j) loads p once and writes all 16 nibble entries ----
     {
-        float cb[4];
+        float cbv[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) cb[i] = __ldg(m.codebook + i);
-        for (int u = threadIdx.x; u < CPR * 32; u += blockDim.x) {
-            const int qq = u >> 5, j = u & 31;
+        for (int i = 0; i < 4; i++) cbv[i] = __ldg(c.codebook + i);
+        for (int uu = threadIdx.x; uu < CPR * 32; uu += blockDim.x) {
+            const int qq = uu >> 5, j = uu & 31;
             const int col = qq * 64 + 2 * j;
-            const float p0 = __ldg(p + col), p1 = __ldg(p + col + 1);
+            const float p0 = FUSED ? pv[col] : __ldg(pv + col);
+            const float p1 = FUSED ? pv[col + 1] : __ldg(pv + col + 1);
             float lo_prod[4];
 #pragma unroll
-            for (int i = 0; i < 4; i++) lo_prod[i] = cb[i] * p0;
+            for (int i = 0; i < 4; i++) lo_prod[i] = cbv[i] * p0;
             const int slot = (j + RPW * qq) & 31;
             float *blk = table + (qq * 256) / 4 + slot;
 #pragma unroll
             for (int hi = 0; hi < 4; hi++) {
 #pragma unroll
                 for (int lo = 0; lo < 4; lo++) {
-                    const float v = fmaf(cb[hi], p1, lo_prod[lo]);
+                    const float v = fmaf(cbv[hi], p1, lo_prod[lo]);
                     float *e = blk + (lo | (hi << 2)) * (NIB_STRIDE / 4);
                     e[0] = v;
                     e[32] = v;
@@ -394,12 +501,19 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(qmv_cq_matrix m, con
                                unsigned(q * 256 + 4 * (rho + RPW * q));
     const unsigned sh = 4u * unsigned(rho);
 
-    for (; rg < ngroups_rows; rg += nwarps) {
-        const int64_t r = rg * RPW + rho;
+    for (; u < nunits; u += nwarps) {
+        const int64_t r = (u - c.first[mi]) * RPW + rho;
+        const int64_t out = c.output[mi];
+        float *y = c.y[mi];
         // next rows' loads before this row's lookups
-        uint4 dn;
-        float nn;
-        cq2_load<CPR>(dn, nn, m, (rg + nwarps) * RPW + rho, q, g, nG);
+        uint4 dn = make_uint4(0, 0, 0, 0);
+        float nn = 0.0f;
+        const int64_t un = u + nwarps;
+        int mn = mi;
+        if (un < nunits) {
+            mn = set_matrix(c, un, mi);
+            cq2_load(dn, nn, c, mn, (un - c.first[mn]) * RPW + rho, q, g);
+        }
         // rotate the 128-bit chunk right by 4*rho bits, then split every word
         // into its even nibbles (one per byte) and its odd nibbles
         unsigned w[4];
@@ -428,27 +542,61 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(qmv_cq_matrix m, con
         float acc = n * part;
 #pragma unroll
         for (int dd = CPR / 2; dd >= 1; dd >>= 1) acc += __shfl_xor_sync(kFull, acc, dd);
-        if (q == 0 && r < m.output) y[r] = acc;
+        if (q == 0 && r < out) y[r] = acc;
         d = dn;
         n = nn;
+        mi = mn;
     }
 }
 
-template <int CPR>
-qmv_status launch_cq2_table(const qmv_cq_matrix &m, const float *p, float *y, cudaStream_t s) {
-    const size_t smem = size_t(64) * CPR * 64;
-    const void *kp = reinterpret_cast<const void *>(cq2_table_kernel<CPR>);
+template <int CPR, bool FUSED>
+qmv_status launch_cq2_table(CqSet c, cudaStream_t s) {
+    constexpr int RPW = 32 / CPR;
+    const size_t smem = size_t(64) * CPR * 64 + (FUSED ? size_t(4) * CPR * 64 : 0);
+    const void *kp = reinterpret_cast<const void *>(cq2_table_kernel<CPR, FUSED>);
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
-    const int64_t rgroups = (m.output + (32 / CPR) - 1) / (32 / CPR);
-    int64_t blocks = (rgroups + 31) / 32;  // 32 warps per block
+    c.first[0] = 0;
+    for (int i = 0; i < c.nmats; i++) c.first[i + 1] = c.first[i] + (c.output[i] + RPW - 1) / RPW;
+    int64_t blocks = (c.first[c.nmats] + 31) / 32;  // 32 warps per block
     if (blocks > sm_count()) blocks = sm_count();
-    return from_cuda(launch_pdl(cq2_table_kernel<CPR>, dim3(unsigned(blocks)), dim3(1024), smem, s, m, p, y));
+    if (blocks < 1) blocks = 1;
+    return from_cuda(launch_pdl(cq2_table_kernel<CPR, FUSED>, dim3(unsigned(blocks)), dim3(1024), smem, s, c));
 }
 
-template <int B>
-qmv_status launch_cq_general(const qmv_cq_matrix &m, const float *p, float *y, cudaStream_t s) {
-    int blocks = grid_blocks(reinterpret_cast<const void *>(cq_matvec_general_kernel<B>), 256, 0, m.output);
-    return from_cuda(launch_pdl(cq_matvec_general_kernel<B>, dim3(unsigned(blocks)), dim3(256), 0, s, m, p, y));
+template <int B, bool FUSED>
+qmv_status launch_cq_general(CqSet c, cudaStream_t s) {
+    const size_t smem = FUSED ? size_t(4) * B * c.P : 0;
+    const void *kp = reinterpret_cast<const void *>(cq_matvec_general_kernel<B, FUSED>);
+    if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
+    c.first[0] = 0;
+    for (int i = 0; i < c.nmats; i++) c.first[i + 1] = c.first[i] + c.output[i];
+    const int blocks = grid_blocks(kp, 256, smem, c.first[c.nmats]);
+    return from_cuda(launch_pdl(cq_matvec_general_kernel<B, FUSED>, dim3(unsigned(blocks)), dim3(256), smem, s, c));
+}
+
+template <bool FUSED>
+qmv_status launch_set(const CqSet &c, int batch, bool all_aligned16, cudaStream_t s) {
+    const int64_t P = c.P;
+    const bool table_ok = c.bits == 2 && batch == 1 && c.G >= 64 &&
+                          (P == 256 || P == 512 || P == 1024 || P == 2048) && all_aligned16;
+    if (table_ok) {
+        switch (P) {
+            case 256: return launch_cq2_table<4, FUSED>(c, s);
+            case 512: return launch_cq2_table<8, FUSED>(c, s);
+            case 1024: return launch_cq2_table<16, FUSED>(c, s);
+            default: return launch_cq2_table<32, FUSED>(c, s);
+        }
+    }
+    switch (batch) {
+        case 1: return launch_cq_general<1, FUSED>(c, s);
+        case 2: return launch_cq_general<2, FUSED>(c, s);
+        case 3: return launch_cq_general<3, FUSED>(c, s);
+        case 4: return launch_cq_general<4, FUSED>(c, s);
+        case 5: return launch_cq_general<5, FUSED>(c, s);
+        case 6: return launch_cq_general<6, FUSED>(c, s);
+        case 7: return launch_cq_general<7, FUSED>(c, s);
+        default: return launch_cq_general<8, FUSED>(c, s);
+    }
 }
 
 }  // namespace
@@ -472,30 +620,40 @@ qmv_status launch_cq_dequantize_row(const qmv_cq_matrix &m, const int32_t *rows,
     return launch_group<GMode::Gather>(a, s);
 }
 
-qmv_status launch_cq_matvec(const qmv_cq_matrix &m, const float *p, int batch, float *y,
-                            cudaStream_t s) {
-    const int64_t P = m.input_padded;
-    const bool table_ok = m.bits == 2 && batch == 1 && m.group >= 64 &&
-                          (P == 256 || P == 512 || P == 1024 || P == 2048) &&
-                          (reinterpret_cast<uintptr_t>(m.packed) % 16) == 0;
-    if (table_ok) {
-        switch (P) {
-            case 256: return launch_cq2_table<4>(m, p, y, s);
-            case 512: return launch_cq2_table<8>(m, p, y, s);
-            case 1024: return launch_cq2_table<16>(m, p, y, s);
-            default: return launch_cq2_table<32>(m, p, y, s);
-        }
+bool cq_fused_fits(const qmv_cq_matrix &m, int batch) {
+    return m.group <= 1024 && int64_t(batch) * m.input_padded * 4 <= 96 * 1024;
+}
+
+qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, const float *x,
+                         float *prepared_out, int batch, float *const *ys, cudaStream_t s) {
+    CqSet c = {};
+    const qmv_cq_matrix &m0 = mats[0];
+    c.nmats = nmats;
+    c.bits = m0.bits;
+    c.input = m0.input;
+    c.P = m0.input_padded;
+    c.G = m0.group;
+    c.nG = m0.input_padded / m0.group;
+    c.row_bytes = m0.row_bytes;
+    c.codebook = m0.codebook;
+    c.s = 1.0 / sqrt(double(m0.group));
+    c.p = p;
+    c.x = x;
+    c.prepared_out = prepared_out;
+    bool aligned16 = true;
+    for (int i = 0; i < nmats; i++) {
+        c.output[i] = mats[i].output;
+        c.packed[i] = mats[i].packed;
+        c.norms[i] = mats[i].norms;
+        c.y[i] = ys[i];
+        if (reinterpret_cast<uintptr_t>(mats[i].packed) % 16 != 0) aligned16 = false;
     }
-    switch (batch) {
-        case 1: return launch_cq_general<1>(m, p, y, s);
-        case 2: return launch_cq_general<2>(m, p, y, s);
-        case 3: return launch_cq_general<3>(m, p, y, s);
-        case 4: return launch_cq_general<4>(m, p, y, s);
-        case 5: return launch_cq_general<5>(m, p, y, s);
-        case 6: return launch_cq_general<6>(m, p, y, s);
-        case 7: return launch_cq_general<7>(m, p, y, s);
-        default: return launch_cq_general<8>(m, p, y, s);
-    }
+    return x ? launch_set<true>(c, batch, aligned16, s) : launch_set<false>(c, batch, aligned16, s);
+}
+
+qmv_status launch_cq_matvec(const qmv_cq_matrix &m, const float *p, int batch, float *y, cudaStream_t s) {
+    float *ys[1] = {y};
+    return launch_cq_set(&m, 1, p, nullptr, nullptr, batch, ys, s);
 }
 
 }  // namespace qmv

@@ -204,17 +204,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
     return d;
 }
 
-__device__ __forceinline__ void decode4(unsigned word, float (&f)[4]) {
-    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(word & 0xffffu), __NV_E4M3);
-    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(word >> 16), __NV_E4M3);
-    float2 a = __half22float2(__half2(lo));
-    float2 b = __half22float2(__half2(hi));
-    f[0] = a.x;
-    f[1] = a.y;
-    f[2] = b.x;
-    f[3] = b.y;
-}
-
 __device__ __forceinline__ unsigned word_of(const uint4 &d, int q) {
     return q == 0 ? d.x : q == 1 ? d.y : q == 2 ? d.z : d.w;
 }
@@ -343,8 +332,16 @@ __device__ __forceinline__ bool setup_scale(const F8Args &a, int64_t r0, int row
     return false;
 }
 
+// Resident blocks per SM the register budget is sized for: batch 1 streams
+// best at 3 blocks (the plain variant fits there on its own; the argmax
+// variant is held to it), batches up to 4 at 2, larger batches at 1.
+template <int B, bool AM>
+struct FastMinBlocks {
+    static constexpr int value = (B == 1) ? (AM ? 3 : 0) : (B <= 4 ? 2 : 1);
+};
+
 template <int B, int T, bool PF, bool GS, bool AM>
-__global__ void __launch_bounds__(256) f8_fast_kernel(F8Args a) {
+__global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kernel(F8Args a) {
     extern __shared__ int chunk_cb[];
     const int64_t nchunk = a.C >> 4;
     // (depends only on the shapes: runs before the wait)

@@ -140,6 +140,53 @@ qmv_status check_cq_data(const qmv_cq_matrix *m) {
     return QMV_OK;
 }
 
+// Checks shared by cq_matvec_multi and cq_prepare_matvec: the set's size, each
+// matrix, the fields they must share, the output pointers, and that no output
+// overlaps any matrix array, the activation `act` (act_bytes) or another output.
+qmv_status check_cq_set(const qmv_cq_matrix *mats, int32_t nmats, int32_t batch, float *const *ys,
+                        const void *act, int64_t act_bytes, const void *extra_out, int64_t extra_bytes) {
+    if (!mats || !ys) return QMV_ERR_NULL;
+    if (nmats < 1 || nmats > QMV_MAX_MATRICES) return QMV_ERR_SHAPE;
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    const qmv_cq_matrix &m0 = mats[0];
+    int64_t yb[QMV_MAX_MATRICES];
+    for (int i = 0; i < nmats; i++) {
+        const qmv_cq_matrix &m = mats[i];
+        if ((st = check_cq_shape(&m)) != QMV_OK) return st;
+        if ((st = check_cq_data(&m)) != QMV_OK) return st;
+        if (m.input != m0.input || m.input_padded != m0.input_padded || m.group != m0.group ||
+            m.bits != m0.bits || m.row_bytes != m0.row_bytes || m.codebook != m0.codebook)
+            return QMV_ERR_SHAPE;
+        if (m.output > 0 && !ys[i]) return QMV_ERR_NULL;
+        if (!aligned(ys[i], 4)) return QMV_ERR_ALIGN;
+        if (!mul_ok(int64_t(batch) * 4, m.output, &yb[i])) return QMV_ERR_OVERFLOW;
+    }
+    for (int i = 0; i < nmats; i++) {
+        if (overlaps(ys[i], yb[i], act, act_bytes) || overlaps(ys[i], yb[i], extra_out, extra_bytes))
+            return QMV_ERR_ALIAS;
+        for (int j = 0; j < nmats; j++) {
+            const CqBytes b = cq_bytes(&mats[j]);
+            if (overlaps(ys[i], yb[i], mats[j].packed, b.packed) ||
+                overlaps(ys[i], yb[i], mats[j].norms, b.norms) ||
+                overlaps(ys[i], yb[i], mats[j].codebook, b.codebook) ||
+                overlaps(extra_out, extra_bytes, mats[j].packed, b.packed) ||
+                overlaps(extra_out, extra_bytes, mats[j].norms, b.norms) ||
+                overlaps(extra_out, extra_bytes, mats[j].codebook, b.codebook))
+                return QMV_ERR_ALIAS;
+            if (j != i && overlaps(ys[i], yb[i], ys[j], yb[j])) return QMV_ERR_ALIAS;
+        }
+    }
+    if (overlaps(extra_out, extra_bytes, act, act_bytes)) return QMV_ERR_ALIAS;
+    return QMV_OK;
+}
+
+int64_t cq_set_rows(const qmv_cq_matrix *mats, int32_t nmats) {
+    int64_t rows = 0;
+    for (int i = 0; i < nmats; i++) rows += mats[i].output;
+    return rows;
+}
+
 }  // namespace
 
 extern "C" {
@@ -195,6 +242,47 @@ qmv_status cq_matvec(const qmv_cq_matrix *m, const float *prepared, int32_t batc
         return QMV_ERR_ALIAS;
     if (m->output == 0) return QMV_OK;
     return qmv::launch_cq_matvec(*m, prepared, batch, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status cq_matvec_multi(const qmv_cq_matrix *mats, int32_t nmats, const float *prepared,
+                           int32_t batch, float *const *ys, qmv_stream stream) {
+    if (!prepared) return QMV_ERR_NULL;
+    if (!aligned(prepared, 4)) return QMV_ERR_ALIGN;
+    if (!mats) return QMV_ERR_NULL;
+    int64_t pb = 0;
+    if (nmats >= 1 && !mul_ok(int64_t(batch < 1 ? 1 : batch) * 4, mats[0].input_padded, &pb))
+        return QMV_ERR_OVERFLOW;
+    qmv_status st = check_cq_set(mats, nmats, batch, ys, prepared, pb, nullptr, 0);
+    if (st != QMV_OK) return st;
+    if (cq_set_rows(mats, nmats) == 0) return QMV_OK;
+    return qmv::launch_cq_set(mats, nmats, prepared, nullptr, nullptr, batch, ys,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, const float *x, int32_t batch,
+                             float *prepared, float *const *ys, qmv_stream stream) {
+    if (!x) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(prepared, 4)) return QMV_ERR_ALIGN;
+    if (!mats) return QMV_ERR_NULL;
+    int64_t xb = 0, pb = 0;
+    if (nmats >= 1 && (!mul_ok(int64_t(batch < 1 ? 1 : batch) * 4, mats[0].input, &xb) ||
+                       !mul_ok(int64_t(batch < 1 ? 1 : batch) * 4, mats[0].input_padded, &pb)))
+        return QMV_ERR_OVERFLOW;
+    qmv_status st = check_cq_set(mats, nmats, batch, ys, x, xb, prepared, prepared ? pb : 0);
+    if (st != QMV_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (qmv::cq_fused_fits(mats[0], batch)) {
+        if (cq_set_rows(mats, nmats) == 0) {
+            // no matrix rows: the prepared activation is still produced on request
+            return prepared ? qmv::launch_cq_prepare(mats[0], x, batch, prepared, s) : QMV_OK;
+        }
+        return qmv::launch_cq_set(mats, nmats, nullptr, x, prepared, batch, ys, s);
+    }
+    // too wide to prepare on chip: two launches through the prepared vector
+    if (!prepared) return QMV_ERR_NULL;
+    st = qmv::launch_cq_prepare(mats[0], x, batch, prepared, s);
+    if (st != QMV_OK || cq_set_rows(mats, nmats) == 0) return st;
+    return qmv::launch_cq_set(mats, nmats, prepared, nullptr, nullptr, batch, ys, s);
 }
 
 qmv_status cq_dequantize_row(const qmv_cq_matrix *m, const int32_t *rows, int64_t n, float *out,

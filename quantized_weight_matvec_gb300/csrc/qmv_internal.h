@@ -68,6 +68,13 @@ qmv_status launch_cq_dequantize_row(const qmv_cq_matrix &m, const int32_t *rows,
                                     float *out, int32_t *dev_status, cudaStream_t s);
 qmv_status launch_cq_matvec(const qmv_cq_matrix &m, const float *prepared, int batch, float *y,
                             cudaStream_t s);
+// Several matrices sharing input width, group, bits and codebook.  With x
+// non-NULL the activation is prepared inside the launch (and also stored to
+// prepared_out when that is non-NULL); otherwise p is the prepared vector.
+qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, const float *x,
+                         float *prepared_out, int batch, float *const *ys, cudaStream_t s);
+// Whether cq_prepare_matvec can prepare on chip (else it runs two launches).
+bool cq_fused_fits(const qmv_cq_matrix &m, int batch);
 
 // ---- F8 ------------------------------------------------------------------
 qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,

@@ -72,11 +72,14 @@ def load() -> ctypes.CDLL:
     lib.cq_prepare.argtypes = [CQP, P, I32, P, P]
     lib.cq_matvec.argtypes = [CQP, P, I32, P, P]
     lib.cq_dequantize_row.argtypes = [CQP, P, I64, P, P, P]
+    lib.cq_matvec_multi.argtypes = [CQP, I32, P, I32, P, P]
+    lib.cq_prepare_matvec.argtypes = [CQP, I32, P, I32, P, P, P]
     lib.f8_matvec.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P]
     lib.f8_matvec_argmax.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P, I64, P]
     lib.f8_matvec_argmax_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P]
-    for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.f8_matvec,
-               lib.f8_matvec_argmax, lib.f8_matvec_argmax_noalloc):
+    for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.cq_matvec_multi,
+               lib.cq_prepare_matvec, lib.f8_matvec, lib.f8_matvec_argmax,
+               lib.f8_matvec_argmax_noalloc):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
     lib.qmv_status_string.restype = ctypes.c_char_p
@@ -111,6 +114,25 @@ def cq_prepare(m: CQMatrixStruct, x: int, batch: int, prepared: int, stream: int
 
 def cq_matvec(m: CQMatrixStruct, prepared: int, batch: int, y: int, stream: int = 0) -> int:
     return load().cq_matvec(ctypes.byref(m), prepared or None, batch, y or None, stream or None)
+
+
+def _set(mats, ys):
+    n = len(mats)
+    arr = (CQMatrixStruct * max(n, 1))(*mats)
+    yarr = (ctypes.c_void_p * max(n, 1))(*[int(v) or None for v in ys])
+    return arr, yarr, n
+
+
+def cq_matvec_multi(mats, prepared: int, batch: int, ys, stream: int = 0) -> int:
+    """mats: list of CQMatrixStruct; ys: list of device pointers."""
+    arr, yarr, n = _set(mats, ys)
+    return load().cq_matvec_multi(arr, n, prepared or None, batch, yarr, stream or None)
+
+
+def cq_prepare_matvec(mats, x: int, batch: int, prepared: int, ys, stream: int = 0) -> int:
+    arr, yarr, n = _set(mats, ys)
+    return load().cq_prepare_matvec(arr, n, x or None, batch, prepared or None, yarr,
+                                    stream or None)
 
 
 def cq_dequantize_row(m: CQMatrixStruct, rows: int, n: int, out: int, dev_status: int = 0,
@@ -286,3 +308,29 @@ def f8_matvec_argmax_t(w, scale, x, y=None, workspace=None, stream=None):
                             idx.data_ptr(), val.data_ptr(), workspace.data_ptr(), workspace.numel(),
                             _stream(stream)), "f8_matvec_argmax")
     return idx, val
+
+
+def cq_matvec_multi_t(mats, prepared, stream=None):
+    """[y_i] = cq_matvec(mats[i], prepared) for every CQMatrix in one launch."""
+    torch = _torch()
+    prepared = _dev(prepared, torch.float32, "prepared")
+    batch = prepared.shape[0] if prepared.dim() == 2 else 1
+    ys = [torch.empty((batch, m.output), dtype=torch.float32, device=prepared.device)
+          for m in mats]
+    _check(cq_matvec_multi([m.struct for m in mats], prepared.data_ptr(), batch,
+                           [y.data_ptr() for y in ys], _stream(stream)), "cq_matvec_multi")
+    return ys
+
+
+def cq_prepare_matvec_t(mats, x, prepared=None, stream=None):
+    """[y_i] for x prepared inside the launch; `prepared` (optional) receives it."""
+    torch = _torch()
+    x = _dev(x, torch.float32, "x")
+    batch = x.shape[0] if x.dim() == 2 else 1
+    ys = [torch.empty((batch, m.output), dtype=torch.float32, device=x.device) for m in mats]
+    pp = 0
+    if prepared is not None:
+        pp = _dev(prepared, torch.float32, "prepared").data_ptr()
+    _check(cq_prepare_matvec([m.struct for m in mats], x.data_ptr(), batch, pp,
+                             [y.data_ptr() for y in ys], _stream(stream)), "cq_prepare_matvec")
+    return ys

@@ -131,3 +131,23 @@ def test_f8_argmax_rejections():
     assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, W, need) == 8         # workspace over weights
     assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, Y + 4, K, need) == 8     # value inside y
     assert a(W, 16, 16, S, 1, 1, X, 9, Y, I, V, K, need) == 5
+
+
+def test_cq_set_rejections():
+    m = _m()
+    other = _m(packed=FAKE + (1 << 24), norms=FAKE + (1 << 25))
+    P, Y1, Y2 = FAKE + (1 << 30), FAKE + (1 << 31), FAKE + (1 << 32)
+    f = qmv.cq_matvec_multi
+    assert f([], P, 1, []) == 2                                    # nmats 0
+    assert f([m] * 9, P, 1, [Y1 + 65536 * i for i in range(9)]) == 2   # too many
+    assert f([m, _m(group=64)], P, 1, [Y1, Y2]) == 2               # group differs
+    assert f([m, _m(codebook=FAKE + 64)], P, 1, [Y1, Y2]) == 2     # codebook differs
+    assert f([m, other], P, 1, [Y1, 0]) == 1                        # missing output
+    assert f([m, other], P, 1, [Y1, Y1 + 64]) == 8                 # outputs overlap
+    assert f([m, other], P, 1, [Y1, FAKE + (1 << 24) + 16]) == 8   # output over packed rows
+    assert f([m, other], 0, 1, [Y1, Y2]) == 1
+    g = qmv.cq_prepare_matvec
+    X = FAKE + (1 << 33)
+    assert g([m, other], X, 1, X + 16, [Y1, Y2]) == 8               # prepared over x
+    assert g([m, other], 0, 1, P, [Y1, Y2]) == 1
+    assert g([m, other], X, 9, P, [Y1, Y2]) == 5
