@@ -618,6 +618,23 @@ def run_configs(args):
                              cq_gather_bytes(len(c.rows), c.input, c.input_padded, c.group,
                                              c.bits), med, best, k)
                     del packed, norms, mats
+            elif wl["kind"] == "i8":
+                f = synth.workload_inputs(name, batch=batch)
+                nb = f.R * f.C + f.R * ((f.C + 15) // 16) + 4 * batch * (f.C + f.R)
+                k = copies_for(f.R * f.C)
+                w = torch.from_numpy(f.w).to(dev)
+                ws = [w] + [w.clone() for _ in range(k - 1)]
+                s8 = torch.from_numpy(f.scale).to(dev)
+                x = torch.from_numpy(f.x).to(dev)
+                y = torch.empty((batch, f.R), device=dev)
+                calls = [(lambda wi: lambda sh: qmv.i8_matvec(
+                    wi.data_ptr(), f.R, f.C, s8.data_ptr(), x.data_ptr(), batch, y.data_ptr(),
+                    sh))(wi) for wi in ws]
+                if k == 1:
+                    calls = calls * 8
+                med, best = _graph_time(torch, calls, reps=10)
+                emit(name, batch, "i8_matvec", nb, med, best, k)
+                del ws, w
             else:
                 f = synth.workload_inputs(name, batch=batch)
                 nb = f8_bytes(f.R, f.C, f.SR, f.SC, batch)

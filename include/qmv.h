@@ -210,6 +210,24 @@ QMV_API qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8
                      int64_t SR, int64_t SC, const float *x, int32_t batch, float *y,
                      qmv_stream stream);
 
+/*
+ * i8_matvec -- ds4f-disk issue #6, step 4: the I8 matvec ("int8 widen,
+ * per-16-group E8M0 scales"; step 3's first tokens ran an I8 head):
+ *
+ *   y[v][r] = sum_c w[r][c] * e8m0(scale[r][c / 16]) * x[v][c]
+ *
+ * with groups of 16 consecutive columns of a row sharing one E8M0 scale
+ * (2^(e-127); code 255 is NaN).  Accumulated in float32; accuracy within
+ * 1e-4 * sum_c |w * s * x| + 1e-6 of the exact value.
+ *
+ *   w      [R, C] int8, R >= 0, C >= 1
+ *   scale  [R, ceil(C / 16)] E8M0 bytes
+ *   x      [batch, C] float32
+ *   y      [batch, R] float32, written
+ */
+QMV_API qmv_status i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                             const float *x, int32_t batch, float *y, qmv_stream stream);
+
 /* Bytes of device workspace f8_matvec_argmax needs for `batch` vectors: one
  * (value, row) partial result per block and vector, for at most
  * QMV_ARGMAX_MAX_BLOCKS blocks. */

@@ -15,7 +15,8 @@ Every function cites the page section it follows:
 * ``needle-1`` -- needle.js tutorial "Inference engine, part 1: loader and
   tokenizer": section 3 (FP16 decode) and section 4 (CqMatrix).
 * ``ds4f-6`` -- ds4f-disk issue #6 "attention + tokenizer + sampling",
-  work item 1 / step 1 (F8 E4M3 + E8M0 block-scaled matvec), work item 3 /
+  work item 1 / step 1 (F8 E4M3 + E8M0 block-scaled matvec), step 4 (I8
+  matvec with per-16 E8M0 group scales), work item 3 /
   step 3 (head logits then sampling: greedy selection).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
@@ -85,6 +86,10 @@ def _load():
     lib.orc_f8_matvec_mt.argtypes = [P, I64, I64, P, I64, I64, P, I64, P, P, I64, I64,
                                      ctypes.c_int]
     lib.orc_f8_matvec_mt.restype = ctypes.c_int
+    lib.orc_i8_matvec.argtypes = [P, I64, I64, P, P, I64, P, P, I64, I64]
+    lib.orc_i8_matvec.restype = ctypes.c_int
+    lib.orc_i8_matvec_mt.argtypes = [P, I64, I64, P, P, I64, P, P, I64, I64, ctypes.c_int]
+    lib.orc_i8_matvec_mt.restype = ctypes.c_int
     lib.orc_argmax_f32.argtypes = [P, I64]
     lib.orc_argmax_f32.restype = I64
     _lib = lib
@@ -256,3 +261,27 @@ def argmax_rows(y) -> np.ndarray:
     y = _c(np.atleast_2d(y), np.float32)
     lib = _load()
     return np.array([lib.orc_argmax_f32(_ptr(row), row.size) for row in y], dtype=np.int64)
+
+
+def i8_matvec(w, scale, x, rows=None, threads: int = 1, with_mag: bool = True):
+    """I8 matvec with per-16 E8M0 group scales (ds4f-6 step 4) in float64.
+
+    ``w`` [R, C] int8, ``scale`` [R, ceil(C/16)] uint8 E8M0, ``x`` [batch, C]
+    float32.  Returns (y, mag) [batch, R] float64."""
+    w = _c(w, np.int8)
+    scale = _c(scale, np.uint8)
+    x = _c(np.atleast_2d(x), np.float32)
+    R, C = w.shape
+    assert scale.shape == (R, (C + 15) // 16)
+    batch = x.shape[0]
+    r0, r1 = (0, R) if rows is None else rows
+    y = np.zeros((batch, R), dtype=np.float64)
+    mag = np.zeros((batch, R), dtype=np.float64) if with_mag else None
+    args = (_ptr(w), R, C, _ptr(scale), _ptr(x), batch, _ptr(y), _ptr(mag) if with_mag else None,
+            r0, r1)
+    lib = _load()
+    if threads > 1:
+        lib.orc_i8_matvec_mt(*args, threads)
+    else:
+        lib.orc_i8_matvec(*args)
+    return y, mag

@@ -278,6 +278,37 @@ ORC_API int orc_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t 
 }
 
 /* ------------------------------------------------------------------------ */
+/* I8 matvec with per-16 E8M0 group scales, [ds4f-6] step 4 ("I8 matvec     */
+/* (int8 widen, per-16-group E8M0 scales)").  Read as: groups of 16          */
+/* consecutive columns of a row share one scale; scale is [R, ceil(C/16)].  */
+/*   y[v,r] = sum_c w[r,c] * e8m0(scale[r][c/16]) * x[v,c]                   */
+/* in float64 for rows [r0, r1); mag = sum_c |w * s * x|.                    */
+/* ------------------------------------------------------------------------ */
+
+ORC_API int orc_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                          const float *x, int64_t batch, double *y, double *mag, int64_t r0,
+                          int64_t r1)
+{
+    int64_t ngroups = (C + 15) / 16;
+    for (int64_t r = r0; r < r1; r++)
+        for (int64_t v = 0; v < batch; v++) {
+            const float *xv = x + v * C;
+            double sum = 0.0, abs_sum = 0.0;
+            for (int64_t c = 0; c < C; c++) {
+                double term = (double)w[r * C + c] *
+                              (double)orc_e8m0_to_f32(scale[r * ngroups + c / 16]) * (double)xv[c];
+                sum += term;
+                abs_sum += fabs(term);
+            }
+            y[v * R + r] = sum;
+            if (mag)
+                mag[v * R + r] = abs_sum;
+        }
+    (void)R;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Greedy selection over one vector of head outputs (ds4f-6 work item 3 and  */
 /* step 3: logits = head x state, then sampling; greedy = temperature 0).    */
 /* Order: NaN above every number, larger above smaller, then the lower       */
@@ -307,7 +338,7 @@ ORC_API int64_t orc_argmax_f32(const float *y, int64_t n)
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
-    int kind; /* 0 = cq, 1 = f8 */
+    int kind; /* 0 = cq, 1 = f8, 2 = i8 */
     const orc_cq *m;
     const double *prepared;
     const uint8_t *w, *scale;
@@ -323,8 +354,11 @@ static void *orc_run_job(void *arg)
     orc_job *j = (orc_job *)arg;
     if (j->kind == 0)
         orc_cq_matvec(j->m, j->prepared, j->batch, j->y, j->mag, j->r0, j->r1);
-    else
+    else if (j->kind == 1)
         orc_f8_matvec(j->w, j->R, j->C, j->scale, j->SR, j->SC, j->x, j->batch, j->y, j->mag,
+                      j->r0, j->r1);
+    else
+        orc_i8_matvec((const int8_t *)j->w, j->R, j->C, j->scale, j->x, j->batch, j->y, j->mag,
                       j->r0, j->r1);
     return NULL;
 }
@@ -381,6 +415,24 @@ ORC_API int orc_f8_matvec_mt(const uint8_t *w, int64_t R, int64_t C, const uint8
     j.scale = scale;
     j.SR = SR;
     j.SC = SC;
+    j.x = x;
+    j.batch = batch;
+    j.y = y;
+    j.mag = mag;
+    return orc_run_threads(j, r0, r1, nthreads);
+}
+
+ORC_API int orc_i8_matvec_mt(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                             const float *x, int64_t batch, double *y, double *mag, int64_t r0,
+                             int64_t r1, int nthreads)
+{
+    orc_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 2;
+    j.w = (const uint8_t *)w;
+    j.R = R;
+    j.C = C;
+    j.scale = scale;
     j.x = x;
     j.batch = batch;
     j.y = y;

@@ -1,0 +1,314 @@
+// i8_kernels.cu -- int8-weight matvec with per-16 E8M0 group scales, sm_103a.
+//
+// Method: ds4f-disk issue #6 "attention + tokenizer + sampling", step 4 (the
+// I8 matvec of simd.c: int8 weights widened, E8M0 scales per group of 16)
+// and the first real tokens of step 3, which ran an I8 head over the 246k
+// vocabulary.  Groups are 16 consecutive columns of a row; scale is
+// [R, ceil(C/16)] row-major; code 255 is NaN, every other code 2^(e-127).
+//
+//   y[v][r] = sum_c w[r][c] * e8m0(scale[r][c/16]) * x[v][c]
+//
+// The fast kernel streams rows like the F8 one (grid-stride tiles of T rows,
+// lane l on the 16-byte chunks l, l+32, ...), so each lane's chunk is exactly
+// one scale group: the 16 products of a chunk are summed, then multiplied by
+// the group's scale once.  int8 -> float32 is exact: the byte is biased to
+// unsigned, permuted into the low mantissa byte of 2^23 (0x4B0000uu) and
+// 2^23 + 128 is subtracted.
+#include <stdint.h>
+
+#include "qmv_internal.h"
+
+namespace qmv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+struct I8Args {
+    const int8_t *w;
+    const uint8_t *scale;
+    const float *x;
+    float *y;
+    int64_t R, C, SG;  // SG = ceil(C / 16) scale groups per row
+};
+
+__device__ __forceinline__ float e8m0_scale(unsigned e) {
+    if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, subnormal
+    if (e == 255) return __uint_as_float(0x7fc00000u);
+    return __uint_as_float(e << 23);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;
+}
+
+// The four int8 weights of a word as exact floats.
+__device__ __forceinline__ void widen4(unsigned word, float (&f)[4]) {
+    const unsigned u = word ^ 0x80808080u;
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+        f[k] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u | unsigned(k))) - 8388736.0f;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const int8_t *p) {
+    uint4 d;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+        : "l"(p));
+    return d;
+}
+
+__device__ __forceinline__ unsigned word_of(const uint4 &d, int q) {
+    return q == 0 ? d.x : q == 1 ? d.y : q == 2 ? d.z : d.w;
+}
+
+// Accumulators: one float per (row, vector) at batch 1; larger batches keep
+// (even column, odd column) pairs and use the packed FMA (fma.rn.f32x2).
+template <int B>
+struct Acc {
+    typedef float2 type;
+};
+template <>
+struct Acc<1> {
+    typedef float type;
+};
+__device__ __forceinline__ float total(float v) { return v; }
+__device__ __forceinline__ float total(float2 v) { return v.x + v.y; }
+__device__ __forceinline__ void zero(float &v) { v = 0.0f; }
+__device__ __forceinline__ void zero(float2 &v) { v = make_float2(0.0f, 0.0f); }
+
+// The T weight chunks (and their scale bytes) of one step; rows past the
+// tile's end and chunks past the row's end re-read in-bounds data (unused).
+template <int T>
+__device__ __forceinline__ void load_step(uint4 (&d)[T], unsigned (&e)[T], const I8Args &a, int64_t r0,
+                                          int rows, int64_t ch, int64_t nchunk) {
+    const int64_t chc = ch < nchunk ? ch : nchunk - 1;
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        const int64_t r = r0 + (t < rows ? t : rows - 1);
+        d[t] = ld_stream(a.w + r * a.C + chc * 16);
+        e[t] = __ldg(a.scale + r * a.SG + chc);
+    }
+}
+
+// The four int8 weights of a word as two exact float pairs, with packed
+// additions of -(2^23 + 128).
+__device__ __forceinline__ void widen4_pairs(unsigned word, float2 &w01, float2 &w23) {
+    const unsigned u = word ^ 0x80808080u;
+    const float2 k = make_float2(-8388736.0f, -8388736.0f);
+    w01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441u))), k);
+    w23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442u)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443u))), k);
+}
+
+// acc[t][v] += e8m0(e[t]) * sum over chunk ch of w[t] * x[v].  Scalar FMAs
+// at batch 1, column-paired packed FMAs otherwise.
+template <int B, int T>
+__device__ __forceinline__ void compute_step(typename Acc<B>::type (&acc)[T][B], const uint4 (&d)[T],
+                                             const unsigned (&e)[T], const I8Args &a, int64_t ch) {
+    constexpr bool SCALAR = (B == 1);
+    typename Acc<B>::type part[T][B];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int v = 0; v < B; v++) zero(part[t][v]);
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        float4 xv[B];
+#pragma unroll
+        for (int v = 0; v < B; v++)
+            xv[v] = __ldg(reinterpret_cast<const float4 *>(a.x + v * a.C + ch * 16 + 4 * q));
+#pragma unroll
+        for (int t = 0; t < T; t++) {
+            if constexpr (SCALAR) {
+                float f[4];
+                widen4(word_of(d[t], q), f);
+                part[t][0] = fmaf(f[0], xv[0].x, part[t][0]);
+                part[t][0] = fmaf(f[1], xv[0].y, part[t][0]);
+                part[t][0] = fmaf(f[2], xv[0].z, part[t][0]);
+                part[t][0] = fmaf(f[3], xv[0].w, part[t][0]);
+            } else {
+                float2 w01, w23;
+                widen4_pairs(word_of(d[t], q), w01, w23);
+#pragma unroll
+                for (int v = 0; v < B; v++) {
+                    part[t][v] = __ffma2_rn(w01, make_float2(xv[v].x, xv[v].y), part[t][v]);
+                    part[t][v] = __ffma2_rn(w23, make_float2(xv[v].z, xv[v].w), part[t][v]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        const float s = e8m0_scale(e[t]);
+#pragma unroll
+        for (int v = 0; v < B; v++) {
+            if constexpr (SCALAR)
+                acc[t][0] = fmaf(part[t][0], s, acc[t][0]);
+            else
+                acc[t][v] = __ffma2_rn(part[t][v], make_float2(s, s), acc[t][v]);
+        }
+    }
+}
+
+template <int B, int T>
+__device__ __forceinline__ void finish_tile(typename Acc<B>::type (&acc)[T][B], const I8Args &a,
+                                            int64_t r0, int rows, int lane) {
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+#pragma unroll
+        for (int v = 0; v < B; v++) {
+            const float val = warp_sum(total(acc[t][v]));
+            zero(acc[t][v]);
+            if (t < rows && lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Streaming kernel (C % 16 == 0, 16-byte aligned w and x): grid-stride tiles
+// of T rows, one step = the T chunks a lane owns in one 512-byte column band.
+// ---------------------------------------------------------------------------
+template <int B, int T>
+__global__ void __launch_bounds__(256, (B == 1) ? 0 : ((B <= 4) ? 2 : 1)) i8_fast_kernel(I8Args a) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunk = a.C >> 4;
+    const int iters = int((nchunk + 31) >> 5);
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    const int64_t tile_stride = nwarps * T;
+    int64_t r0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * T;
+    if (r0 >= a.R) return;
+    int rows = int(min(int64_t(T), a.R - r0));
+    typename Acc<B>::type acc[T][B];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int v = 0; v < B; v++) zero(acc[t][v]);
+    for (int j = 0;;) {
+        uint4 d[T];
+        unsigned e[T];
+        const int64_t ch = lane + 32 * int64_t(j);
+        load_step<T>(d, e, a, r0, rows, ch, nchunk);
+        if (ch < nchunk) compute_step<B, T>(acc, d, e, a, ch);
+        if (++j == iters) {
+            finish_tile<B, T>(acc, a, r0, rows, lane);
+            r0 += tile_stride;
+            if (r0 >= a.R) break;
+            rows = int(min(int64_t(T), a.R - r0));
+            j = 0;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Small-matrix kernel: 2-row tiles, all NSTEP chunk steps of a tile loaded at
+// once (too few rows to keep a streaming grid busy).
+// ---------------------------------------------------------------------------
+template <int B, int T, int NSTEP>
+__global__ void __launch_bounds__(256) i8_rows_kernel(I8Args a) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunk = a.C >> 4;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    const int64_t ntiles = (a.R + T - 1) / T;
+    typename Acc<B>::type acc[T][B];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int v = 0; v < B; v++) zero(acc[t][v]);
+    for (int64_t tile = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tile < ntiles;
+         tile += nwarps) {
+        const int64_t r0 = tile * T;
+        const int rows = int(min(int64_t(T), a.R - r0));
+        for (int64_t base = 0; base < nchunk; base += 32 * NSTEP) {
+            uint4 d[NSTEP][T];
+            unsigned e[NSTEP][T];
+#pragma unroll
+            for (int st = 0; st < NSTEP; st++)
+                load_step<T>(d[st], e[st], a, r0, rows, base + lane + 32 * st, nchunk);
+#pragma unroll
+            for (int st = 0; st < NSTEP; st++) {
+                const int64_t ch = base + lane + 32 * st;
+                if (ch < nchunk) compute_step<B, T>(acc, d[st], e[st], a, ch);
+            }
+        }
+        finish_tile<B, T>(acc, a, r0, rows, lane);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// General kernel: any C and alignment.  One warp per row, one element per
+// lane step: (w * scale) * x in a float32 FMA.
+// ---------------------------------------------------------------------------
+template <int B>
+__global__ void __launch_bounds__(256) i8_general_kernel(I8Args a) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < a.R; r += nwarps) {
+        const int8_t *wr = a.w + r * a.C;
+        const uint8_t *sr = a.scale + r * a.SG;
+        float acc[B];
+#pragma unroll
+        for (int v = 0; v < B; v++) acc[v] = 0.0f;
+        for (int64_t c = lane; c < a.C; c += 32) {
+            const float ws = float(__ldg(wr + c)) * e8m0_scale(__ldg(sr + (c >> 4)));
+#pragma unroll
+            for (int v = 0; v < B; v++) acc[v] = fmaf(ws, __ldg(a.x + v * a.C + c), acc[v]);
+        }
+#pragma unroll
+        for (int v = 0; v < B; v++) {
+            const float val = warp_sum(acc[v]);
+            if (lane == 0) a.y[int64_t(v) * a.R + r] = val;
+        }
+    }
+}
+
+template <int B>
+qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
+    const bool fast = (a.C % 16 == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) &&
+                      (reinterpret_cast<uintptr_t>(a.x) % 16 == 0);
+    if (!fast) {
+        const void *kp = reinterpret_cast<const void *>(i8_general_kernel<B>);
+        const int blocks = grid_blocks(kp, 256, 0, a.R);
+        return from_cuda(launch_pdl(i8_general_kernel<B>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
+    }
+    // Four rows per tile at every batch: eight (the F8 kernel's choice at
+    // batch 1) ran 25% slower here.
+    constexpr int T = 4;
+    const void *kp = reinterpret_cast<const void *>(i8_fast_kernel<B, T>);
+    const int64_t capacity = int64_t(occupancy(kp, 256, 0)) * sm_count() * 8;
+    if ((a.R + T - 1) / T < 4 * capacity) {
+        constexpr int TS = 2, NSTEP = (B <= 2) ? 8 : 4;
+        const void *rp = reinterpret_cast<const void *>(i8_rows_kernel<B, TS, NSTEP>);
+        const int blocks = grid_blocks(rp, 256, 0, (a.R + TS - 1) / TS);
+        return from_cuda(launch_pdl(i8_rows_kernel<B, TS, NSTEP>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
+    }
+    const int blocks = grid_blocks(kp, 256, 0, (a.R + T - 1) / T);
+    return from_cuda(launch_pdl(i8_fast_kernel<B, T>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
+}
+
+}  // namespace
+
+qmv_status launch_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale, const float *x,
+                            int batch, float *y, cudaStream_t s) {
+    I8Args a{w, scale, x, y, R, C, (C + 15) / 16};
+    switch (batch) {
+        case 1: return launch_i8<1>(a, s);
+        case 2: return launch_i8<2>(a, s);
+        case 3: return launch_i8<3>(a, s);
+        case 4: return launch_i8<4>(a, s);
+        case 5: return launch_i8<5>(a, s);
+        case 6: return launch_i8<6>(a, s);
+        case 7: return launch_i8<7>(a, s);
+        default: return launch_i8<8>(a, s);
+    }
+}
+
+}  // namespace qmv

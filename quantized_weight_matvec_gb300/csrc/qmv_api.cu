@@ -343,6 +343,24 @@ qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_
                                         workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+qmv_status i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale, const float *x,
+                     int32_t batch, float *y, qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (R < 0 || R > kMaxDim || C < 1 || C > kMaxDim) return QMV_ERR_SHAPE;
+    int64_t wb = 0, sb = 0, xb = 0, yb = 0;
+    if (!mul_ok(R, C, &wb) || !mul_ok(R, (C + 15) / 16, &sb) || !mul_ok(int64_t(batch) * 4, C, &xb) ||
+        !mul_ok(int64_t(batch) * 4, R, &yb))
+        return QMV_ERR_OVERFLOW;
+    if (!x) return QMV_ERR_NULL;
+    if (R > 0 && (!w || !scale || !y)) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(y, 4)) return QMV_ERR_ALIGN;
+    if (overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb) || overlaps(y, yb, x, xb))
+        return QMV_ERR_ALIAS;
+    if (R == 0) return QMV_OK;
+    return qmv::launch_i8_matvec(w, R, C, scale, x, batch, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
 qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
                      int64_t SC, const float *x, int32_t batch, float *y, qmv_stream stream) {
     qmv_status st = check_batch(batch);

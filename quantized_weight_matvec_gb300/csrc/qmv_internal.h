@@ -76,6 +76,10 @@ qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, c
 // Whether cq_prepare_matvec can prepare on chip (else it runs two launches).
 bool cq_fused_fits(const qmv_cq_matrix &m, int batch);
 
+// ---- I8 ------------------------------------------------------------------
+qmv_status launch_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                            const float *x, int batch, float *y, cudaStream_t s);
+
 // ---- F8 ------------------------------------------------------------------
 qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                             int64_t SR, int64_t SC, const float *x, int batch, float *y,

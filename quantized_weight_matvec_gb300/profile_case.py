@@ -2,7 +2,8 @@
 
   python -m quantized_weight_matvec_gb300.profile_case --kernel f8 --rows 65536 --iters 3
 
-Kernels: f8 (E4M3 head-shaped rows x 4096, scales [rows/128, 32]), cq2
+Kernels: f8 (E4M3 head-shaped rows x 4096, scales [rows/128, 32]), i8
+(int8 rows x 4096, per-16 E8M0 group scales), cq2
 (2-bit rows x 512, group 128), gather (64 rows of a 32768 x 512 2-bit
 matrix), prepare.  Inputs are seeded synthetic data; the case is chosen
 larger than L2 but a few hundred MB at most.  Prints one checksum line and
@@ -19,7 +20,7 @@ from . import qmv, synth
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["f8", "cq2", "gather", "prepare"], required=True)
+    ap.add_argument("--kernel", choices=["f8", "i8", "cq2", "gather", "prepare"], required=True)
     ap.add_argument("--rows", type=int, default=65536)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--iters", type=int, default=3)
@@ -33,6 +34,13 @@ def main(argv=None):
         y = torch.empty((args.batch, args.rows), device=dev)
         for _ in range(args.iters):
             qmv.f8_matvec_t(w, s, x, out=y)
+        out = y
+    elif args.kernel == "i8":
+        f = synth.i8_inputs(7, args.rows, 4096, 110, 124, batch=args.batch)
+        w, s, x = (torch.from_numpy(a).to(dev) for a in (f.w, f.scale, f.x))
+        y = torch.empty((args.batch, args.rows), device=dev)
+        for _ in range(args.iters):
+            qmv.i8_matvec_t(w, s, x, out=y)
         out = y
     else:
         rows = args.rows if args.kernel == "cq2" else 32768

@@ -75,10 +75,11 @@ def load() -> ctypes.CDLL:
     lib.cq_matvec_multi.argtypes = [CQP, I32, P, I32, P, P]
     lib.cq_prepare_matvec.argtypes = [CQP, I32, P, I32, P, P, P]
     lib.f8_matvec.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P]
+    lib.i8_matvec.argtypes = [P, I64, I64, P, P, I32, P, P]
     lib.f8_matvec_argmax.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P, I64, P]
     lib.f8_matvec_argmax_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P]
     for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.cq_matvec_multi,
-               lib.cq_prepare_matvec, lib.f8_matvec, lib.f8_matvec_argmax,
+               lib.cq_prepare_matvec, lib.f8_matvec, lib.i8_matvec, lib.f8_matvec_argmax,
                lib.f8_matvec_argmax_noalloc):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
@@ -144,6 +145,12 @@ def cq_dequantize_row(m: CQMatrixStruct, rows: int, n: int, out: int, dev_status
 def f8_matvec(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: int, batch: int, y: int,
               stream: int = 0) -> int:
     return load().f8_matvec(w or None, R, C, scale or None, SR, SC, x or None, batch, y or None,
+                            stream or None)
+
+
+def i8_matvec(w: int, R: int, C: int, scale: int, x: int, batch: int, y: int,
+              stream: int = 0) -> int:
+    return load().i8_matvec(w or None, R, C, scale or None, x or None, batch, y or None,
                             stream or None)
 
 
@@ -334,3 +341,21 @@ def cq_prepare_matvec_t(mats, x, prepared=None, stream=None):
     _check(cq_prepare_matvec([m.struct for m in mats], x.data_ptr(), batch, pp,
                              [y.data_ptr() for y in ys], _stream(stream)), "cq_prepare_matvec")
     return ys
+
+
+def i8_matvec_t(w, scale, x, out=None, stream=None):
+    """y[B, R] = i8_matvec(w[R, C] int8, scale[R, ceil(C/16)] uint8, x[B, C])."""
+    torch = _torch()
+    w = _dev(w, torch.int8, "w")
+    scale = _dev(scale, torch.uint8, "scale")
+    x = _dev(x, torch.float32, "x")
+    R, C = w.shape
+    if tuple(scale.shape) != (R, (C + 15) // 16):
+        raise ValueError("scale must be [R, ceil(C/16)]")
+    batch = x.shape[0] if x.dim() == 2 else 1
+    if out is None:
+        out = torch.empty((batch, R), dtype=torch.float32, device=w.device)
+    _dev(out, torch.float32, "out")
+    _check(i8_matvec(w.data_ptr(), R, C, scale.data_ptr(), x.data_ptr(), batch, out.data_ptr(),
+                     _stream(stream)), "i8_matvec")
+    return out

@@ -18,6 +18,10 @@ Workloads (the shapes named by the pages' CQ and F8 formats):
                     exponents in [120, 130], batch 1 and 8.
 * ``f8_head``       F8 E4M3 head shape, 245760 x 4096 (~1 GB), scales
                     [1920, 32] with exponents in [118, 132], batch 1/2/4/8.
+* ``i8_4096``       I8, 4096 x 4096, per-16 E8M0 group scales with
+                    exponents in [110, 124], batch 1 and 8.
+* ``i8_head``       I8 head shape (the run's "I8 head (246k vocab)"),
+                    245760 x 4096, batch 1 and 8.
 
 Packed CQ rows are drawn as uniform random bytes: for every bit width this
 makes every index uniform over [0, 2^bits) (the 2/4-bit layouts are two
@@ -46,6 +50,8 @@ WORKLOADS = {
                     batch=(1, 8)),
     "f8_head": dict(kind="f8", seed=5, R=245760, C=4096, SR=1920, SC=32, e_lo=118, e_hi=132,
                     batch=(1, 2, 4, 8)),
+    "i8_4096": dict(kind="i8", seed=6, R=4096, C=4096, e_lo=110, e_hi=124, batch=(1, 8)),
+    "i8_head": dict(kind="i8", seed=7, R=245760, C=4096, e_lo=110, e_hi=124, batch=(1, 8)),
 }
 
 
@@ -138,6 +144,26 @@ def f8_inputs(seed: int, R: int, C: int, SR: int, SC: int, e_lo: int, e_hi: int,
     return F8Inputs(R, C, SR, SC, w, scale, x)
 
 
+@dataclass
+class I8Inputs:
+    R: int
+    C: int
+    w: np.ndarray       # [R, C] int8
+    scale: np.ndarray   # [R, ceil(C/16)] uint8 E8M0 codes
+    x: np.ndarray       # [batch, C] float32
+
+
+def i8_inputs(seed: int, R: int, C: int, e_lo: int, e_hi: int, batch: int = 1) -> I8Inputs:
+    """Seeded int8 weights (uniform over [-128, 127]), per-16 E8M0 group scales
+    (uniform integers in [e_lo, e_hi]) and x ~ N(0,1)."""
+    ss = np.random.SeedSequence([int(seed), int(R), int(C), int(batch), 8])
+    g_w, g_s, g_x = (np.random.default_rng(s) for s in ss.spawn(3))
+    w = g_w.integers(-128, 128, size=(R, C), dtype=np.int8)
+    scale = g_s.integers(e_lo, e_hi + 1, size=(R, (C + 15) // 16), dtype=np.int64).astype(np.uint8)
+    x = g_x.standard_normal((batch, C)).astype(np.float32)
+    return I8Inputs(R, C, w, scale, x)
+
+
 def workload_inputs(name: str, bits: int | None = None, batch: int = 1):
     """Inputs for one named workload at one bit width / batch."""
     w = WORKLOADS[name]
@@ -145,4 +171,6 @@ def workload_inputs(name: str, bits: int | None = None, batch: int = 1):
         b = w["bits"][0] if bits is None else bits
         return cq_inputs(w["seed"], w["output"], w["input"], w["group"], b, batch,
                          w["x_scale"], w.get("gather", 0))
+    if w["kind"] == "i8":
+        return i8_inputs(w["seed"], w["R"], w["C"], w["e_lo"], w["e_hi"], batch)
     return f8_inputs(w["seed"], w["R"], w["C"], w["SR"], w["SC"], w["e_lo"], w["e_hi"], batch)

@@ -151,3 +151,17 @@ def test_cq_set_rejections():
     assert g([m, other], X, 1, X + 16, [Y1, Y2]) == 8               # prepared over x
     assert g([m, other], 0, 1, P, [Y1, Y2]) == 1
     assert g([m, other], X, 9, P, [Y1, Y2]) == 5
+
+
+def test_i8_rejections():
+    W, S, X, Y = FAKE, FAKE + (1 << 30), FAKE + (1 << 31), FAKE + (1 << 32)
+    f = qmv.i8_matvec
+    assert f(W, 16, 16, S, X, 0, Y) == 5
+    assert f(W, 16, 0, S, X, 1, Y) == 2
+    assert f(W, -1, 16, S, X, 1, Y) == 2
+    assert f(W, 16, 16, 0, X, 1, Y) == 1
+    assert f(W, 16, 16, S, 0, 1, Y) == 1
+    assert f(W, 16, 16, S, X + 2, 1, Y) == 6
+    assert f(W, 16, 16, S, X, 1, W + 8) == 8
+    assert f(W, 16, 16, S, X, 1, S) == 8
+    assert f(W, 0, 16, S, X, 1, 0) == 0

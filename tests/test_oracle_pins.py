@@ -400,3 +400,31 @@ def test_argmax_hand_cases():
     assert list(oracle.argmax_rows(np.array([[1, 3, 3, 2], [np.nan, 5, np.nan, 9]],
                                             np.float32))) == [1, 0]
     assert oracle.argmax_rows(np.array([[-np.inf, -np.inf]], np.float32))[0] == 0
+
+
+# ---------------------------------------------------------------------------
+# I8 matvec with per-16 E8M0 group scales
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R,C", [(5, 16), (7, 37), (3, 1), (40, 100)])
+def test_i8_matches_expanded_group_scales(R, C):
+    f = synth.i8_inputs(R + C, R, C, 100, 140, batch=3)
+    y, mag = oracle.i8_matvec(f.w, f.scale, f.x)
+    S = np.exp2(np.repeat(f.scale.astype(np.float64), 16, axis=1)[:, :C] - 127)
+    W = f.w.astype(np.float64) * S
+    assert np.allclose(y, f.x.astype(np.float64) @ W.T, rtol=1e-13, atol=1e-300)
+    assert np.allclose(mag, np.abs(f.x.astype(np.float64)) @ np.abs(W).T, rtol=1e-13)
+
+
+def test_i8_hand_cases():
+    # one group of 16 weights (1..16) at scale 2^1, x = 1: y = 2 * 136
+    w = np.arange(1, 17, dtype=np.int8)[None, :]
+    y, _ = oracle.i8_matvec(w, np.array([[128]], np.uint8), np.ones((1, 16), np.float32))
+    assert y[0, 0] == 272.0
+    # the 17th column starts a new group: its scale alone changes y
+    w = np.zeros((1, 17), np.int8)
+    w[0, 16] = -128
+    y, _ = oracle.i8_matvec(w, np.array([[127, 130]], np.uint8), np.ones((1, 17), np.float32))
+    assert y[0, 0] == -1024.0
+    y, _ = oracle.i8_matvec(w, np.array([[127, 255]], np.uint8), np.ones((1, 17), np.float32))
+    assert np.isnan(y[0, 0])
