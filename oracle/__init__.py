@@ -90,6 +90,9 @@ def _load():
     lib.orc_i8_matvec.restype = ctypes.c_int
     lib.orc_i8_matvec_mt.argtypes = [P, I64, I64, P, P, I64, P, P, I64, I64, ctypes.c_int]
     lib.orc_i8_matvec_mt.restype = ctypes.c_int
+    lib.orc_silu_f64.argtypes, lib.orc_silu_f64.restype = [ctypes.c_double], ctypes.c_double
+    lib.orc_hadamard_mlp.argtypes = [P, I64, I64, P, P, P, P, P, I64, ctypes.c_int, P, P, P]
+    lib.orc_hadamard_mlp.restype = ctypes.c_int
     lib.orc_argmax_f32.argtypes = [P, I64]
     lib.orc_argmax_f32.restype = I64
     _lib = lib
@@ -285,3 +288,39 @@ def i8_matvec(w, scale, x, rows=None, threads: int = 1, with_mag: bool = True):
     else:
         lib.orc_i8_matvec(*args)
     return y, mag
+
+
+def silu_f64(v) -> np.ndarray:
+    """silu(v) = v / (1 + e^-v) in float64, elementwise (the activation of
+    needle-2 section 8)."""
+    v = np.asarray(v, dtype=np.float64)
+    lib = _load()
+    return np.array([lib.orc_silu_f64(float(t)) for t in v.ravel()]).reshape(v.shape)
+
+
+def hadamard_mlp(x, D: int, d1, d2, d3, residual=None, u=None, mode: str = "f32"):
+    """Hadamard MLP block of needle-2 section 8 from the normalised block input:
+    pad to D, x d1, normalised FWHT, silu(d2 x .), normalised FWHT, x d3,
+    first n values, then + residual and - u when given.
+
+    ``x`` [batch, n] float32; d1..d3 [D] float32.  mode "f32" follows the
+    page's Float32Array staging and returns float32; "f64" is float64
+    throughout.  Returns (out, mag), both [batch, n]."""
+    x = _c(np.atleast_2d(x), np.float32)
+    batch, n = x.shape
+    d1, d2, d3 = (_c(d, np.float32) for d in (d1, d2, d3))
+    assert d1.shape == d2.shape == d3.shape == (D,) and n <= D
+    res = None if residual is None else _c(np.atleast_2d(residual), np.float32)
+    uu = None if u is None else _c(np.atleast_2d(u), np.float32)
+    for t in (res, uu):
+        assert t is None or t.shape == (batch, n)
+    m = 0 if mode == "f32" else 1
+    out32 = np.zeros((batch, n), dtype=np.float32)
+    out64 = np.zeros((batch, n), dtype=np.float64)
+    mag = np.zeros((batch, n), dtype=np.float64)
+    st = _load().orc_hadamard_mlp(_ptr(x), n, D, _ptr(d1), _ptr(d2), _ptr(d3),
+                                  None if res is None else _ptr(res),
+                                  None if uu is None else _ptr(uu), batch, m,
+                                  _ptr(out32), _ptr(out64), _ptr(mag))
+    assert st == 0
+    return (out32 if m == 0 else out64), mag

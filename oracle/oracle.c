@@ -15,7 +15,7 @@
  *
  * Citations name the page and its section:
  *   [needle-2] "Inference engine, part 2: kernels and token step"
- *              (needle.js tutorial), sections 1-3 and "Row gather".
+ *              (needle.js tutorial), sections 1-3, "Row gather" and 8.
  *   [needle-1] "Inference engine, part 1: loader and tokenizer"
  *              (needle.js tutorial), sections 3-4.
  *   [ds4f-6]   "attention + tokenizer + sampling: the path to real text
@@ -305,6 +305,98 @@ ORC_API int orc_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *
                 mag[v * R + r] = abs_sum;
         }
     (void)R;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Hadamard MLP block, [needle-2] section 8, from the padded normalised     */
+/* block input on:                                                            */
+/*   z = pad(x, D); z *= d1; normalizedFwht(z); z = silu(d2 * z);             */
+/*   normalizedFwht(z); z *= d3; out = (residual + z[:n]) - u                 */
+/* normalizedFwht is the section-1 butterfly over the whole length D         */
+/* followed by the product with 1/sqrt(D), as in prepare.  silu(v) =         */
+/* v / (1 + e^-v).                                                           */
+/* ------------------------------------------------------------------------ */
+
+ORC_API double orc_silu_f64(double v)
+{
+    return v / (1.0 + exp(-v));
+}
+
+/* mode 0: the page's staging.  z is a Float32Array, so every stored value
+ *         is rounded to float32: the diagonal products (float32 x float32,
+ *         exact in float64, then rounded), each butterfly result, the
+ *         1/sqrt(D) products, and silu, which takes the exact float64
+ *         product d2 * z and is evaluated in float64.  The residual sum and
+ *         the update difference are float32 array stores too.
+ * mode 1: float64 throughout; out64 receives the result.
+ * x, residual, u and out are [batch, n]; d1, d2, d3 are [D]; residual and
+ * u may be NULL (the term is left out).  mag (may be NULL) receives, per
+ * output, |d3| / sqrt(D) * sum_j |silu_j| + |residual| + |u|: the size of
+ * the terms the last transform and the epilogue combine. */
+ORC_API int orc_hadamard_mlp(const float *x, int64_t n, int64_t D, const float *d1,
+                             const float *d2, const float *d3, const float *residual,
+                             const float *u, int64_t batch, int mode, float *out32,
+                             double *out64, double *mag)
+{
+    double s = inv_sqrt_group(D);
+    float *z32 = (float *)malloc((size_t)D * sizeof(float));
+    double *z64 = (double *)malloc((size_t)D * sizeof(double));
+    if (!z32 || !z64) {
+        free(z32);
+        free(z64);
+        return -1;
+    }
+    for (int64_t v = 0; v < batch; v++) {
+        const float *xv = x + v * n;
+        double silu_abs = 0.0;
+        if (mode == 0) {
+            for (int64_t i = 0; i < D; i++)
+                z32[i] = (float)((double)(i < n ? xv[i] : 0.0f) * (double)d1[i]);
+            orc_fwht_f32(z32, D);
+            for (int64_t i = 0; i < D; i++)
+                z32[i] = (float)((double)z32[i] * s);
+            for (int64_t i = 0; i < D; i++) {
+                z32[i] = (float)orc_silu_f64((double)d2[i] * (double)z32[i]);
+                silu_abs += fabs((double)z32[i]);
+            }
+            orc_fwht_f32(z32, D);
+            for (int64_t i = 0; i < D; i++)
+                z32[i] = (float)((double)z32[i] * s);
+            for (int64_t i = 0; i < n; i++) {
+                float o = (float)((double)z32[i] * (double)d3[i]);
+                if (residual)
+                    o = (float)((double)residual[v * n + i] + (double)o);
+                if (u)
+                    o = (float)((double)o - (double)u[v * n + i]);
+                out32[v * n + i] = o;
+            }
+        } else {
+            for (int64_t i = 0; i < D; i++)
+                z64[i] = (i < n ? (double)xv[i] : 0.0) * (double)d1[i];
+            orc_fwht_f64(z64, D);
+            for (int64_t i = 0; i < D; i++) {
+                z64[i] = orc_silu_f64((double)d2[i] * (z64[i] * s));
+                silu_abs += fabs(z64[i]);
+            }
+            orc_fwht_f64(z64, D);
+            for (int64_t i = 0; i < n; i++) {
+                double o = z64[i] * s * (double)d3[i];
+                if (residual)
+                    o = (double)residual[v * n + i] + o;
+                if (u)
+                    o = o - (double)u[v * n + i];
+                out64[v * n + i] = o;
+            }
+        }
+        if (mag)
+            for (int64_t i = 0; i < n; i++)
+                mag[v * n + i] = fabs((double)d3[i]) * s * silu_abs +
+                                 (residual ? fabs((double)residual[v * n + i]) : 0.0) +
+                                 (u ? fabs((double)u[v * n + i]) : 0.0);
+    }
+    free(z32);
+    free(z64);
     return 0;
 }
 

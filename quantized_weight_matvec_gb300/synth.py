@@ -22,6 +22,13 @@ Workloads (the shapes named by the pages' CQ and F8 formats):
                     exponents in [110, 124], batch 1 and 8.
 * ``i8_head``       I8 head shape (the run's "I8 head (246k vocab)"),
                     245760 x 4096, batch 1 and 8.
+* ``hmlp_512``      Hadamard MLP block on the 512-value block input with no
+                    widening (D = 512), batch 1 and 4.
+* ``hmlp_2048``     the same block widened to D = 2048, batch 1, 4 and 8.
+
+Hadamard MLP inputs: x ~ N(0,1) (a normalised vector has unit RMS), the
+three diagonals uniform in magnitude over [0.5, 1.5] with random signs,
+residual and u ~ N(0,1).
 
 Packed CQ rows are drawn as uniform random bytes: for every bit width this
 makes every index uniform over [0, 2^bits) (the 2/4-bit layouts are two
@@ -52,6 +59,8 @@ WORKLOADS = {
                     batch=(1, 2, 4, 8)),
     "i8_4096": dict(kind="i8", seed=6, R=4096, C=4096, e_lo=110, e_hi=124, batch=(1, 8)),
     "i8_head": dict(kind="i8", seed=7, R=245760, C=4096, e_lo=110, e_hi=124, batch=(1, 8)),
+    "hmlp_512": dict(kind="hmlp", seed=8, n=512, D=512, batch=(1, 4)),
+    "hmlp_2048": dict(kind="hmlp", seed=9, n=512, D=2048, batch=(1, 4, 8)),
 }
 
 
@@ -164,6 +173,34 @@ def i8_inputs(seed: int, R: int, C: int, e_lo: int, e_hi: int, batch: int = 1) -
     return I8Inputs(R, C, w, scale, x)
 
 
+@dataclass
+class HMLPInputs:
+    n: int
+    D: int
+    x: np.ndarray         # [batch, n] float32
+    d1: np.ndarray        # [D] float32
+    d2: np.ndarray
+    d3: np.ndarray
+    residual: np.ndarray  # [batch, n] float32
+    u: np.ndarray         # [batch, n] float32
+
+
+def hmlp_inputs(seed: int, n: int, D: int, batch: int = 1) -> HMLPInputs:
+    """Seeded Hadamard MLP inputs.  Sub-streams: x, d1, d2, d3, residual, u."""
+    ss = np.random.SeedSequence([int(seed), int(n), int(D), int(batch), 9])
+    g = [np.random.default_rng(s) for s in ss.spawn(6)]
+
+    def diag(r):
+        mag = r.uniform(0.5, 1.5, D)
+        return np.where(r.random(D) < 0.5, -mag, mag).astype(np.float32)
+
+    x = g[0].standard_normal((batch, n)).astype(np.float32)
+    d1, d2, d3 = diag(g[1]), diag(g[2]), diag(g[3])
+    res = g[4].standard_normal((batch, n)).astype(np.float32)
+    u = g[5].standard_normal((batch, n)).astype(np.float32)
+    return HMLPInputs(n, D, x, d1, d2, d3, res, u)
+
+
 def workload_inputs(name: str, bits: int | None = None, batch: int = 1):
     """Inputs for one named workload at one bit width / batch."""
     w = WORKLOADS[name]
@@ -173,4 +210,6 @@ def workload_inputs(name: str, bits: int | None = None, batch: int = 1):
                          w["x_scale"], w.get("gather", 0))
     if w["kind"] == "i8":
         return i8_inputs(w["seed"], w["R"], w["C"], w["e_lo"], w["e_hi"], batch)
+    if w["kind"] == "hmlp":
+        return hmlp_inputs(w["seed"], w["n"], w["D"], batch)
     return f8_inputs(w["seed"], w["R"], w["C"], w["SR"], w["SC"], w["e_lo"], w["e_hi"], batch)

@@ -428,3 +428,116 @@ def test_i8_hand_cases():
     assert y[0, 0] == -1024.0
     y, _ = oracle.i8_matvec(w, np.array([[127, 255]], np.uint8), np.ones((1, 17), np.float32))
     assert np.isnan(y[0, 0])
+
+
+# ---------------------------------------------------------------------------
+# Hadamard MLP block (needle.js "Inference engine, part 2", section 8)
+# ---------------------------------------------------------------------------
+
+def test_silu_matches_scipy_expit():
+    from scipy.special import expit
+    v = np.concatenate([np.linspace(-50, 50, 2001), [-745.0, -200.0, 0.0, 1e-300, 200.0, 700.0]])
+    got = oracle.silu_f64(v)
+    want = v * expit(v)
+    assert np.allclose(got, want, rtol=4e-16, atol=0)
+
+
+@pytest.mark.parametrize("D,n", [(1, 1), (2, 1), (16, 16), (64, 50), (512, 512), (1024, 700)])
+def test_hadamard_mlp_f64_matches_dense_hadamard(D, n):
+    """Dense-matrix restatement: two Sylvester-matrix products instead of the
+    butterfly, scipy's logistic function instead of exp."""
+    from scipy.special import expit
+    rng = np.random.default_rng(D * 31 + n)
+    x = rng.standard_normal((3, n)).astype(np.float32)
+    d1, d2, d3 = (rng.uniform(-1.5, 1.5, D).astype(np.float32) for _ in range(3))
+    res = rng.standard_normal((3, n)).astype(np.float32)
+    u = rng.standard_normal((3, n)).astype(np.float32)
+    got, mag = oracle.hadamard_mlp(x, D, d1, d2, d3, res, u, mode="f64")
+    Hn = hadamard(D) / math.sqrt(D)
+    z = np.zeros((3, D))
+    z[:, :n] = x
+    z = (z * d1) @ Hn.T
+    z = d2 * z
+    z = z * expit(z)
+    z = (z @ Hn.T) * d3
+    want = (res + z[:, :n]) - u
+    assert np.all(np.abs(got - want) <= 1e-12 * mag + 1e-300)
+
+
+def test_hadamard_mlp_tanh_closed_form():
+    """D = 4, x = [1, 1], d1 = 1, d2 = [2, 1, -2, 1]: the first transform gives
+    [1, 0, 1, 0] exactly, silu gives [s(2), 0, s(-2), 0], and since
+    s(a) + s(-a) = a tanh(a/2) and s(a) - s(-a) = a the second gives
+    [tanh 1, tanh 1, 1, 1]."""
+    x = np.array([[1.0, 1.0]], dtype=np.float32)
+    d1 = np.ones(4, dtype=np.float32)
+    d2 = np.array([2, 1, -2, 1], dtype=np.float32)
+    d3 = np.array([1, -3, 5, 7], dtype=np.float32)
+    got64, _ = oracle.hadamard_mlp(x, 4, d1, d2, d3, mode="f64")
+    assert np.allclose(got64[0], [math.tanh(1.0), -3 * math.tanh(1.0)], rtol=1e-15, atol=0)
+    got32, _ = oracle.hadamard_mlp(x, 4, d1, d2, d3, mode="f32")
+    assert np.allclose(got32[0], [math.tanh(1.0), -3 * math.tanh(1.0)], rtol=3e-7, atol=0)
+
+
+@pytest.mark.parametrize("k", [0, 5, 13])
+def test_hadamard_mlp_identity_silu_closed_form(k):
+    """x = 2 e_k, D = 16, d1 = 1: the first normalised transform is
+    H[:, k] / 2 exactly.  With d2 = 128 H[:, k] every silu input is +64, where
+    e^-64 is below half an ulp of 1 in float64, so silu is the identity and
+    the second transform collapses the constant 64 onto output 0: 256 d3[0],
+    zero elsewhere, exactly."""
+    D = 16
+    H = hadamard(D)
+    x = np.zeros((1, D), dtype=np.float32)
+    x[0, k] = 2.0
+    d1 = np.ones(D, dtype=np.float32)
+    d2 = (128.0 * H[:, k]).astype(np.float32)
+    d3 = np.linspace(-2, 3, D).astype(np.float32)
+    res = np.full((1, D), 0.5, dtype=np.float32)
+    u = np.full((1, D), 0.25, dtype=np.float32)
+    got, _ = oracle.hadamard_mlp(x, D, d1, d2, d3, res, u, mode="f32")
+    want = np.full(D, 0.25, dtype=np.float32)
+    want[0] = np.float32(np.float32(0.5) + np.float32(256.0) * d3[0]) - np.float32(0.25)
+    assert np.array_equal(got[0], want)
+
+
+def test_hadamard_mlp_zero_gate_leaves_residual_minus_u():
+    """d2 = 0: silu(0) = 0, the rest of the block is zero and the update is
+    residual - u, one float32 subtraction."""
+    rng = np.random.default_rng(5)
+    D, n = 64, 40
+    x = rng.standard_normal((2, n)).astype(np.float32)
+    d1, d3 = (rng.standard_normal(D).astype(np.float32) for _ in range(2))
+    res = rng.standard_normal((2, n)).astype(np.float32)
+    u = rng.standard_normal((2, n)).astype(np.float32)
+    got, _ = oracle.hadamard_mlp(x, D, d1, np.zeros(D, np.float32), d3, res, u)
+    assert np.array_equal(got, res - u)
+    bare, _ = oracle.hadamard_mlp(x, D, d1, np.zeros(D, np.float32), d3)
+    assert np.array_equal(bare, np.zeros_like(bare))
+
+
+def test_hadamard_mlp_pads_before_the_first_diagonal():
+    """The page pads, then multiplies by d1: an infinite d1 entry in the
+    padding meets a zero and makes NaN, which the transform spreads to every
+    output."""
+    D, n = 32, 20
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((1, n)).astype(np.float32)
+    d1, d2, d3 = (rng.standard_normal(D).astype(np.float32) for _ in range(3))
+    finite, _ = oracle.hadamard_mlp(x, D, d1, d2, d3)
+    assert np.all(np.isfinite(finite))
+    d1[25] = np.inf
+    got, _ = oracle.hadamard_mlp(x, D, d1, d2, d3)
+    assert np.all(np.isnan(got))
+
+
+@pytest.mark.parametrize("D,n", [(256, 256), (2048, 512)])
+def test_hadamard_mlp_f32_staging_within_f64_bound(D, n):
+    rng = np.random.default_rng(D + n)
+    x = rng.standard_normal((2, n)).astype(np.float32)
+    d1, d2, d3 = (rng.uniform(-1.5, 1.5, D).astype(np.float32) for _ in range(3))
+    res = rng.standard_normal((2, n)).astype(np.float32)
+    u = rng.standard_normal((2, n)).astype(np.float32)
+    g32, mag = oracle.hadamard_mlp(x, D, d1, d2, d3, res, u)
+    g64, _ = oracle.hadamard_mlp(x, D, d1, d2, d3, res, u, mode="f64")
+    assert np.all(np.abs(g32 - g64) <= 2e-6 * mag)
