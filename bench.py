@@ -197,7 +197,7 @@ def measured_hbm_gbs():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("f8_kernels.cu", "qmv_internal.h"):
+    for name in ("f8_kernels.cu",):
         with open(os.path.join(ROOT, "quantized_weight_matvec_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -618,6 +618,18 @@ def run_configs(args):
                              cq_gather_bytes(len(c.rows), c.input, c.input_padded, c.group,
                                              c.bits), med, best, k)
                     del packed, norms, mats
+            elif wl["kind"] == "hmlp":
+                f = synth.workload_inputs(name, batch=batch)
+                # x, residual, u in and out: 4 [batch, n] float32; three diagonals
+                nb = 4 * (4 * batch * f.n + 3 * f.D)
+                hx, hr, hu = (torch.from_numpy(a).to(dev) for a in (f.x, f.residual, f.u))
+                hd = [torch.from_numpy(a).to(dev) for a in (f.d1, f.d2, f.d3)]
+                ho = torch.empty((batch, f.n), device=dev)
+                hcalls = [lambda sh: qmv.hadamard_mlp(
+                    hx.data_ptr(), f.n, f.D, hd[0].data_ptr(), hd[1].data_ptr(), hd[2].data_ptr(),
+                    hr.data_ptr(), hu.data_ptr(), batch, ho.data_ptr(), sh)] * 64
+                med, best = _graph_time(torch, hcalls)
+                emit("%s/D%d" % (name, f.D), batch, "hadamard_mlp", nb, med, best, 1)
             elif wl["kind"] == "i8":
                 f = synth.workload_inputs(name, batch=batch)
                 nb = f.R * f.C + f.R * ((f.C + 15) // 16) + 4 * batch * (f.C + f.R)

@@ -71,6 +71,9 @@ typedef enum {
 #define QMV_MAX_GROUP 32768
 /* Largest activation batch per call. */
 #define QMV_MAX_BATCH 8
+/* Largest Hadamard dimension of hadamard_mlp (the vector is transformed
+ * in one block's shared memory as float32). */
+#define QMV_MAX_HADAMARD 32768
 
 /*
  * A CQ matrix, the page's CqMatrix record ("part 1", section 4): fields
@@ -227,6 +230,45 @@ QMV_API qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8
  */
 QMV_API qmv_status i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                              const float *x, int32_t batch, float *y, qmv_stream stream);
+
+/*
+ * hadamard_mlp -- the Hadamard MLP block of "part 2", section 8, from the
+ * normalised block input on.  For each of `batch` vectors:
+ *
+ *   z = x zero-padded to D values
+ *   z[i] = z[i] * d1[i]                      (float32 product)
+ *   z = normalizedFwht(z)                    (section-1 butterfly over all D
+ *                                             values, strides 1, 2, 4, ...,
+ *                                             each result float32, then the
+ *                                             float64 product with
+ *                                             1/sqrt(D) rounded to float32)
+ *   z[i] = silu(d2[i] * z[i])                (silu(v) = v / (1 + e^-v))
+ *   z = normalizedFwht(z)
+ *   o[i] = z[i] * d3[i]                      for i < n (float32 product)
+ *   o[i] = residual[i] + o[i]                if residual is non-NULL
+ *   o[i] = o[i] - u[i]                       if u is non-NULL
+ *
+ * The page's block takes its input from zcrms(afterAttention, weight) and
+ * adds afterAttention back before subtracting the lane-mix input u; the
+ * pages do not define zcrms, so the caller passes its output as x and
+ * afterAttention as residual.  Every step is computed as defined above
+ * except silu, which is evaluated in float32 (the page evaluates it in
+ * float64): o is within 1e-5 * A of the float64-silu result, A =
+ * |d3[i]| / sqrt(D) * sum_j |silu_j| + |residual[i]| + |u[i]|.
+ *
+ *   x         [batch, n] float32, 1 <= n <= D
+ *   D         Hadamard dimension, a power of two, 1 <= D <= QMV_MAX_HADAMARD
+ *   d1,d2,d3  [D] float32 diagonals
+ *   residual  [batch, n] float32 or NULL
+ *   u         [batch, n] float32 or NULL
+ *   out       [batch, n] float32, written; must not overlap any input
+ * Errors: QMV_ERR_BATCH, QMV_ERR_SHAPE (D not a power of two in range, n
+ * outside [1, D]), QMV_ERR_NULL, QMV_ERR_ALIGN (a pointer not 4-byte
+ * aligned), QMV_ERR_ALIAS, QMV_ERR_CUDA.
+ */
+QMV_API qmv_status hadamard_mlp(const float *x, int64_t n, int64_t D, const float *d1,
+                                const float *d2, const float *d3, const float *residual,
+                                const float *u, int32_t batch, float *out, qmv_stream stream);
 
 /* Bytes of device workspace f8_matvec_argmax needs for `batch` vectors: one
  * (value, row) partial result per block and vector, for at most

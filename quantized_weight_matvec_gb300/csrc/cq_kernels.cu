@@ -18,6 +18,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "fwht_device.cuh"
 #include "qmv_internal.h"
 
 namespace qmv {
@@ -39,40 +40,6 @@ __device__ __forceinline__ int cq_index(const uint8_t *row, int64_t k, int bits)
     unsigned v = __ldg(row + byte);
     if (sh + bits > 8) v |= unsigned(__ldg(row + byte + 1)) << 8;
     return int((v >> sh) & ((1u << bits) - 1u));
-}
-
-// RN32(RN64(v * s)): the page multiplies a float32 element by the float64
-// 1/sqrt(group) and stores the product into float32.
-__device__ __forceinline__ float scale_f64(float v, double s) {
-    return __double2float_rn(__dmul_rn(double(v), s));
-}
-
-// Unnormalised FWHT of one group spread over a warp.  For G >= 32 each lane
-// holds E = G/32 consecutive elements (element i = lane*E + e); for G < 32
-// (E == 1) the warp holds 32/G groups, element i = lane % G.  Stride h is
-// in-register while h < E, else a shuffle with lane distance h/E; the lane
-// owning the lower index keeps a+b, the upper one keeps a-b.
-template <int E>
-__device__ __forceinline__ void fwht_warp(float (&v)[E], int G, int lane) {
-#pragma unroll
-    for (int h = 1; h < E; h <<= 1) {
-#pragma unroll
-        for (int e = 0; e < E; e++) {
-            if ((e & h) == 0) {
-                float a = v[e], b = v[e + h];
-                v[e] = __fadd_rn(a, b);
-                v[e + h] = __fsub_rn(a, b);
-            }
-        }
-    }
-    for (int d = 1; d * E < G; d <<= 1) {
-        bool upper = (lane & d) != 0;
-#pragma unroll
-        for (int e = 0; e < E; e++) {
-            float o = __shfl_xor_sync(kFull, v[e], d);
-            v[e] = upper ? __fsub_rn(o, v[e]) : __fadd_rn(v[e], o);
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------

@@ -10,6 +10,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <cmath>
+
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -359,6 +361,26 @@ qmv_status i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale
         return QMV_ERR_ALIAS;
     if (R == 0) return QMV_OK;
     return qmv::launch_i8_matvec(w, R, C, scale, x, batch, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status hadamard_mlp(const float *x, int64_t n, int64_t D, const float *d1, const float *d2,
+                        const float *d3, const float *residual, const float *u, int32_t batch,
+                        float *out, qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (D < 1 || D > QMV_MAX_HADAMARD || (D & (D - 1)) != 0 || n < 1 || n > D) return QMV_ERR_SHAPE;
+    if (!x || !d1 || !d2 || !d3 || !out) return QMV_ERR_NULL;
+    const float *in[] = {x, d1, d2, d3, residual, u};
+    for (const float *p : in)
+        if (p && !aligned(p, 4)) return QMV_ERR_ALIGN;
+    if (!aligned(out, 4)) return QMV_ERR_ALIGN;
+    const int64_t vb = int64_t(batch) * n * 4, db = D * 4;
+    if (overlaps(out, vb, x, vb) || overlaps(out, vb, d1, db) || overlaps(out, vb, d2, db) ||
+        overlaps(out, vb, d3, db) || (residual && overlaps(out, vb, residual, vb)) ||
+        (u && overlaps(out, vb, u, vb)))
+        return QMV_ERR_ALIAS;
+    return qmv::launch_hadamard_mlp(x, n, int(D), d1, d2, d3, residual, u, batch, out,
+                                    1.0 / std::sqrt(double(D)), reinterpret_cast<cudaStream_t>(stream));
 }
 
 qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,

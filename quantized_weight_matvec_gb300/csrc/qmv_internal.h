@@ -80,6 +80,11 @@ bool cq_fused_fits(const qmv_cq_matrix &m, int batch);
 qmv_status launch_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                             const float *x, int batch, float *y, cudaStream_t s);
 
+// ---- Hadamard MLP ----------------------------------------------------------
+qmv_status launch_hadamard_mlp(const float *x, int64_t n, int D, const float *d1, const float *d2,
+                               const float *d3, const float *residual, const float *u, int batch,
+                               float *out, double s, cudaStream_t stream);
+
 // ---- F8 ------------------------------------------------------------------
 qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                             int64_t SR, int64_t SC, const float *x, int batch, float *y,

@@ -78,9 +78,10 @@ def load() -> ctypes.CDLL:
     lib.i8_matvec.argtypes = [P, I64, I64, P, P, I32, P, P]
     lib.f8_matvec_argmax.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P, I64, P]
     lib.f8_matvec_argmax_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P]
+    lib.hadamard_mlp.argtypes = [P, I64, I64, P, P, P, P, P, I32, P, P]
     for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.cq_matvec_multi,
                lib.cq_prepare_matvec, lib.f8_matvec, lib.i8_matvec, lib.f8_matvec_argmax,
-               lib.f8_matvec_argmax_noalloc):
+               lib.f8_matvec_argmax_noalloc, lib.hadamard_mlp):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
     lib.qmv_status_string.restype = ctypes.c_char_p
@@ -152,6 +153,12 @@ def i8_matvec(w: int, R: int, C: int, scale: int, x: int, batch: int, y: int,
               stream: int = 0) -> int:
     return load().i8_matvec(w or None, R, C, scale or None, x or None, batch, y or None,
                             stream or None)
+
+
+def hadamard_mlp(x: int, n: int, D: int, d1: int, d2: int, d3: int, residual: int, u: int,
+                 batch: int, out: int, stream: int = 0) -> int:
+    return load().hadamard_mlp(x or None, n, D, d1 or None, d2 or None, d3 or None,
+                               residual or None, u or None, batch, out or None, stream or None)
 
 
 def f8_matvec_argmax(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: int, batch: int,
@@ -358,4 +365,32 @@ def i8_matvec_t(w, scale, x, out=None, stream=None):
     _dev(out, torch.float32, "out")
     _check(i8_matvec(w.data_ptr(), R, C, scale.data_ptr(), x.data_ptr(), batch, out.data_ptr(),
                      _stream(stream)), "i8_matvec")
+    return out
+
+
+def hadamard_mlp_t(x, D, d1, d2, d3, residual=None, u=None, out=None, stream=None):
+    """out[B, n] = hadamard_mlp(x[B, n], D, d1, d2, d3[D], residual, u)."""
+    torch = _torch()
+    x = _dev(x, torch.float32, "x")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    batch, n = x.shape
+    d1, d2, d3 = (_dev(d, torch.float32, name) for d, name in ((d1, "d1"), (d2, "d2"), (d3, "d3")))
+    for d in (d1, d2, d3):
+        if d.numel() != D:
+            raise ValueError("diagonals must have D elements")
+    ptrs = []
+    for t, name in ((residual, "residual"), (u, "u")):
+        if t is None:
+            ptrs.append(0)
+            continue
+        t = _dev(t, torch.float32, name)
+        if t.numel() != batch * n:
+            raise ValueError(name + " must be [batch, n]")
+        ptrs.append(t.data_ptr())
+    if out is None:
+        out = torch.empty((batch, n), dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(hadamard_mlp(x.data_ptr(), n, D, d1.data_ptr(), d2.data_ptr(), d3.data_ptr(), ptrs[0],
+                        ptrs[1], batch, out.data_ptr(), _stream(stream)), "hadamard_mlp")
     return out

@@ -25,9 +25,10 @@ def declared_functions():
     return re.findall(r"QMV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
 
 
-def test_header_declares_the_four_entry_points():
+def test_header_declares_every_entry_point():
     names = declared_functions()
     for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec", "f8_matvec_argmax",
+              "cq_matvec_multi", "cq_prepare_matvec", "i8_matvec", "hadamard_mlp",
               "qmv_status_string", "qmv_abi_version"):
         assert n in names
 
@@ -165,3 +166,26 @@ def test_i8_rejections():
     assert f(W, 16, 16, S, X, 1, W + 8) == 8
     assert f(W, 16, 16, S, X, 1, S) == 8
     assert f(W, 0, 16, S, X, 1, 0) == 0
+
+
+def test_hadamard_mlp_rejections():
+    X, D1, D2, D3 = FAKE, FAKE + (1 << 30), FAKE + (1 << 31), FAKE + (3 << 30)
+    R, U, O = FAKE + (1 << 32), FAKE + (5 << 30), FAKE + (6 << 30)
+    f = qmv.hadamard_mlp
+    assert f(X, 512, 2048, D1, D2, D3, R, U, 0, O) == 5             # batch
+    assert f(X, 512, 2048, D1, D2, D3, R, U, 9, O) == 5
+    assert f(X, 512, 2000, D1, D2, D3, R, U, 1, O) == 2             # D not a power of two
+    assert f(X, 512, 0, D1, D2, D3, R, U, 1, O) == 2
+    assert f(X, 512, 65536, D1, D2, D3, R, U, 1, O) == 2            # above the limit
+    assert f(X, 0, 2048, D1, D2, D3, R, U, 1, O) == 2               # n outside [1, D]
+    assert f(X, 2049, 2048, D1, D2, D3, R, U, 1, O) == 2
+    assert f(0, 512, 2048, D1, D2, D3, R, U, 1, O) == 1             # NULL required pointers
+    assert f(X, 512, 2048, D1, 0, D3, R, U, 1, O) == 1
+    assert f(X, 512, 2048, D1, D2, D3, R, U, 1, 0) == 1
+    assert f(X + 2, 512, 2048, D1, D2, D3, R, U, 1, O) == 6         # alignment
+    assert f(X, 512, 2048, D1, D2, D3, R + 1, U, 1, O) == 6
+    assert f(X, 512, 2048, D1, D2, D3, R, U, 1, O + 2) == 6
+    assert f(X, 512, 2048, D1, D2, D3, R, U, 2, X + 1024) == 8      # out overlaps x
+    assert f(X, 512, 2048, D1, D2, D3, R, U, 1, D3 + 4096) == 8     # out overlaps d3
+    assert f(X, 512, 2048, D1, D2, D3, R, U, 1, R) == 8             # out overlaps residual
+    assert f(X, 512, 2048, D1, D2, D3, 0, U, 1, U + 4) == 8         # out overlaps u
