@@ -8,12 +8,14 @@
 //
 //   y[v][r] = sum_c w[r][c] * e8m0(scale[r][c/16]) * x[v][c]
 //
-// The fast kernel streams rows like the F8 one (grid-stride tiles of T rows,
-// lane l on the 16-byte chunks l, l+32, ...), so each lane's chunk is exactly
-// one scale group: the 16 products of a chunk are summed, then multiplied by
-// the group's scale once.  int8 -> float32 is exact: the byte is biased to
-// unsigned, permuted into the low mantissa byte of 2^23 (0x4B0000uu) and
-// 2^23 + 128 is subtracted.
+// The streaming kernels walk rows like the F8 one (grid-stride tiles of T
+// rows, lane l on the 16-byte chunks l, l+32, ...), so each lane's chunk is
+// exactly one scale group: the chunk's 16 products are summed, then
+// multiplied by the group's scale once.  Up to batch 4 the sums are exact
+// int32 dot products against fixed-point limbs of x (i8_dot_kernel, below);
+// otherwise int8 is widened to float32 exactly (the byte is biased to
+// unsigned, permuted into the low mantissa byte of 2^23 and 2^23 + 128 is
+// subtracted) and multiplied in float32.
 #include <stdint.h>
 
 #include "qmv_internal.h"
@@ -270,6 +272,204 @@ __global__ void __launch_bounds__(256) i8_general_kernel(I8Args a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Integer-dot kernel (C % 16 == 0, 16-byte aligned w and x).
+//
+// Each 16-column group of x is written once per block as fixed-point
+// integers relative to the group's largest finite |x|: with m in
+// [2^(k-1), 2^k) and E = min(29 - k, 149), x_int = rint(x * 2^E) has
+// |x_int| <= 2^29, and x = (x_int + err) * 2^-E with |err| <= 1/2, i.e. an
+// absolute error of at most 2^-30 * m per element.  x_int is split into two
+// signed 16-bit limbs, x_int = hi * 2^15 + lo (lo in [-2^14, 2^14)), so that
+// dp2a (two int16 x int8 products and an add per instruction) forms the
+// group's sums sum_c w_c * hi_c and sum_c w_c * lo_c exactly in int32
+// (each at most 16 * 128 * (2^14 + 1) in magnitude).  The group result is
+// (float(sum_hi) * 2^15 + float(sum_lo)) * 2^-E * e8m0(scale), accumulated in
+// float32.  This is the integer-dot scheme of the Mnemonic page ("In the
+// browser": int8 weights against activations scaled per group and widened
+// to int16, exact int32 sums, then floats times the group scale), with
+// 31-bit instead of 8-bit activations so that the result stays within the
+// float32-accumulation tolerance.  A group holding Inf or NaN is flagged
+// (its 2^-E is stored as NaN) and evaluated in float32 from x directly.
+// ---------------------------------------------------------------------------
+
+// Shared-memory layout, per vector v and step j (32 chunks = 512 columns):
+//   limbs[v][j][part][lane]  uint4: part 0/1 = lo limbs of columns 0-7 / 8-15
+//                            of the lane's chunk, part 2/3 = hi limbs
+//   xs[v][j][lane]           float: 2^-E of the chunk's group (NaN: flagged)
+__device__ __forceinline__ unsigned pack_s16(int a, int b) {
+    return (unsigned(a) & 0xffffu) | (unsigned(b) << 16);
+}
+
+__device__ void prep_x_limbs(const I8Args &a, int B, int nj, uint4 *limbs, float *xs) {
+    const int64_t nchunk = a.C >> 4;
+    const int jobs = B * nj * 32;
+    for (int job = threadIdx.x; job < jobs; job += blockDim.x) {
+        const int v = job / (nj * 32), rem = job - v * nj * 32;
+        const int j = rem >> 5, lane = rem & 31;
+        const int64_t ch = int64_t(j) * 32 + lane;
+        uint4 *out = limbs + (int64_t(v * nj + j) * 4) * 32 + lane;
+        float sx = 0.0f;
+        unsigned lw[8] = {0, 0, 0, 0, 0, 0, 0, 0}, hw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (ch < nchunk) {
+            const float4 *xp = reinterpret_cast<const float4 *>(a.x + int64_t(v) * a.C + ch * 16);
+            float xv[16];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float4 t = __ldg(xp + q);
+                xv[4 * q] = t.x;
+                xv[4 * q + 1] = t.y;
+                xv[4 * q + 2] = t.z;
+                xv[4 * q + 3] = t.w;
+            }
+            float m = 0.0f;
+            bool finite = true;
+#pragma unroll
+            for (int c = 0; c < 16; c++) {
+                finite = finite && isfinite(xv[c]);
+                m = fmaxf(m, fabsf(xv[c]));
+            }
+            if (!finite) {
+                sx = __uint_as_float(0x7fc00000u);
+            } else {
+                int k = 0;
+                frexpf(m, &k);
+                const int E = m == 0.0f ? 0 : min(29 - k, 149);
+                sx = scalbnf(1.0f, -E);
+#pragma unroll
+                for (int c = 0; c < 16; c += 2) {
+                    int xi0 = __float2int_rn(scalbnf(xv[c], E));
+                    int xi1 = __float2int_rn(scalbnf(xv[c + 1], E));
+                    const int lo0 = ((xi0 + 0x4000) & 0x7fff) - 0x4000;
+                    const int lo1 = ((xi1 + 0x4000) & 0x7fff) - 0x4000;
+                    lw[c >> 1] = pack_s16(lo0, lo1);
+                    hw[c >> 1] = pack_s16((xi0 - lo0) >> 15, (xi1 - lo1) >> 15);
+                }
+            }
+        }
+        out[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        out[32] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        out[64] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        out[96] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        xs[int64_t(v * nj + j) * 32 + lane] = sx;
+    }
+}
+
+__device__ __forceinline__ unsigned limb_word(const uint4 &p0, const uint4 &p1, int i) {
+    const uint4 &p = i < 4 ? p0 : p1;
+    const int k = i & 3;
+    return k == 0 ? p.x : k == 1 ? p.y : k == 2 ? p.z : p.w;
+}
+
+template <int B, int T>
+__global__ void __launch_bounds__(256) i8_dot_kernel(I8Args a, int nj) {
+    extern __shared__ uint4 dsm[];
+    uint4 *limbs = dsm;
+    float *xs = reinterpret_cast<float *>(dsm + int64_t(B) * nj * 128);
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunk = a.C >> 4;
+    const int iters = int((nchunk + 31) >> 5);
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    const int64_t tile_stride = nwarps * T;
+    int64_t r0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * T;
+    int rows = int(min(int64_t(T), a.R - max(r0, int64_t(0))));
+    // first step's weights in flight while x is converted
+    uint4 d[T];
+    unsigned e[T];
+    if (r0 < a.R) load_step<T>(d, e, a, r0, rows, lane, nchunk);
+    prep_x_limbs(a, B, nj, limbs, xs);
+    __syncthreads();
+    if (r0 >= a.R) return;
+    float acc[T][B];
+#pragma unroll
+    for (int t = 0; t < T; t++)
+#pragma unroll
+        for (int v = 0; v < B; v++) acc[t][v] = 0.0f;
+    for (int j = 0;;) {
+        const int64_t ch = lane + 32 * int64_t(j);
+        if (ch < nchunk) {
+            float sw[T];
+#pragma unroll
+            for (int t = 0; t < T; t++) sw[t] = e8m0_scale(e[t]);
+#pragma unroll
+            for (int v = 0; v < B; v++) {
+                const uint4 *lp = limbs + (int64_t(v * nj + j) * 4) * 32 + lane;
+                const uint4 l0 = lp[0], l1 = lp[32], h0 = lp[64], h1 = lp[96];
+                const float sx = xs[int64_t(v * nj + j) * 32 + lane];
+                if (isnan(sx)) {
+                    // group with Inf/NaN in x: float32 products from x itself
+                    const float *xv = a.x + int64_t(v) * a.C + ch * 16;
+#pragma unroll
+                    for (int t = 0; t < T; t++) {
+                        float part = 0.0f;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            float f[4];
+                            widen4(word_of(d[t], q), f);
+#pragma unroll
+                            for (int k = 0; k < 4; k++) part = fmaf(f[k], __ldg(xv + 4 * q + k), part);
+                        }
+                        acc[t][v] = fmaf(part, sw[t], acc[t][v]);
+                    }
+                    continue;
+                }
+#pragma unroll
+                for (int t = 0; t < T; t++) {
+                    int sl = 0, sh = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int wq = int(word_of(d[t], q));
+                        sl = __dp2a_lo(int(limb_word(l0, l1, 2 * q)), wq, sl);
+                        sl = __dp2a_hi(int(limb_word(l0, l1, 2 * q + 1)), wq, sl);
+                        sh = __dp2a_lo(int(limb_word(h0, h1, 2 * q)), wq, sh);
+                        sh = __dp2a_hi(int(limb_word(h0, h1, 2 * q + 1)), wq, sh);
+                    }
+                    const float g = fmaf(__int2float_rn(sh), 32768.0f, __int2float_rn(sl));
+                    acc[t][v] = fmaf(g * sx, sw[t], acc[t][v]);
+                }
+            }
+        }
+        if (++j == iters) {
+#pragma unroll
+            for (int t = 0; t < T; t++) {
+#pragma unroll
+                for (int v = 0; v < B; v++) {
+                    const float val = warp_sum(acc[t][v]);
+                    acc[t][v] = 0.0f;
+                    if (t < rows && lane == 0) a.y[int64_t(v) * a.R + r0 + t] = val;
+                }
+            }
+            r0 += tile_stride;
+            if (r0 >= a.R) break;
+            rows = int(min(int64_t(T), a.R - r0));
+            j = 0;
+        }
+        load_step<T>(d, e, a, r0, rows, lane + 32 * int64_t(j), nchunk);
+    }
+}
+
+// Shared memory of i8_dot_kernel for B vectors of C columns.
+inline size_t dot_smem(int B, int64_t C) {
+    const int64_t nj = ((C >> 4) + 31) >> 5;
+    return size_t(B) * size_t(nj) * (128 * 16 + 32 * 4);
+}
+
+template <int B, int T>
+qmv_status launch_i8_dot(const I8Args &a, cudaStream_t s) {
+    const int nj = int(((a.C >> 4) + 31) >> 5);
+    const size_t smem = dot_smem(B, a.C);
+    const void *kp = reinterpret_cast<const void *>(i8_dot_kernel<B, T>);
+    if (smem > 48 * 1024 && !allow_smem(kp, smem)) return QMV_ERR_CUDA;
+    const int blocks = grid_blocks(kp, 256, smem, (a.R + T - 1) / T);
+    return from_cuda(launch_pdl(i8_dot_kernel<B, T>, dim3(unsigned(blocks)), dim3(256), smem, s, a, nj));
+}
+
+// Largest shared memory the integer-dot kernel may take (x limbs of all
+// vectors); wider rows run on the float kernel.
+constexpr size_t kDotSmemMax = 160 * 1024;
+
 template <int B>
 qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
     const bool fast = (a.C % 16 == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) &&
@@ -279,8 +479,8 @@ qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
         const int blocks = grid_blocks(kp, 256, 0, a.R);
         return from_cuda(launch_pdl(i8_general_kernel<B>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
     }
-    // Four rows per tile at every batch: eight (the F8 kernel's choice at
-    // batch 1) ran 25% slower here.
+    // Too few tiles to keep a streaming grid busy: the small-matrix kernel
+    // (at 4096 rows it also beats converting x in every block).
     constexpr int T = 4;
     const void *kp = reinterpret_cast<const void *>(i8_fast_kernel<B, T>);
     const int64_t capacity = int64_t(occupancy(kp, 256, 0)) * sm_count() * 8;
@@ -290,6 +490,11 @@ qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
         const int blocks = grid_blocks(rp, 256, 0, (a.R + TS - 1) / TS);
         return from_cuda(launch_pdl(i8_rows_kernel<B, TS, NSTEP>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
     }
+    // Integer dot products up to batch 4: one dp2a per weight and vector is
+    // cheaper than widening every weight to float, until the dp2a rate
+    // (half the FMA rate) runs out at larger batches.  Tile heights from a
+    // sweep on the 245760 x 4096 head: 6 rows at batch 1-2, 4 at 3-4.
+    if (B <= 4 && dot_smem(B, a.C) <= kDotSmemMax) return launch_i8_dot<B, (B <= 2) ? 6 : 4>(a, s);
     const int blocks = grid_blocks(kp, 256, 0, (a.R + T - 1) / T);
     return from_cuda(launch_pdl(i8_fast_kernel<B, T>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
 }

@@ -1,5 +1,10 @@
 """GPU parity of i8_matvec (ds4f-disk issue #6, step 4: int8 weights with
-per-16 E8M0 group scales) against the float64 oracle."""
+per-16 E8M0 group scales) against the float64 oracle.
+
+Matrices with many rows run on the streaming kernels: up to batch 4 the
+integer-dot kernel (x in fixed-point limbs per 16-column group, exact int32
+sums), above it the float32 kernel; small matrices run on the small-matrix
+kernel.  The tests below cover each route."""
 import numpy as np
 import pytest
 import torch
@@ -29,7 +34,8 @@ def check(f, x=None, rows=None):
     torch.cuda.synchronize()
     y = y.cpu().numpy().astype(np.float64)
     ref, mag = oracle.i8_matvec(f.w, f.scale, x, threads=8)
-    ok = (np.isnan(y) & np.isnan(ref)) | (np.abs(y - ref) <= REL * mag + ABS)
+    with np.errstate(invalid="ignore"):  # inf - inf where both sides are infinite
+        ok = (np.isnan(y) & np.isnan(ref)) | (y == ref) | (np.abs(y - ref) <= REL * mag + ABS)
     assert ok.all(), (np.argwhere(~ok)[:3], int((~ok).sum()))
     return y
 
@@ -75,3 +81,66 @@ def test_i8_deterministic():
     b = qmv.i8_matvec_t(w, s, x)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+# Enough rows for the streaming kernels (more than four waves of tiles).
+STREAM_R = 120000
+
+
+@pytest.mark.parametrize("batch", [1, 2, 3, 4, 6])
+@pytest.mark.parametrize("C", [528, 1040])
+def test_i8_streaming_ragged_steps(batch, C):
+    """C = 528 / 1040: 33 / 65 chunks, so the last 512-column step is ragged."""
+    check(synth.i8_inputs(C + batch, STREAM_R, C, 100, 130, batch=batch))
+
+
+def test_i8_streaming_nonfinite_x_groups():
+    f = synth.i8_inputs(50, STREAM_R, 256, 110, 124, batch=3)
+    f.x[0, 37] = np.inf    # group 2 of vector 0
+    f.x[1, 200] = np.nan   # group 12 of vector 1
+    f.x[2, 5] = -np.inf
+    f.x[2, 6] = np.inf     # -inf and +inf in one group of vector 2
+    y = check(f)
+    assert np.isnan(y[1]).all()
+    # vector 2: NaN where the two infinite products have opposite signs,
+    # +-inf where they agree
+    assert not np.isfinite(y[2]).any() and np.isnan(y[2]).any() and np.isinf(y[2]).any()
+    assert np.isinf(y[0]).any()
+
+
+def test_i8_streaming_wide_dynamic_range_in_groups():
+    """x spans six decades inside each 16-column group."""
+    f = synth.i8_inputs(51, STREAM_R, 512, 110, 124, batch=2)
+    rng = np.random.default_rng(51)
+    f.x *= (10.0 ** rng.uniform(-3, 3, f.x.shape)).astype(np.float32)
+    check(f)
+
+
+@pytest.mark.parametrize("mult", [1e30, 1e-30, 0.0])
+def test_i8_streaming_extreme_magnitudes(mult):
+    f = synth.i8_inputs(52, STREAM_R, 256, 120, 134, batch=2)
+    f.x = (f.x * np.float32(mult)).astype(np.float32)
+    f.x[1, 16:48] = 0.0  # two all-zero groups
+    y = qmv.i8_matvec_t(dev(f.w), dev(f.scale), dev(f.x)).cpu().numpy().astype(np.float64)
+    ref, mag = oracle.i8_matvec(f.w, f.scale, f.x, threads=8)
+    assert np.all(np.abs(y - ref) <= REL * mag), "relative bound without the absolute term"
+    if mult == 0.0:
+        assert not y.any()
+
+
+def test_i8_streaming_integer_inputs_are_exact():
+    """Small-integer x and unit scales: every partial sum is an integer below
+    2^24, so both float32 accumulation and the integer dots are exact."""
+    f = synth.i8_inputs(53, STREAM_R, 512, 127, 127, batch=2)
+    rng = np.random.default_rng(53)
+    f.x = rng.integers(-8, 9, f.x.shape).astype(np.float32)
+    y = qmv.i8_matvec_t(dev(f.w), dev(f.scale), dev(f.x)).cpu().numpy().astype(np.float64)
+    ref, _ = oracle.i8_matvec(f.w, f.scale, f.x, threads=8)
+    assert np.array_equal(y, ref)
+
+
+def test_i8_streaming_extreme_scales():
+    f = synth.i8_inputs(54, STREAM_R, 256, 0, 180, batch=2)
+    f.scale[7, 3] = 255
+    y = check(f)
+    assert np.isnan(y[:, 7]).all()
