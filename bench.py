@@ -538,6 +538,8 @@ def run_configs(args):
     for label, outs, inp, group, bits in (("set3_2048x512", (2048, 2048, 2048), 512, 64, 2),
                                           ("set3_2048x512", (2048, 2048, 2048), 512, 64, 4),
                                           ("cq2_vocab_fused", (32768,), 500, 128, 2)):
+        if args.only and args.only not in label:
+            continue
         cs = [synth.cq_inputs(60 + i, o, inp, group, bits, x_scale=3.0) for i, o in enumerate(outs)]
         c0 = cs[0]
         per = [c.output * (c.row_bytes + 2 * (c.input_padded // c.group)) for c in cs]
@@ -581,6 +583,8 @@ def run_configs(args):
         del packs, norms, sets
 
     for name, wl in synth.WORKLOADS.items():
+        if args.only and args.only not in name:
+            continue
         for batch in wl["batch"]:
             if wl["kind"] == "cq":
                 for bits in wl["bits"]:
@@ -688,6 +692,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--configs", action="store_true",
                     help="per-workload sweep (one JSON line per workload, batch and op)")
+    ap.add_argument("--only", default="",
+                    help="with --configs: only the workloads whose name contains this text")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
     if args.configs:

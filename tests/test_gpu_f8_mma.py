@@ -1,0 +1,167 @@
+"""GPU parity of the tensor-core F8 kernel (batch 2..8).
+
+f8_matvec at batch >= 2 on C % 64 == 0 with 64-column-aligned scale blocks
+runs on mma.sync (f16 operands, float32 accumulation): E4M3 weights decode
+exactly to f16, and each 64-column block of every activation vector is split
+into f16 hi + lo parts under a per-block power-of-two exponent.  The bar is the
+matvec tolerance of ds4f-disk issue #6 step 1's definition,
+|y - y_oracle| <= 1e-4 * sum_c |w * s * x| + 1e-6, against the float64 oracle.
+
+Two kernels take this path: a staged one (C <= 4096 in the common shapes:
+weights copied into a shared-memory ring with cp.async, B fragments in
+registers) and a register-streaming one for wider rows.  Cases: every batch
+2..8 on both; ragged row tiles; rows whose scale row changes inside a 16-row
+tile; 1, 2 and 4 column blocks per warp; warps with unequal numbers of
+64-column blocks (and more than one step of four); activations with a wide
+dynamic range inside a block, huge, tiny, subnormal and zero; Inf / NaN in x;
+saturated E4M3 codes and NaN scales; integer inputs, where the result is exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_weight_matvec_gb300 import qmv, synth
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-4, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qmv.load()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run(f, x=None):
+    x = f.x if x is None else x
+    y = qmv.f8_matvec_t(dev(f.w), dev(f.scale), dev(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy().astype(np.float64)
+
+
+def check(f, abs_tol=ABS):
+    y = run(f)
+    ref, mag = oracle.f8_matvec(f.w, f.scale, f.x, threads=8)
+    with np.errstate(invalid="ignore"):  # inf - inf where both sides are infinite
+        ok = (np.isnan(y) & np.isnan(ref)) | (y == ref) | (np.abs(y - ref) <= REL * mag + abs_tol)
+    if not ok.all():
+        i = tuple(np.argwhere(~ok)[0])
+        raise AssertionError("mismatch at %s: gpu %r oracle %r bound %r (%d bad)" % (
+            i, y[i], ref[i], REL * mag[i] + abs_tol, int((~ok).sum())))
+    return y
+
+
+@pytest.mark.parametrize("batch", [2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("R,C,SR,SC", [
+    (1000, 4096, 8, 32),     # ragged last tile; scale rows change inside tiles
+    (333, 1280, 7, 20),      # 20 column blocks over 16 warps: 1 or 2 per warp
+    (129, 4480, 129, 35),    # 70 blocks: register kernel, 4 or 5 per warp (1 or 2 steps)
+    (50, 256, 1, 1),         # four column blocks: 1 warp x 4 blocks, 2 x 2 or 4 x 1 by batch
+    (50, 192, 1, 3),         # three column blocks: not this kernel (the float one)
+    (17, 8192, 3, 64),       # register kernel, 8 blocks per warp: two full steps
+    (2000, 2048, 2000, 16),  # one scale row per weight row
+    (4100, 1024, 41, 4)])    # more tiles than blocks: grid-stride tiles
+def test_mma_shapes(batch, R, C, SR, SC):
+    check(synth.f8_inputs(R * 3 + C + batch, R, C, SR, SC, 112, 140, batch=batch))
+
+
+def test_mma_wide_dynamic_range_inside_blocks():
+    """x spans six decades inside every 64-column block."""
+    f = synth.f8_inputs(61, 3000, 2048, 30, 16, 118, 132, batch=8)
+    rng = np.random.default_rng(61)
+    f.x = (f.x * (10.0 ** rng.uniform(-3, 3, f.x.shape))).astype(np.float32)
+    check(f)
+
+
+@pytest.mark.parametrize("mult", [1e30, 1e-30, 1e-40, 0.0])
+def test_mma_extreme_magnitudes(mult):
+    """Huge, tiny and subnormal activations, and all-zero blocks: the relative
+    bound holds without the absolute term."""
+    f = synth.f8_inputs(62, 700, 1024, 7, 8, 120, 134, batch=4)
+    f.x = (f.x * np.float32(mult)).astype(np.float32)
+    f.x[1, 64:192] = 0.0  # two all-zero column blocks
+    y = run(f)
+    ref, mag = oracle.f8_matvec(f.w, f.scale, f.x, threads=8)
+    assert np.all(np.abs(y - ref) <= REL * mag), "relative bound without the absolute term"
+    if mult == 0.0:
+        assert not y.any()
+
+
+def test_mma_subnormal_scales_and_large_exponents():
+    f = synth.f8_inputs(63, 256, 1024, 16, 8, 0, 190, batch=3)
+    check(f)
+
+
+def test_mma_nonfinite_x():
+    f = synth.f8_inputs(64, 900, 1024, 9, 8, 118, 132, batch=5)
+    f.x[0, 37] = np.inf
+    f.x[1, 700] = np.nan
+    f.x[2, 5] = -np.inf
+    f.x[2, 6] = np.inf
+    y = check(f)
+    assert np.isnan(y[1]).all()
+    assert np.isinf(y[0]).any()
+    assert not np.isfinite(y[2]).any()
+    assert np.isfinite(y[3:]).all()
+
+
+def test_mma_saturated_codes_and_nan_scale():
+    f = synth.f8_inputs(65, 500, 4096, 10, 32, 120, 130, batch=6, finite_only=False)
+    assert (f.w == 0x7F).any() and (f.w == 0xFF).any()
+    check(f)
+    f.scale[3, 5] = 255
+    y = check(f)
+    rows_with_nan = np.nonzero((np.arange(500) * 10) // 500 == 3)[0]
+    assert np.isnan(y[:, rows_with_nan]).all()
+    assert not np.isnan(np.delete(y, rows_with_nan, axis=1)).any()
+
+
+def test_mma_integer_inputs_are_exact():
+    """Integer weights (E4M3 codes of 0, +-1, +-2, 3, 4), integer x in [-8, 8]
+    and unit scales: every partial sum is an integer below 2^24, so the result
+    equals the float64 oracle exactly."""
+    rng = np.random.default_rng(66)
+    codes = np.array([0x00, 0x38, 0x40, 0x44, 0x48, 0xB8, 0xC0], np.uint8)
+    R, C = 1500, 2048
+    f = synth.F8Inputs(R, C, 4, 16, codes[rng.integers(0, len(codes), (R, C))],
+                       np.full((4, 16), 127, np.uint8),
+                       rng.integers(-8, 9, (8, C)).astype(np.float32))
+    y = run(f)
+    ref, _ = oracle.f8_matvec(f.w, f.scale, f.x, threads=8)
+    assert np.array_equal(y, ref)
+
+
+def test_mma_deterministic_and_writes_only_its_outputs():
+    f = synth.f8_inputs(67, 2049, 4096, 16, 32, 118, 132, batch=7)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    buf = torch.full((7 * 2049 + 64,), float("nan"), device="cuda")
+    buf[7 * 2049:] = 3.5
+    out = buf[:7 * 2049].view(7, 2049)
+    qmv.f8_matvec_t(w, s, x, out=out)
+    torch.cuda.synchronize()
+    a = out.clone()
+    qmv.f8_matvec_t(w, s, x, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), out.view(torch.int32))
+    assert not torch.isnan(a).any() and bool((buf[7 * 2049:] == 3.5).all())
+
+
+def test_mma_kernel_is_the_one_launched():
+    from torch.profiler import ProfilerActivity, profile
+    f = synth.f8_inputs(68, 512, 1024, 4, 8, 118, 132, batch=8)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        qmv.f8_matvec_t(w, s, x)
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events()]
+    if not names:
+        pytest.skip("the profiler recorded no kernels on this box")
+    assert any("f8_mma" in n for n in names), names
