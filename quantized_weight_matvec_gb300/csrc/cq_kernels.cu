@@ -416,15 +416,17 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(CqSet c) {
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
     int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
 
-    // the first rows' loads go out before the table is built
+    // the loads of this warp's first two units go out before the table is
+    // built (most warps of a launch have one or two units: their weights then
+    // cost one DRAM round trip, not two)
     int mi = set_matrix(c, u, 0);
-    uint4 d;
-    float n;
-    if (u < nunits) {
-        cq2_load(d, n, c, mi, (u - c.first[mi]) * RPW + rho, q, g);
-    } else {
-        d = make_uint4(0, 0, 0, 0);
-        n = 0.0f;
+    uint4 d = make_uint4(0, 0, 0, 0), dn = make_uint4(0, 0, 0, 0);
+    float n = 0.0f, nn = 0.0f;
+    if (u < nunits) cq2_load(d, n, c, mi, (u - c.first[mi]) * RPW + rho, q, g);
+    int mn = mi;
+    if (u + nwarps < nunits) {
+        mn = set_matrix(c, u + nwarps, mi);
+        cq2_load(dn, nn, c, mn, (u + nwarps - c.first[mn]) * RPW + rho, q, g);
     }
 
     const float *pv = c.p;
@@ -472,14 +474,14 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(CqSet c) {
         const int64_t r = (u - c.first[mi]) * RPW + rho;
         const int64_t out = c.output[mi];
         float *y = c.y[mi];
-        // next rows' loads before this row's lookups
-        uint4 dn = make_uint4(0, 0, 0, 0);
-        float nn = 0.0f;
-        const int64_t un = u + nwarps;
-        int mn = mi;
-        if (un < nunits) {
-            mn = set_matrix(c, un, mi);
-            cq2_load(dn, nn, c, mn, (un - c.first[mn]) * RPW + rho, q, g);
+        // the unit after next: its loads before this unit's lookups
+        uint4 dnn = make_uint4(0, 0, 0, 0);
+        float nnn = 0.0f;
+        const int64_t unn = u + 2 * nwarps;
+        int mnn = mn;
+        if (unn < nunits) {
+            mnn = set_matrix(c, unn, mn);
+            cq2_load(dnn, nnn, c, mnn, (unn - c.first[mnn]) * RPW + rho, q, g);
         }
         // rotate the 128-bit chunk right by 4*rho bits, then split every word
         // into its even nibbles (one per byte) and its odd nibbles
@@ -513,6 +515,9 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(CqSet c) {
         d = dn;
         n = nn;
         mi = mn;
+        dn = dnn;
+        nn = nnn;
+        mn = mnn;
     }
 }
 
