@@ -17,10 +17,17 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include "mma_device.cuh"
 #include "qmv_internal.h"
 
 namespace qmv {
 namespace {
+
+using mma::cp_async_commit;
+using mma::cp_async_wait;
+using mma::kRing;
+using mma::mma_16816;
+using mma::split_block;
 
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -562,14 +569,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
     return out;
 }
 
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                          uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // tot[j][h] += sum over the step's K-blocks of row (g + 8h), vector 4j+t.
 // frag is [K-step][lane][NJ] of (b0b1, b2b3); fv is [K-block][4*NJ] of 2^-E.
 template <int NJ>
@@ -608,29 +607,6 @@ __device__ __forceinline__ void mma_compute(float (&tot)[NJ][2], const MmaStep &
     }
 }
 
-// Splits one 64-column block of one activation vector (lane l holds columns
-// 2l and 2l+1; the whole warp calls it): with m the block's largest finite
-// |x| and E = min(14 - floor(log2 m), 127) (0 when m = 0), x * 2^E = hi + lo,
-// hi = f16(x * 2^E), lo = f16(x * 2^E - hi).  Returns the packed f16 pairs
-// and f = 2^-E, or f = NaN when the block holds Inf or NaN.
-__device__ __forceinline__ void split_block(float2 xv, uint32_t &hi, uint32_t &lo, float &f) {
-    const bool fin = isfinite(xv.x) && isfinite(xv.y);
-    float m = fmaxf(isfinite(xv.x) ? fabsf(xv.x) : 0.0f, isfinite(xv.y) ? fabsf(xv.y) : 0.0f);
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
-    const bool all_finite = __all_sync(kFull, fin);
-    int E = 0;
-    if (m > 0.0f) E = min(14 - ilogbf(m), 127);  // in [-113, 127]
-    const float up = __uint_as_float(uint32_t(127 + E) << 23);
-    const float down = (E == 127) ? __uint_as_float(0x00400000u) : __uint_as_float(uint32_t(127 - E) << 23);
-    const float s0 = xv.x * up, s1 = xv.y * up;
-    const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
-    const __half l0 = __float2half_rn(s0 - __half2float(h0)), l1 = __float2half_rn(s1 - __half2float(h1));
-    hi = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
-    lo = uint32_t(__half_as_ushort(l0)) | (uint32_t(__half_as_ushort(l1)) << 16);
-    f = all_finite ? down : __uint_as_float(0x7fc00000u);
-}
-
 // x -> B fragments in shared memory: one warp per (64-column block kb,
 // vector slot v); lane l holds columns 64*kb + 2l and 2l+1.
 template <int NJ>
@@ -663,60 +639,12 @@ __host__ __device__ inline size_t mma_smem_bytes(int64_t C, int NJ, int NW) {
                   + nkb * 4);                 // scale column of each K-block
 }
 
-// Tile epilogue of the mma kernels.  Every warp stores its partial sums (rows
-// g and g+8 of vector 4j+t) to red[buf]; after the barrier, reducer thread
-// o = 16*v + rho adds the warps' partials for row r0+rho of vector v in warp
-// order, recomputes a non-finite result exactly, and stores it (and, for the
-// argmax, keeps the best row it has seen).  Every thread of the block calls it.
-template <int NJ, bool AM>
-__device__ __forceinline__ void mma_tile_epilogue(float (&tot)[NJ][2], float *red, int buf, int NW,
-                                                  const F8Args &a, int batch, int64_t r0, float &best_v,
-                                                  int64_t &best_i) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float2 *rw = reinterpret_cast<float2 *>(red) + ((buf * NW + warp) * NJ) * 32;
-#pragma unroll
-    for (int j = 0; j < NJ; j++) {
-        rw[j * 32 + lane] = make_float2(tot[j][0], tot[j][1]);
-        tot[j][0] = tot[j][1] = 0.0f;
-    }
-    __syncthreads();
-    if (warp < (16 * batch + 31) / 32) {  // warp-uniform
-        const int o = threadIdx.x, o_v = o >> 4, o_rho = o & 15;
-        const bool valid = o < 16 * batch && r0 + o_rho < a.R;
-        float sum = 0.0f;
-        if (valid) {
-            const int j = o_v >> 2, lp = (o_rho & 7) * 4 + (o_v & 3), comp = o_rho >> 3;
-            // four interleaved partial sums, combined in a fixed order
-            const float *rp = red + ((buf * NW * NJ + j) * 32 + lp) * 2 + comp;
-            const int wstride = NJ * 64;
-            float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
-            int w2 = 0;
-            for (; w2 + 4 <= NW; w2 += 4) {
-                p0 += rp[(w2 + 0) * wstride];
-                p1 += rp[(w2 + 1) * wstride];
-                p2 += rp[(w2 + 2) * wstride];
-                p3 += rp[(w2 + 3) * wstride];
-            }
-            for (; w2 < NW; w2++) p0 += rp[w2 * wstride];
-            sum = (p0 + p1) + (p2 + p3);
-        }
-        unsigned bad = __ballot_sync(kFull, valid && !isfinite(sum));
-        while (bad) {
-            const int bl = __ffs(bad) - 1;
-            bad &= bad - 1;
-            const int ob = warp * 32 + bl;
-            const float ex = f8_row_exact(a, r0 + (ob & 15), ob >> 4, nullptr);
-            if (lane == bl) sum = ex;
-        }
-        if (valid) {
-            if (AM && arg_better(sum, r0 + o_rho, best_v, best_i)) {
-                best_v = sum;
-                best_i = r0 + o_rho;
-            }
-            if (!AM || a.y) a.y[int64_t(o_v) * a.R + r0 + o_rho] = sum;
-        }
-    }
-}
+// The exact per-element evaluation of one output, as the tile epilogue's
+// fix-up of non-finite results (warp-collective).
+struct F8Exact {
+    const F8Args &a;
+    __device__ __forceinline__ float operator()(int64_t r, int v) const { return f8_row_exact(a, r, v, nullptr); }
+};
 
 // Argmax epilogue of the mma kernels: the 16 reducer threads of vector v
 // (lanes 16*(v%2) .. +15 of one warp) reduce their bests, and the block's
@@ -802,7 +730,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_kernel(F8Args a, int batch) {
             mma_compute<NJ>(tot, cur, frag, fv, kb_lo + kMmaKS * step, kb_hi, lane);
 
             if (step == nsteps - 1) {
-                mma_tile_epilogue<NJ, AM>(tot, red, buf, NW, a, batch, tile * 16, best_v, best_i);
+                mma::tile_epilogue<NJ, AM>(tot, red, buf, NW, batch, a.R, a.y, tile * 16, best_v, best_i, F8Exact{a}, arg_better);
                 buf ^= 1;
             }
             if (!has_next) break;
@@ -836,87 +764,6 @@ __global__ void __launch_bounds__(512, 1) f8_mma_kernel(F8Args a, int batch) {
 // copies are coalesced whole lines and the reads follow the fragment order,
 // so a __syncwarp after cp.async.wait_group publishes the lanes' copies.
 // ---------------------------------------------------------------------------
-
-constexpr int kRing = 3;  // tiles per warp in the cp.async ring
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Copies this warp's part of tile `tl` -- 16 rows x NK 64-column blocks from
-// column 64*kb_lo, rows past R clamped to R-1 -- into the stage at shared
-// address `dst`.  The copies are coalesced (lane l of copy m takes 16-byte
-// chunk e = 32m + l, row e / (4 NK), so each instruction reads whole 128-byte
-// lines); chunk c of row rho is stored at position c ^ (rho & 7) (mod 4 NK)
-// of the row, which makes the fragment-order reads conflict free.
-template <int NK>
-__device__ __forceinline__ void staged_issue(uint32_t dst, const F8Args &a, int64_t tl, int kb_lo, int lane) {
-    constexpr int NCH = 4 * NK;                       // 16-byte chunks per row
-    constexpr int LOG = NK == 1 ? 2 : NK == 2 ? 3 : 4;
-    const int64_t r0 = tl * 16;
-    const uint8_t *base = a.w + r0 * a.C + int64_t(kb_lo) * 64;
-    const bool full = r0 + 16 <= a.R;  // block-uniform: only the last tile is ragged
-    const int C32 = int(a.C);          // C <= 4096 here, so rho * C fits in 32 bits
-#pragma unroll
-    for (int m = 0; m < NCH / 2; m++) {
-        const int e = 32 * m + lane, rho = e >> LOG, c = e & (NCH - 1);
-        const int rr = full ? rho : int(min(int64_t(rho), a.R - 1 - r0));
-        const int pos = c ^ (rho & (NCH - 1) & 7);
-        cp_async16(dst + uint32_t((rho * NCH + pos) * 16), base + (rr * C32 + 16 * c));
-    }
-}
-
-// This warp's B fragments (K-block k of its range, mma i, vector group j,
-// half) and 2^-E factors of vector 4j+t, built from x with split_block.
-template <int NJ>
-struct StagedB {
-    uint32_t b[4][4][NJ][2];
-    float f[4][NJ];
-};
-
-template <int NJ>
-__device__ __forceinline__ void staged_build_b(StagedB<NJ> &B, const F8Args &a, int batch, int kb_lo, int nk,
-                                               int lane) {
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const bool live = k < nk;  // warp-uniform
-        float2 xv[4 * NJ];
-#pragma unroll
-        for (int v = 0; v < 4 * NJ; v++) {
-            xv[v] = make_float2(0.0f, 0.0f);
-            if (live && v < batch)
-                xv[v] = __ldg(reinterpret_cast<const float2 *>(a.x + int64_t(v) * a.C + int64_t(kb_lo + k) * 64) +
-                              lane);
-        }
-#pragma unroll
-        for (int v = 0; v < 4 * NJ; v++) {
-            uint32_t hi, lo;
-            float f;
-            split_block(xv[v], hi, lo, f);
-            // lane (g', t') of mma i takes columns 16t' + 4i + {0,1} (from lane
-            // 8t' + 2i) and + {2,3} (from lane 8t' + 2i + 1): hi for even g', lo
-            // for odd g', of vector 4j + g'/2
-            const bool mine = (g >> 1) == (v & 3);
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const int src = 8 * t + 2 * i;
-                const uint32_t h01 = __shfl_sync(kFull, hi, src), h23 = __shfl_sync(kFull, hi, src + 1);
-                const uint32_t l01 = __shfl_sync(kFull, lo, src), l23 = __shfl_sync(kFull, lo, src + 1);
-                if (mine) {
-                    B.b[k][i][v >> 2][0] = (g & 1) ? l01 : h01;
-                    B.b[k][i][v >> 2][1] = (g & 1) ? l23 : h23;
-                }
-            }
-            if (t == (v & 3)) B.f[k][v >> 2] = f;
-        }
-    }
-}
 
 // Scale-row offset (row * SR / R) * SC of row r; `div32` when R * SR < 2^32.
 __device__ __forceinline__ int64_t scale_row_offset(const F8Args &a, int64_t r, bool div32) {
@@ -966,13 +813,13 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
 #pragma unroll
         for (int st = 0; st < kRing - 1; st++) {
             const int64_t tl = blockIdx.x + st * gstride;
-            if (tl < ntiles) staged_issue<NK>(ring + uint32_t(st * SLOT), a, tl, kb_lo, lane);
+            if (tl < ntiles) mma::issue_tile<NK>(ring + uint32_t(st * SLOT), a.w, a.R, a.C, tl, kb_lo, lane);
             cp_async_commit();
         }
         unsigned sa[NK], sb[NK];
         load_scales(blockIdx.x, sa, sb);
-        StagedB<NJ> B;
-        staged_build_b<NJ>(B, a, batch, kb_lo, NK, lane);
+        mma::StagedB<NJ> B;
+        mma::build_b<NJ>(B, a.x, a.C, batch, kb_lo, NK, lane);
 
         float tot[NJ][2];
 #pragma unroll
@@ -985,7 +832,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
                 const int64_t tn = tl + (kRing - 1) * gstride;
                 int sn = slot + kRing - 1;
                 if (sn >= kRing) sn -= kRing;
-                if (tn < ntiles) staged_issue<NK>(ring + uint32_t(sn * SLOT), a, tn, kb_lo, lane);
+                if (tn < ntiles) mma::issue_tile<NK>(ring + uint32_t(sn * SLOT), a.w, a.R, a.C, tn, kb_lo, lane);
                 cp_async_commit();
             }
             // next tile's scale codes, one tile ahead
@@ -1001,9 +848,8 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
             const uint4 *src = ring_g + slot * (SLOT / 16);
 #pragma unroll
             for (int k = 0; k < NK; k++) {
-                const int c = 4 * k + t;
-                const uint4 wa4 = src[g * NCH + (c ^ (g & (NCH - 1) & 7))];
-                const uint4 wb4 = src[(g + 8) * NCH + (c ^ (g & (NCH - 1) & 7))];
+                const uint4 wa4 = mma::row_chunk<NK>(src, g, 4 * k + t);
+                const uint4 wb4 = mma::row_chunk<NK>(src, g + 8, 4 * k + t);
                 // NJ == 1: two accumulator chains (even / odd mma) for latency
                 constexpr int NA = NJ == 1 ? 2 : 1;
                 float acc[NA][NJ][4];
@@ -1033,7 +879,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
                     tot[j][1] = fmaf(hb * f, s_b, tot[j][1]);
                 }
             }
-            mma_tile_epilogue<NJ, AM>(tot, red, buf, NW, a, batch, tl * 16, best_v, best_i);
+            mma::tile_epilogue<NJ, AM>(tot, red, buf, NW, batch, a.R, a.y, tl * 16, best_v, best_i, F8Exact{a}, arg_better);
             buf ^= 1;
             if (++slot == kRing) slot = 0;
 #pragma unroll
@@ -1107,26 +953,10 @@ bool mma_fits(const F8Args &a, int batch) {
     return chunks_uniform(a.C, a.SC, 64);
 }
 
-// The staged kernel gives every warp NK = 4, 2 or 1 whole 64-column blocks:
-// the largest that divides C / 64 with at most 16 warps and at least
-// ceil(batch / 2) (the tile epilogue has 16 * batch reducer threads).
-// 0: not applicable.
-int staged_nk(int64_t C, int batch) {
-    const int64_t nkb = C / 64;
-    for (int nk = 4; nk >= 1; nk >>= 1)
-        if (nkb % nk == 0 && nkb / nk <= 16 && nkb / nk >= (batch + 1) / 2) return nk;
-    return 0;
-}
-
-// Shared memory of the staged kernel: the cp.async rings and the partial sums.
-size_t staged_smem_bytes(int NW, int NK, int NJ) {
-    return size_t(NW) * kRing * 16 * 4 * NK * 16 + size_t(2) * NW * NJ * 32 * 8 + size_t(NW) * NK * 4;
-}
-
 template <int NJ, int NK, bool AM>
 qmv_status launch_mma_staged(const F8Args &a, int batch, cudaStream_t s, int &blocks_out) {
     const int NW = int(a.C / 64 / NK);
-    const size_t smem = staged_smem_bytes(NW, NK, NJ);
+    const size_t smem = mma::staged_smem_bytes(NW, NK, NJ, size_t(NW) * NK * 4);  // + scale columns
     auto kern = f8_mma_staged_kernel<NJ, NK, AM>;
     const void *kp = reinterpret_cast<const void *>(kern);
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
@@ -1142,7 +972,7 @@ qmv_status launch_mma_staged(const F8Args &a, int batch, cudaStream_t s, int &bl
 
 template <int NJ, bool AM>
 qmv_status launch_mma(const F8Args &a, int batch, cudaStream_t s, int &blocks_out) {
-    switch (staged_nk(a.C, batch)) {
+    switch (mma::staged_nk(a.C, batch)) {
         case 4: return launch_mma_staged<NJ, 4, AM>(a, batch, s, blocks_out);
         case 2: return launch_mma_staged<NJ, 2, AM>(a, batch, s, blocks_out);
         case 1: return launch_mma_staged<NJ, 1, AM>(a, batch, s, blocks_out);

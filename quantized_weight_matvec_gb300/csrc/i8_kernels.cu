@@ -18,6 +18,7 @@
 // subtracted) and multiplied in float32.
 #include <stdint.h>
 
+#include "mma_device.cuh"
 #include "qmv_internal.h"
 
 namespace qmv {
@@ -470,6 +471,202 @@ qmv_status launch_i8_dot(const I8Args &a, cudaStream_t s) {
 // vectors); wider rows run on the float kernel.
 constexpr size_t kDotSmemMax = 160 * 1024;
 
+// ---------------------------------------------------------------------------
+// Batch 2..8: the multiply-accumulate on the tensor cores (mma.sync m16n8k16,
+// f16 operands, float32 accumulation), in the staged layout of the F8 kernel
+// (mma_device.cuh): weights copied into a three-deep shared-memory ring with
+// cp.async, B fragments (x split into f16 hi + lo per 64-column block) in
+// registers, a fixed-order tile epilogue.
+//
+// In that layout lane (g, t) holds, for rows g and g+8, the 16 bytes at
+// column 64*kb + 16*t: exactly one scale group.  So the group scale is folded
+// into the weights as they are decoded: the byte is biased to unsigned and
+// placed in the low mantissa byte of 1024 (f16 0x6400), and one f16 fma by
+// (s, s) with addend -1152 s gives w * s -- the exact product, rounded once,
+// hence exact whenever w * s is an f16: for every scale 2^-24 <= s <= 2^5
+// (codes 103..132).  The mma then mixes groups freely.  A row with any group
+// scale outside that range gets NaN weights, so the epilogue recomputes it
+// by the exact per-element path (as it does for non-finite x and the NaN
+// scale code 255).
+// ---------------------------------------------------------------------------
+
+// Exact per-element value of output (r, v) (warp-collective).
+__device__ float i8_row_exact(const I8Args &a, int64_t r, int v) {
+    const int lane = threadIdx.x & 31;
+    const int8_t *wr = a.w + r * a.C;
+    const uint8_t *sr = a.scale + r * a.SG;
+    const float *xv = a.x + int64_t(v) * a.C;
+    float acc = 0.0f;
+    for (int64_t c = lane; c < a.C; c += 32) {
+        const float ws = float(__ldg(wr + c)) * e8m0_scale(__ldg(sr + (c >> 4)));
+        acc = fmaf(ws, __ldg(xv + c), acc);
+    }
+    return warp_sum(acc);
+}
+
+struct I8Exact {
+    const I8Args &a;
+    __device__ __forceinline__ float operator()(int64_t r, int v) const { return i8_row_exact(a, r, v); }
+};
+
+__device__ __forceinline__ bool no_better(float, int64_t, float, int64_t) { return false; }
+
+// E8M0 code e -> f16x2 (s, s) and (-1152 s, -1152 s); `ok` false (and NaN
+// pairs) outside 103..132, where w * s is not always an f16.
+__device__ __forceinline__ void i8_fold(unsigned e, uint32_t &s2, uint32_t &c2, bool &ok) {
+    ok = (e - 103u) <= 29u;
+    const uint32_t sb = e >= 113u ? (e - 112u) << 10 : 1u << ((e - 103u) & 31u);
+    const uint32_t cb = 0x8000u | (((e - 102u) & 31u) << 10) | 0x080u;
+    s2 = ok ? (sb | (sb << 16)) : 0x7e007e00u;
+    c2 = ok ? (cb | (cb << 16)) : 0x7e007e00u;
+}
+
+// Four int8 weights of a word times their group scale, as two f16 pairs
+// (bytes 0-1 -> lo, bytes 2-3 -> hi).
+__device__ __forceinline__ void i8x4_fold(uint32_t w, uint32_t s2, uint32_t c2, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t m01 = __byte_perm(u, 0x64646464u, 0x4140u), m23 = __byte_perm(u, 0x64646464u, 0x4342u);
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(m01), "r"(s2), "r"(c2));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(m23), "r"(s2), "r"(c2));
+}
+
+template <int NJ, int NK>
+__global__ void __launch_bounds__(512, 1) i8_mma_staged_kernel(I8Args a, int batch) {
+    extern __shared__ __align__(16) unsigned char st_smem[];
+    using namespace mma;
+    constexpr int NCH = 4 * NK;          // 16-byte chunks per row and warp
+    constexpr int SLOT = 16 * NCH * 16;  // bytes per warp and stage
+    const int NW = blockDim.x >> 5;      // warp w owns column blocks [w NK, w NK + NK)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int kb_lo = warp * NK;
+    const uint32_t ring = uint32_t(__cvta_generic_to_shared(st_smem)) + uint32_t(warp * kRing * SLOT);
+    const uint4 *ring_g = reinterpret_cast<const uint4 *>(st_smem + size_t(warp) * kRing * SLOT);
+    float *red = reinterpret_cast<float *>(st_smem + size_t(NW) * kRing * SLOT);
+    const uint8_t *w8 = reinterpret_cast<const uint8_t *>(a.w);
+
+    pdl_wait();
+    pdl_trigger();
+
+    const int64_t ntiles = (a.R + 15) >> 4;
+    const int64_t gstride = gridDim.x;
+    float best_v = 0.0f;
+    int64_t best_i = 0;
+    // E8M0 codes of the lane's groups (4 (kb_lo + k) + t) of rows g and g+8
+    auto load_scales = [&](int64_t tl, unsigned (&sa)[NK], unsigned (&sb)[NK]) {
+        const int64_t ra = min(tl * 16 + g, a.R - 1), rb = min(tl * 16 + g + 8, a.R - 1);
+        const uint8_t *pa = a.scale + ra * a.SG + 4 * kb_lo + t, *pb = a.scale + rb * a.SG + 4 * kb_lo + t;
+#pragma unroll
+        for (int k = 0; k < NK; k++) {
+            sa[k] = __ldg(pa + 4 * k);
+            sb[k] = __ldg(pb + 4 * k);
+        }
+    };
+    if (int64_t(blockIdx.x) < ntiles) {  // block-uniform
+#pragma unroll
+        for (int st = 0; st < kRing - 1; st++) {
+            const int64_t tl = blockIdx.x + st * gstride;
+            if (tl < ntiles) issue_tile<NK>(ring + uint32_t(st * SLOT), w8, a.R, a.C, tl, kb_lo, lane);
+            cp_async_commit();
+        }
+        unsigned sa[NK], sb[NK];
+        load_scales(blockIdx.x, sa, sb);
+        StagedB<NJ> B;
+        build_b<NJ>(B, a.x, a.C, batch, kb_lo, NK, lane);
+
+        float tot[NJ][2];
+#pragma unroll
+        for (int j = 0; j < NJ; j++) tot[j][0] = tot[j][1] = 0.0f;
+        int buf = 0, slot = 0;
+        for (int64_t tl = blockIdx.x; tl < ntiles; tl += gstride) {
+            {
+                const int64_t tn = tl + (kRing - 1) * gstride;
+                int sn = slot + kRing - 1;
+                if (sn >= kRing) sn -= kRing;
+                if (tn < ntiles) issue_tile<NK>(ring + uint32_t(sn * SLOT), w8, a.R, a.C, tn, kb_lo, lane);
+                cp_async_commit();
+            }
+            unsigned san[NK], sbn[NK];
+            if (tl + gstride < ntiles) {
+                load_scales(tl + gstride, san, sbn);
+            } else {
+#pragma unroll
+                for (int k = 0; k < NK; k++) san[k] = sbn[k] = 127u;
+            }
+            cp_async_wait<kRing - 1>();  // this lane's copies of the tile have landed
+            __syncwarp();                // ... and every other lane's
+            const uint4 *src = ring_g + slot * (SLOT / 16);
+#pragma unroll
+            for (int k = 0; k < NK; k++) {
+                const uint4 wa4 = row_chunk<NK>(src, g, 4 * k + t);
+                const uint4 wb4 = row_chunk<NK>(src, g + 8, 4 * k + t);
+                uint32_t sa2, ca2, sb2, cb2;
+                bool oka, okb;
+                i8_fold(sa[k], sa2, ca2, oka);
+                i8_fold(sb[k], sb2, cb2, okb);
+                constexpr int NA = NJ == 1 ? 2 : 1;
+                float acc[NA][NJ][4];
+#pragma unroll
+                for (int q = 0; q < NA; q++)
+#pragma unroll
+                    for (int j = 0; j < NJ; j++) acc[q][j][0] = acc[q][j][1] = acc[q][j][2] = acc[q][j][3] = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    uint32_t a0, a2, a1, a3;
+                    i8x4_fold(word_of(wa4, i), sa2, ca2, a0, a2);
+                    i8x4_fold(word_of(wb4, i), sb2, cb2, a1, a3);
+#pragma unroll
+                    for (int j = 0; j < NJ; j++)
+                        mma_16816(acc[i % NA][j], a0, a1, a2, a3, B.b[k][i][j][0], B.b[k][i][j][1]);
+                }
+#pragma unroll
+                for (int j = 0; j < NJ; j++) {
+                    const float f = B.f[k][j];
+                    float ha = acc[0][j][0] + acc[0][j][1], hb = acc[0][j][2] + acc[0][j][3];
+                    if (NA == 2) {
+                        ha += acc[NA - 1][j][0] + acc[NA - 1][j][1];
+                        hb += acc[NA - 1][j][2] + acc[NA - 1][j][3];
+                    }
+                    tot[j][0] = fmaf(ha, f, tot[j][0]);
+                    tot[j][1] = fmaf(hb, f, tot[j][1]);
+                }
+            }
+            tile_epilogue<NJ, false>(tot, red, buf, NW, batch, a.R, a.y, tl * 16, best_v, best_i, I8Exact{a},
+                                     no_better);
+            buf ^= 1;
+            if (++slot == kRing) slot = 0;
+#pragma unroll
+            for (int k = 0; k < NK; k++) {
+                sa[k] = san[k];
+                sb[k] = sbn[k];
+            }
+        }
+        cp_async_wait<0>();  // (only empty groups can remain)
+    }
+}
+
+template <int NJ, int NK>
+qmv_status launch_i8_mma(const I8Args &a, int batch, cudaStream_t s) {
+    const int NW = int(a.C / 64 / NK);
+    const size_t smem = mma::staged_smem_bytes(NW, NK, NJ, 0);
+    auto kern = i8_mma_staged_kernel<NJ, NK>;
+    const void *kp = reinterpret_cast<const void *>(kern);
+    if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
+    const int64_t ntiles = (a.R + 15) / 16;
+    int64_t blocks = int64_t(occupancy(kp, 32 * NW, smem)) * sm_count();
+    if (blocks > ntiles) blocks = ntiles;
+    return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(32 * NW), smem, s, a, batch));
+}
+
+template <int NJ>
+qmv_status launch_i8_mma_any(const I8Args &a, int batch, int nk, cudaStream_t s) {
+    switch (nk) {
+        case 4: return launch_i8_mma<NJ, 4>(a, batch, s);
+        case 2: return launch_i8_mma<NJ, 2>(a, batch, s);
+        default: return launch_i8_mma<NJ, 1>(a, batch, s);
+    }
+}
+
 template <int B>
 qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
     const bool fast = (a.C % 16 == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) &&
@@ -478,6 +675,11 @@ qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
         const void *kp = reinterpret_cast<const void *>(i8_general_kernel<B>);
         const int blocks = grid_blocks(kp, 256, 0, a.R);
         return from_cuda(launch_pdl(i8_general_kernel<B>, dim3(unsigned(blocks)), dim3(256), 0, s, a));
+    }
+    // Batch 2..8 on the tensor cores (C % 64 == 0, 256 <= C <= 4096)
+    if (B >= 2 && a.C >= 256) {
+        const int nk = mma::staged_nk(a.C, B);
+        if (nk) return launch_i8_mma_any<(B + 3) / 4>(a, B, nk, s);
     }
     // Too few tiles to keep a streaming grid busy: the small-matrix kernel
     // (at 4096 rows it also beats converting x in every block).

@@ -21,7 +21,7 @@ Workloads (the shapes named by the pages' CQ and F8 formats):
 * ``i8_4096``       I8, 4096 x 4096, per-16 E8M0 group scales with
                     exponents in [110, 124], batch 1 and 8.
 * ``i8_head``       I8 head shape (the run's "I8 head (246k vocab)"),
-                    245760 x 4096, batch 1 and 8.
+                    245760 x 4096, batch 1, 2, 4 and 8.
 * ``hmlp_512``      Hadamard MLP block on the 512-value block input with no
                     widening (D = 512), batch 1 and 4.
 * ``hmlp_2048``     the same block widened to D = 2048, batch 1, 4 and 8.
@@ -58,7 +58,7 @@ WORKLOADS = {
     "f8_head": dict(kind="f8", seed=5, R=245760, C=4096, SR=1920, SC=32, e_lo=118, e_hi=132,
                     batch=(1, 2, 4, 8)),
     "i8_4096": dict(kind="i8", seed=6, R=4096, C=4096, e_lo=110, e_hi=124, batch=(1, 8)),
-    "i8_head": dict(kind="i8", seed=7, R=245760, C=4096, e_lo=110, e_hi=124, batch=(1, 8)),
+    "i8_head": dict(kind="i8", seed=7, R=245760, C=4096, e_lo=110, e_hi=124, batch=(1, 2, 4, 8)),
     "hmlp_512": dict(kind="hmlp", seed=8, n=512, D=512, batch=(1, 4)),
     "hmlp_2048": dict(kind="hmlp", seed=9, n=512, D=2048, batch=(1, 4, 8)),
 }
