@@ -195,9 +195,13 @@ def measured_hbm_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# What the batch-1 head kernel (f8_fast_kernel) is compiled from.
+TRAFFIC_SOURCES = ("f8_kernels.cu", "f8_common.cuh", "qmv_internal.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("f8_kernels.cu",):
+    for name in TRAFFIC_SOURCES:
         with open(os.path.join(ROOT, "quantized_weight_matvec_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

@@ -1,0 +1,177 @@
+// f8_common.cuh -- definitions shared by the F8 kernel files (f8_kernels.cu:
+// batch 1 and the float kernels; f8_mma_kernels.cu: batch 2..8 on the tensor
+// cores).
+//
+// Method: ds4f-disk issue #6 "attention + tokenizer + sampling" -- work item 1
+// and step 1 (ds4f_f8_matvec: E4M3 decode with e=0 subnormal and the e=15
+// clamp at 448; E8M0 block scales, scale [SR x SC] over weight [R x C], element
+// (r, c) -> scale[r*SR/R][c*SC/C]).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "qmv_internal.h"
+
+namespace qmv {
+namespace f8 {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// One partial argmax result: the best (value, row) a block found for a vector.
+struct ArgBest {
+    float v;
+    int32_t pad;
+    int64_t i;
+};
+
+struct F8Args {
+    const uint8_t *w;
+    const uint8_t *scale;
+    const float *x;
+    float *y;  // may be NULL for the argmax variant (then not stored)
+    int64_t R, C, SR, SC;
+    ArgBest *ws;  // argmax variant: [gridDim.x, B] partial results
+};
+
+// Total order of the greedy choice: NaN above every number (as numpy and
+// torch argmax), larger values above smaller, then the lower row.
+__device__ __forceinline__ bool arg_better(float av, int64_t ai, float bv, int64_t bi) {
+    const bool an = isnan(av), bn = isnan(bv);
+    if (an != bn) return an;
+    if (!an && av != bv) return av > bv;
+    return ai < bi;
+}
+
+// Per-warp running best for each vector (every lane holds the same values).
+template <int B>
+struct WarpBest {
+    float v[B];
+    int64_t i[B];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int k = 0; k < B; k++) {
+            v[k] = -INFINITY;
+            i[k] = INT64_MAX;
+        }
+    }
+    __device__ __forceinline__ void offer(int k, float val, int64_t row) {
+        if (arg_better(val, row, v[k], i[k])) {
+            v[k] = val;
+            i[k] = row;
+        }
+    }
+};
+
+// Block-level reduction of the warps' bests, written to ws[blockIdx.x * B + k].
+// Every thread of the block must call it.
+template <int B>
+__device__ __forceinline__ void block_best_store(const WarpBest<B> &wb, ArgBest *ws) {
+    __shared__ float sv[32][B];
+    __shared__ int64_t si[32][B];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < B; k++) {
+            sv[warp][k] = wb.v[k];
+            si[warp][k] = wb.i[k];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < B) {
+        const int k = threadIdx.x;
+        float bv = sv[0][k];
+        int64_t bi = si[0][k];
+        for (int w2 = 1; w2 < nw; w2++)
+            if (arg_better(sv[w2][k], si[w2][k], bv, bi)) {
+                bv = sv[w2][k];
+                bi = si[w2][k];
+            }
+        ArgBest r;
+        r.v = bv;
+        r.pad = 0;
+        r.i = bi;
+        ws[int64_t(blockIdx.x) * B + k] = r;
+    }
+}
+
+// E4M3 byte -> float32 from its fields, with the saturation at 448 (so the
+// codes 0x7F / 0xFF, NaN in the OCP "fn" variant, read as +/-448).
+__device__ __forceinline__ float e4m3_exact(unsigned b) {
+    const unsigned e = (b >> 3) & 15u, m = b & 7u;
+    float mag;
+    if (e == 0) {
+        mag = float(m) * 0.001953125f;  // m * 2^-9, exact
+    } else {
+        mag = __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) * 2^(e-7)
+        mag = fminf(mag, 448.0f);
+    }
+    return (b & 0x80u) ? -mag : mag;
+}
+
+// E8M0 byte -> 2^(e-127) as float32; 255 -> NaN.
+__device__ __forceinline__ float e8m0_value(unsigned e) {
+    if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, subnormal
+    if (e == 255) return __uint_as_float(0x7fc00000u);
+    return __uint_as_float(e << 23);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
+    return v;  // every lane holds the same bits (a + b == b + a)
+}
+
+// Exact per-element evaluation of one output, shared by the general kernel
+// and by the fast kernel's fix-up of rows that hit a saturated code.  The
+// whole warp calls it.
+static __device__ float f8_row_exact(const F8Args &a, int64_t r, int v, const float *lut) {
+    const int64_t rb = r * a.SR / a.R;
+    const uint8_t *wr = a.w + r * a.C;
+    const uint8_t *sr = a.scale + rb * a.SC;
+    const float *xv = a.x + int64_t(v) * a.C;
+    float acc = 0.0f;
+    for (int64_t c = threadIdx.x & 31; c < a.C; c += 32) {
+        const float wv = lut ? lut[__ldg(wr + c)] : e4m3_exact(__ldg(wr + c));
+        const float sv = e8m0_value(__ldg(sr + c * a.SC / a.C));
+        acc = fmaf(wv * sv, __ldg(xv + c), acc);
+    }
+    return warp_sum(acc);
+}
+
+// Streaming 16-byte load of read-only weights, not kept in L1.  Not volatile:
+// the weights are never written while a matvec runs, so the compiler may
+// schedule these loads freely.
+__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
+    uint4 d;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
+        : "l"(p));
+    return d;
+}
+
+__device__ __forceinline__ unsigned word_of(const uint4 &d, int q) {
+    return q == 0 ? d.x : q == 1 ? d.y : q == 2 ? d.z : d.w;
+}
+
+// True when every `width`-column chunk maps to a single scale block: the
+// first column of each block b, ceil(b*C/SC), is a multiple of `width`.
+inline bool chunks_uniform(int64_t C, int64_t SC, int64_t width = 16) {
+    for (int64_t b = 1; b < SC; b++) {
+        const int64_t start = (b * C + SC - 1) / SC;
+        if (start % width != 0) return false;
+    }
+    return true;
+}
+
+
+// The tensor-core kernels (f8_mma_kernels.cu).  mma_fits: whether they take
+// this call (batch >= 2, C % 64 == 0, C >= 256, 16-byte aligned w and x,
+// 64-column-aligned scale blocks, shared memory in reach); launch_mma runs
+// them (with the argmax epilogue when `am`), setting the grid size used.
+bool mma_fits(const F8Args &a, int batch);
+qmv_status launch_mma(const F8Args &a, int batch, bool am, cudaStream_t s, int &blocks_out);
+
+}  // namespace f8
+}  // namespace qmv
