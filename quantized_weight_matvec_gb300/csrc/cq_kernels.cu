@@ -546,9 +546,154 @@ qmv_status launch_cq_general(CqSet c, cudaStream_t s) {
     return from_cuda(launch_pdl(cq_matvec_general_kernel<B, FUSED>, dim3(unsigned(blocks)), dim3(256), smem, s, c));
 }
 
-template <bool FUSED>
-qmv_status launch_set(const CqSet &c, int batch, bool all_aligned16, cudaStream_t s) {
+// ---------------------------------------------------------------------------
+// Vectorised kernel: any bits (2..5), batch 1..8, group >= 16, P % 16 == 0,
+// 2-byte aligned packed rows (row_bytes = 2 * bits * P / 16 is even).
+//
+// Lane l takes 16-column chunks ch = l, l+32, ... of a row (one warp per
+// row): the chunk's 16 codes are 2 * bits bytes, read as `bits` 16-bit words
+// into one 80-bit field, and code e is bits [bits*e, bits*e + bits) of it.  The
+// level is a warp shuffle from the lane that holds it (lane i keeps codebook
+// level i); the chunk lies inside one group, so the group's norm multiplies
+// the chunk's partial sum once.  The prepared vectors are staged in shared
+// memory with a 17-word pitch per chunk, so at every step the 32 lanes read
+// 32 distinct banks.
+// ---------------------------------------------------------------------------
+
+// Code e (compile-time) of a 16-code chunk held as lo (bits 0..63) and hi
+// (bits 64..79).
+template <int BITS, int E>
+__device__ __forceinline__ int chunk_code(uint64_t lo, uint32_t hi) {
+    constexpr int S = BITS * E;
+    constexpr unsigned M = (1u << BITS) - 1u;
+    if constexpr (S + BITS <= 64) {
+        return int(unsigned(lo >> S) & M);
+    } else if constexpr (S >= 64) {
+        return int((hi >> (S - 64)) & M);
+    } else {
+        return int((unsigned(lo >> S) | (hi << (64 - S))) & M);
+    }
+}
+
+template <int BITS, int B, bool FUSED>
+__global__ void __launch_bounds__(256) cq_vec_kernel(CqSet c) {
+    // [B][P] prepared vectors when FUSED (as the in-block prepare writes
+    // them), then [B][P/16][17] padded
+    extern __shared__ __align__(16) float vec_smem[];
+    float *spad = vec_smem + (FUSED ? int64_t(B) * c.P : 0);
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
     const int64_t P = c.P;
+    const int nch = int(P >> 4);
+    const float *psrc = c.p;
+    if (FUSED) {
+        block_prepare(c, B, vec_smem);
+        __syncthreads();
+        psrc = vec_smem;
+    }
+    for (int64_t i = threadIdx.x; i < int64_t(B) * P; i += blockDim.x) {
+        const int64_t v = i / P, k = i - v * P;
+        spad[(v * nch + (k >> 4)) * 17 + (k & 15)] = FUSED ? psrc[i] : __ldg(psrc + i);
+    }
+    const float cb_lane = lane < (1 << BITS) ? __ldg(c.codebook + lane) : 0.0f;
+    __syncthreads();
+    const int lg = __ffsll(c.G) - 1;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    const int steps = (nch + 31) >> 5;
+    int mi = 0;
+    for (int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; u < c.first[c.nmats]; u += nwarps) {
+        mi = set_matrix(c, u, mi);
+        const int64_t r = u - c.first[mi];
+        const uint16_t *row = reinterpret_cast<const uint16_t *>(c.packed[mi] + r * c.row_bytes);
+        const uint16_t *nrow = c.norms[mi] + r * c.nG;
+        float acc[B];
+#pragma unroll
+        for (int v = 0; v < B; v++) acc[v] = 0.0f;
+        for (int j = 0; j < steps; j++) {  // warp-uniform trip count: every lane shuffles
+            const int ch = lane + 32 * j;
+            const bool valid = ch < nch;
+            uint64_t lo = 0;
+            uint32_t hi = 0;
+            float n = 0.0f;
+            if (valid) {
+                const uint16_t *src = row + ch * BITS;
+#pragma unroll
+                for (int i = 0; i < BITS; i++) {
+                    const uint64_t h = __ldg(src + i);
+                    if (i < 4)
+                        lo |= h << (16 * i);
+                    else
+                        hi = uint32_t(h);
+                }
+                n = half_bits_to_float(__ldg(nrow + ((int64_t(ch) << 4) >> lg)));
+            }
+            const float *pp = spad + (valid ? ch : 0) * 17;
+            float part[B];
+#pragma unroll
+            for (int v = 0; v < B; v++) part[v] = 0.0f;
+#define QMV_CQ_VEC_STEP(E)                                                                   \
+    {                                                                                        \
+        const float lv = __shfl_sync(kFull, cb_lane, chunk_code<BITS, E>(lo, hi));           \
+        _Pragma("unroll") for (int v = 0; v < B; v++) part[v] =                               \
+            fmaf(lv, pp[v * nch * 17 + E], part[v]);                                         \
+    }
+            QMV_CQ_VEC_STEP(0) QMV_CQ_VEC_STEP(1) QMV_CQ_VEC_STEP(2) QMV_CQ_VEC_STEP(3)
+            QMV_CQ_VEC_STEP(4) QMV_CQ_VEC_STEP(5) QMV_CQ_VEC_STEP(6) QMV_CQ_VEC_STEP(7)
+            QMV_CQ_VEC_STEP(8) QMV_CQ_VEC_STEP(9) QMV_CQ_VEC_STEP(10) QMV_CQ_VEC_STEP(11)
+            QMV_CQ_VEC_STEP(12) QMV_CQ_VEC_STEP(13) QMV_CQ_VEC_STEP(14) QMV_CQ_VEC_STEP(15)
+#undef QMV_CQ_VEC_STEP
+            if (valid) {  // (a lane past the row's end shuffled with the others, adds nothing)
+#pragma unroll
+                for (int v = 0; v < B; v++) acc[v] = fmaf(part[v], n, acc[v]);
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < B; v++) {
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) acc[v] += __shfl_xor_sync(kFull, acc[v], d);
+        }
+        if (lane == 0) {
+            const int64_t out = c.output[mi];
+#pragma unroll
+            for (int v = 0; v < B; v++) c.y[mi][v * out + r] = acc[v];
+        }
+    }
+}
+
+template <int BITS, int B, bool FUSED>
+qmv_status launch_cq_vec(CqSet c, cudaStream_t s) {
+    const size_t smem = size_t(4) * B * (c.P / 16) * 17 + (FUSED ? size_t(4) * B * c.P : 0);
+    const void *kp = reinterpret_cast<const void *>(cq_vec_kernel<BITS, B, FUSED>);
+    if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
+    c.first[0] = 0;
+    for (int i = 0; i < c.nmats; i++) c.first[i + 1] = c.first[i] + c.output[i];
+    const int blocks = grid_blocks(kp, 256, smem, c.first[c.nmats]);
+    return from_cuda(launch_pdl(cq_vec_kernel<BITS, B, FUSED>, dim3(unsigned(blocks)), dim3(256), smem, s, c));
+}
+
+template <int BITS, bool FUSED>
+qmv_status launch_cq_vec_b(const CqSet &c, int batch, cudaStream_t s) {
+    switch (batch) {
+        case 1: return launch_cq_vec<BITS, 1, FUSED>(c, s);
+        case 2: return launch_cq_vec<BITS, 2, FUSED>(c, s);
+        case 3: return launch_cq_vec<BITS, 3, FUSED>(c, s);
+        case 4: return launch_cq_vec<BITS, 4, FUSED>(c, s);
+        case 5: return launch_cq_vec<BITS, 5, FUSED>(c, s);
+        case 6: return launch_cq_vec<BITS, 6, FUSED>(c, s);
+        case 7: return launch_cq_vec<BITS, 7, FUSED>(c, s);
+        default: return launch_cq_vec<BITS, 8, FUSED>(c, s);
+    }
+}
+
+template <bool FUSED>
+qmv_status launch_set(const CqSet &c, int batch, bool all_aligned16, bool all_aligned2, cudaStream_t s) {
+    const int64_t P = c.P;
+    // The kernel depends on the matrices' common shape only (never on their
+    // row counts or on FUSED), so a set call, its per-matrix calls and the
+    // fused prepare all run the same arithmetic.  (At 2048 rows the
+    // vectorised kernel would be 0.2 us faster than the table; at 32768 rows
+    // it is 2.3x slower.)
     const bool table_ok = c.bits == 2 && batch == 1 && c.G >= 64 &&
                           (P == 256 || P == 512 || P == 1024 || P == 2048) && all_aligned16;
     if (table_ok) {
@@ -557,6 +702,19 @@ qmv_status launch_set(const CqSet &c, int batch, bool all_aligned16, cudaStream_
             case 512: return launch_cq2_table<8, FUSED>(c, s);
             case 1024: return launch_cq2_table<16, FUSED>(c, s);
             default: return launch_cq2_table<32, FUSED>(c, s);
+        }
+    }
+    // vectorised kernel: group >= 16, P % 16 == 0, 2-byte aligned rows, and the
+    // prepared vectors (padded) in shared memory.  The fused variant takes
+    // exactly the same cases (it prepares wherever cq_fused_fits holds, so
+    // P * batch * 4 <= 96 KB), which keeps cq_prepare_matvec bitwise equal to
+    // cq_prepare + cq_matvec.
+    if (c.G >= 16 && P % 16 == 0 && all_aligned2 && size_t(4) * batch * (P / 16) * 17 <= 102 * 1024) {
+        switch (c.bits) {
+            case 2: return launch_cq_vec_b<2, FUSED>(c, batch, s);
+            case 3: return launch_cq_vec_b<3, FUSED>(c, batch, s);
+            case 4: return launch_cq_vec_b<4, FUSED>(c, batch, s);
+            default: return launch_cq_vec_b<5, FUSED>(c, batch, s);
         }
     }
     switch (batch) {
@@ -612,15 +770,16 @@ qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, c
     c.p = p;
     c.x = x;
     c.prepared_out = prepared_out;
-    bool aligned16 = true;
+    bool aligned16 = true, aligned2 = true;
     for (int i = 0; i < nmats; i++) {
         c.output[i] = mats[i].output;
         c.packed[i] = mats[i].packed;
         c.norms[i] = mats[i].norms;
         c.y[i] = ys[i];
         if (reinterpret_cast<uintptr_t>(mats[i].packed) % 16 != 0) aligned16 = false;
+        if (reinterpret_cast<uintptr_t>(mats[i].packed) % 2 != 0) aligned2 = false;
     }
-    return x ? launch_set<true>(c, batch, aligned16, s) : launch_set<false>(c, batch, aligned16, s);
+    return x ? launch_set<true>(c, batch, aligned16, aligned2, s) : launch_set<false>(c, batch, aligned16, aligned2, s);
 }
 
 qmv_status launch_cq_matvec(const qmv_cq_matrix &m, const float *p, int batch, float *y, cudaStream_t s) {

@@ -177,8 +177,10 @@ def test_cq_matvec_shapes(bits, out, inp, group, batch):
 
 @pytest.mark.parametrize("P", [256, 512, 1024, 2048])
 @pytest.mark.parametrize("group", [64, 128, 256])
-@pytest.mark.parametrize("out", [1, 5, 1000])
+@pytest.mark.parametrize("out", [1, 5, 1000, 5001, 9999])
 def test_cq2_table_path(P, group, out):
+    """2-bit, batch 1, group >= 64: the nibble-table kernel, from one row to
+    several rows per warp of a full grid."""
     check_cq_matvec(synth.cq_inputs(P + group + out, out, P - 3, group, 2, batch=1,
                                     input_padded=P))
 
