@@ -156,11 +156,62 @@ __device__ __forceinline__ void compute_step(typename AccOf<B>::type (&acc)[T][B
     }
 }
 
+// A warp's running argmax best kept in shared memory [warp][B] by lane 0
+// (blocks of at most 8 warps; the values offered are warp-uniform), so it
+// takes no registers from the streaming accumulators.  store_block reduces
+// the block's warps in warp order into ws[blockIdx.x * B + k]; every thread
+// of the block calls it.
+template <int B>
+struct SmemBest {
+    static __device__ __forceinline__ float (&vals())[8][B] {
+        __shared__ float v[8][B];
+        return v;
+    }
+    static __device__ __forceinline__ int64_t (&rows())[8][B] {
+        __shared__ int64_t r[8][B];
+        return r;
+    }
+    __device__ __forceinline__ void init() {
+        if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+            for (int k = 0; k < B; k++) {
+                vals()[threadIdx.x >> 5][k] = -INFINITY;
+                rows()[threadIdx.x >> 5][k] = INT64_MAX;
+            }
+        }
+    }
+    __device__ __forceinline__ void offer(int k, float val, int64_t row) {
+        const int w = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0 && arg_better(val, row, vals()[w][k], rows()[w][k])) {
+            vals()[w][k] = val;
+            rows()[w][k] = row;
+        }
+    }
+    __device__ __forceinline__ void store_block(ArgBest *ws) {
+        __syncthreads();
+        if (threadIdx.x < B) {
+            const int k = threadIdx.x, nw = blockDim.x >> 5;
+            float bv = vals()[0][k];
+            int64_t bi = rows()[0][k];
+            for (int w2 = 1; w2 < nw; w2++)
+                if (arg_better(vals()[w2][k], rows()[w2][k], bv, bi)) {
+                    bv = vals()[w2][k];
+                    bi = rows()[w2][k];
+                }
+            ArgBest r;
+            r.v = bv;
+            r.pad = 0;
+            r.i = bi;
+            ws[int64_t(blockIdx.x) * B + k] = r;
+        }
+    }
+};
+
 // Tile epilogue: reduce each row's sums across the warp (fixed order), fall
 // back to the exact per-element evaluation for rows that came out NaN, store.
-template <int B, int T, bool AM>
+template <int B, int T, bool AM, typename Best>
 __device__ __forceinline__ void finish_tile(typename AccOf<B>::type (&acc)[T][B], const F8Args &a, int64_t r0,
-                                            int rows, int lane, WarpBest<B> &best) {
+                                            int rows, int lane, Best &best) {
 #pragma unroll
     for (int t = 0; t < T; t++) {
 #pragma unroll
@@ -218,7 +269,10 @@ __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kern
     const int64_t row_end = GS ? a.R : a.R * (wid + 1) / nwarps;
     int64_t r0 = GS ? wid * T : a.R * wid / nwarps;
     const int64_t tile_stride = GS ? nwarps * T : T;
-    WarpBest<B> best;
+    // the argmax's running best of each warp lives in shared memory (lane 0
+    // keeps it; the values it is offered are warp-uniform), which leaves the
+    // registers to the streaming accumulators
+    SmemBest<B> best;
     best.init();
     if (r0 < row_end) {  // (no early return: the argmax epilogue has a barrier)
     const int iters = int((nchunk + 31) >> 5);
@@ -276,7 +330,7 @@ __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kern
         if (new_tile) setup_tile();
     }
     }
-    if (AM) block_best_store<B>(best, a.ws);
+    if (AM) best.store_block(a.ws);
 }
 
 // ---------------------------------------------------------------------------
@@ -335,39 +389,36 @@ __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
     if (AM) block_best_store<B>(best, a.ws);
 }
 
-// Final pass of the argmax: one block reduces the [nblocks, B] partials.
+// Final pass of the argmax: warp k reduces the nblocks partials of vector k
+// (lane-strided, then a shuffle tree).  The order of arg_better is total, so
+// the result is the unique greatest element whatever the order of reduction.
 __global__ void __launch_bounds__(256) argmax_reduce_kernel(const ArgBest *ws, int nblocks, int B,
                                                             int64_t *out_index, float *out_value) {
     pdl_wait();
     pdl_trigger();
-    __shared__ float sv[256];
-    __shared__ int64_t si[256];
-    for (int k = 0; k < B; k++) {
-        float bv = -INFINITY;
-        int64_t bi = INT64_MAX;
-        for (int b = threadIdx.x; b < nblocks; b += blockDim.x) {
-            const ArgBest e = ws[int64_t(b) * B + k];
-            if (arg_better(e.v, e.i, bv, bi)) {
-                bv = e.v;
-                bi = e.i;
-            }
+    const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (k >= B) return;  // whole warps
+    float bv = -INFINITY;
+    int64_t bi = INT64_MAX;
+    for (int b = lane; b < nblocks; b += 32) {
+        const ArgBest e = ws[int64_t(b) * B + k];
+        if (arg_better(e.v, e.i, bv, bi)) {
+            bv = e.v;
+            bi = e.i;
         }
-        sv[threadIdx.x] = bv;
-        si[threadIdx.x] = bi;
-        __syncthreads();
-        for (int st = blockDim.x / 2; st > 0; st >>= 1) {
-            if (threadIdx.x < st && arg_better(sv[threadIdx.x + st], si[threadIdx.x + st], sv[threadIdx.x],
-                                               si[threadIdx.x])) {
-                sv[threadIdx.x] = sv[threadIdx.x + st];
-                si[threadIdx.x] = si[threadIdx.x + st];
-            }
-            __syncthreads();
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bv, d);
+        const int64_t oi = __shfl_xor_sync(kFull, bi, d);
+        if (arg_better(ov, oi, bv, bi)) {
+            bv = ov;
+            bi = oi;
         }
-        if (threadIdx.x == 0) {
-            out_index[k] = si[0];
-            out_value[k] = sv[0];
-        }
-        __syncthreads();
+    }
+    if (lane == 0) {
+        out_index[k] = bi;
+        out_value[k] = bv;
     }
 }
 
@@ -455,7 +506,7 @@ qmv_status launch_f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const
     int blocks = 0;
     qmv_status st = f8::launch_any<true>(a, batch, s, blocks);
     if (st != QMV_OK) return st;
-    return from_cuda(launch_pdl(f8::argmax_reduce_kernel, dim3(1), dim3(256), 0, s,
+    return from_cuda(launch_pdl(f8::argmax_reduce_kernel, dim3(1), dim3(32 * batch), 0, s,
                                 static_cast<const f8::ArgBest *>(a.ws), blocks, batch, out_index, out_value));
 }
 
