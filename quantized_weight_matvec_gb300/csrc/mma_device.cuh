@@ -76,40 +76,73 @@ struct StagedB {
 };
 
 // Builds StagedB from x [batch, C] for column blocks kb_lo .. kb_lo+nk-1.
+// Lane (g, t)'s fragments of column block kb all come from its own 16-column
+// chunk 64*kb + 16*t of vector 4j + g/2 (hi part for even g, lo for odd g),
+// so each lane loads that chunk and splits it itself; the block's largest
+// |x| is a max over the 4 lanes t of the same g (two shuffles).  The same
+// split as split_block: m, E = min(14 - floor(log2 m), 127), hi, lo, 2^-E
+// (NaN when the block holds Inf or NaN).  f of vector 4j+t (the lane's
+// accumulator) comes from lane 8t, which split that vector.
 template <int NJ>
 __device__ __forceinline__ void build_b(StagedB<NJ> &B, const float *x, int64_t C, int batch, int kb_lo, int nk,
                                         int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int k = 0; k < 4; k++) {
-        const bool live = k < nk;  // warp-uniform
-        float2 xv[4 * NJ];
+        if (k >= nk) break;  // warp-uniform
 #pragma unroll
-        for (int v = 0; v < 4 * NJ; v++) {
-            xv[v] = make_float2(0.0f, 0.0f);
-            if (live && v < batch)
-                xv[v] = __ldg(reinterpret_cast<const float2 *>(x + int64_t(v) * C + int64_t(kb_lo + k) * 64) + lane);
-        }
+        for (int j = 0; j < NJ; j++) {
+            const int v = 4 * j + (g >> 1);
+            float xs[16];
+            if (v < batch) {
+                const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(v) * C + int64_t(kb_lo + k) * 64 + 16 * t);
 #pragma unroll
-        for (int v = 0; v < 4 * NJ; v++) {
-            uint32_t hi, lo;
-            float f;
-            split_block(xv[v], hi, lo, f);
-            // lane (g', t') of mma i takes columns 16t' + 4i + {0,1} (from lane
-            // 8t' + 2i) and + {2,3} (from lane 8t' + 2i + 1): hi for even g', lo
-            // for odd g', of vector 4j + g'/2
-            const bool mine = (g >> 1) == (v & 3);
+                for (int q = 0; q < 4; q++) {
+                    const float4 f4 = __ldg(src + q);
+                    xs[4 * q] = f4.x;
+                    xs[4 * q + 1] = f4.y;
+                    xs[4 * q + 2] = f4.z;
+                    xs[4 * q + 3] = f4.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; e++) xs[e] = 0.0f;
+            }
+            float m = 0.0f;
+            int fin = 1;
+#pragma unroll
+            for (int e = 0; e < 16; e++) {
+                const bool f = isfinite(xs[e]);
+                fin &= int(f);
+                m = fmaxf(m, f ? fabsf(xs[e]) : 0.0f);
+            }
+            m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+            fin &= __shfl_xor_sync(kFull, fin, 1);
+            fin &= __shfl_xor_sync(kFull, fin, 2);
+            int E = 0;
+            if (m > 0.0f) E = min(14 - ilogbf(m), 127);  // in [-113, 127]
+            const float up = __uint_as_float(uint32_t(127 + E) << 23);
+            const float down = (E == 127) ? __uint_as_float(0x00400000u) : __uint_as_float(uint32_t(127 - E) << 23);
+            const float f = fin ? down : __uint_as_float(0x7fc00000u);
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-                const int src = 8 * t + 2 * i;
-                const uint32_t h01 = __shfl_sync(kFull, hi, src), h23 = __shfl_sync(kFull, hi, src + 1);
-                const uint32_t l01 = __shfl_sync(kFull, lo, src), l23 = __shfl_sync(kFull, lo, src + 1);
-                if (mine) {
-                    B.b[k][i][v >> 2][0] = (g & 1) ? l01 : h01;
-                    B.b[k][i][v >> 2][1] = (g & 1) ? l23 : h23;
+                uint32_t half2[2];
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const float s0 = xs[4 * i + 2 * h] * up, s1 = xs[4 * i + 2 * h + 1] * up;
+                    const __half h0 = __float2half_rn(s0), h1 = __float2half_rn(s1);
+                    __half o0 = h0, o1 = h1;
+                    if (g & 1) {
+                        o0 = __float2half_rn(s0 - __half2float(h0));
+                        o1 = __float2half_rn(s1 - __half2float(h1));
+                    }
+                    half2[h] = uint32_t(__half_as_ushort(o0)) | (uint32_t(__half_as_ushort(o1)) << 16);
                 }
+                B.b[k][i][j][0] = half2[0];
+                B.b[k][i][j][1] = half2[1];
             }
-            if (t == (v & 3)) B.f[k][v >> 2] = f;
+            B.f[k][j] = __shfl_sync(kFull, f, 8 * t);
         }
     }
 }
