@@ -202,7 +202,13 @@ QMV_API qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, c
  * with integer floor division.  E4M3: e=0 subnormal m*2^-9, otherwise
  * (1+m/8)*2^(e-7), saturated at 448 (so 0x7F / 0xFF read as +/-448).  E8M0:
  * 2^(e-127); code 255 is NaN.  Accumulated in float32; accuracy within
- * 1e-4 * sum_c |w * s * x| + 1e-6 of the exact value.
+ * 1e-4 * sum_c |w * s * x| + 1e-6 of the exact value.  At batch 2..8 (C a
+ * multiple of 64, C >= 256, 64-column-aligned scale blocks) the products run
+ * on the tensor cores: every finite E4M3 value is an f16, and each 64-column
+ * block of x is split into f16 parts hi + lo under a power-of-two exponent,
+ * which carries an element to 2^-22 of itself or 2^-39 of the block's
+ * largest |x|, whichever is larger.  Non-finite results are recomputed
+ * element by element, so NaN and Inf follow the formula above.
  *
  *   w      [R, C] E4M3 bytes, R >= 0, C >= 1
  *   scale  [SR, SC] E8M0 bytes, 1 <= SR <= max(R, 1), 1 <= SC <= C
@@ -221,7 +227,13 @@ QMV_API qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8
  *
  * with groups of 16 consecutive columns of a row sharing one E8M0 scale
  * (2^(e-127); code 255 is NaN).  Accumulated in float32; accuracy within
- * 1e-4 * sum_c |w * s * x| + 1e-6 of the exact value.
+ * 1e-4 * sum_c |w * s * x| + 1e-6 of the exact value.  At batch 1 (C a
+ * multiple of 16) each group's products are exact int32 sums over x in
+ * fixed point (error at most 2^-30 of the group's largest |x| per element);
+ * at batch 2..8 (C a multiple of 64, 256 <= C <= 4096) they run on the
+ * tensor cores, with the group scale folded into the f16 weights (exact for
+ * scales 2^-24 .. 2^5; rows with other scales are computed element by
+ * element) and x split as for f8_matvec.
  *
  *   w      [R, C] int8, R >= 0, C >= 1
  *   scale  [R, ceil(C / 16)] E8M0 bytes
