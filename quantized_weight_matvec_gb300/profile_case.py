@@ -4,8 +4,9 @@
 
 Kernels: f8 (E4M3 head-shaped rows x 4096, scales [rows/128, 32]), i8
 (int8 rows x 4096, per-16 E8M0 group scales), cq2
-(2-bit rows x 512, group 128), gather (64 rows of a 32768 x 512 2-bit
-matrix), prepare.  Inputs are seeded synthetic data; the case is chosen
+(2-bit rows x 512, group 128, the table kernel), cqvec (--bits-bit rows x
+512, group 64, the vectorised kernel), gather (64 rows of a 32768 x 512
+2-bit matrix), prepare.  Inputs are seeded synthetic data; the case is chosen
 larger than L2 but a few hundred MB at most.  Prints one checksum line and
 no timings: numbers taken under a profiler are not measurements.
 """
@@ -20,7 +21,8 @@ from . import qmv, synth
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["f8", "i8", "cq2", "gather", "prepare"], required=True)
+    ap.add_argument("--kernel", choices=["f8", "i8", "cq2", "cqvec", "gather", "prepare"], required=True)
+    ap.add_argument("--bits", type=int, default=4)
     ap.add_argument("--rows", type=int, default=65536)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--iters", type=int, default=3)
@@ -42,6 +44,12 @@ def main(argv=None):
         for _ in range(args.iters):
             qmv.i8_matvec_t(w, s, x, out=y)
         out = y
+    elif args.kernel == "cqvec":
+        c = synth.cq_inputs(2, args.rows, 512, 64, args.bits, batch=args.batch)
+        m = qmv.CQMatrix.from_numpy(c, device=dev)
+        p = qmv.cq_prepare_t(m, torch.from_numpy(c.x).to(dev))
+        for _ in range(args.iters):
+            out = qmv.cq_matvec_t(m, p)
     else:
         rows = args.rows if args.kernel == "cq2" else 32768
         c = synth.cq_inputs(3, rows, 500, 128, 2, batch=args.batch, x_scale=3.0, gather=64)
