@@ -17,7 +17,8 @@ Every function cites the page section it follows:
 * ``ds4f-6`` -- ds4f-disk issue #6 "attention + tokenizer + sampling",
   work item 1 / step 1 (F8 E4M3 + E8M0 block-scaled matvec), step 4 (I8
   matvec with per-16 E8M0 group scales), work item 3 /
-  step 3 (head logits then sampling: greedy selection).
+  step 3 (head logits then sampling: greedy selection and top-k
+  temperature sampling).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 against values the pages fix, closed forms, library routines (numpy float16,
@@ -95,6 +96,8 @@ def _load():
     lib.orc_hadamard_mlp.restype = ctypes.c_int
     lib.orc_argmax_f32.argtypes = [P, I64]
     lib.orc_argmax_f32.restype = I64
+    lib.orc_topk_sample.argtypes = [P, I64, I64, ctypes.c_double, ctypes.c_double, P, P, P]
+    lib.orc_topk_sample.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -264,6 +267,28 @@ def argmax_rows(y) -> np.ndarray:
     y = _c(np.atleast_2d(y), np.float32)
     lib = _load()
     return np.array([lib.orc_argmax_f32(_ptr(row), row.size) for row in y], dtype=np.int64)
+
+
+def topk_sample(y, k: int, temperature: float, u):
+    """Top-k temperature sampling per row of y [batch, n] float32 (ds4f-6
+    work item 3 / step 3), in float64: the k best entries in the greedy
+    order, weights exp((l_i - l_0) / T), probabilities w / sum(w), and the
+    first entry whose cumulative weight exceeds u * sum(w).  ``u`` holds one
+    uniform draw per row.  Returns (index [batch, k] int64 best first,
+    prob [batch, k] float64, token [batch] int64)."""
+    y = _c(np.atleast_2d(y), np.float32)
+    batch, n = y.shape
+    u = np.broadcast_to(np.asarray(u, dtype=np.float64), (batch,))
+    index = np.zeros((batch, k), dtype=np.int64)
+    prob = np.zeros((batch, k), dtype=np.float64)
+    token = np.zeros(batch, dtype=np.int64)
+    lib = _load()
+    for v in range(batch):
+        rc = lib.orc_topk_sample(_ptr(y[v]), n, k, float(temperature), float(u[v]),
+                                 _ptr(index[v]), _ptr(prob[v]), _ptr(token[v:]))
+        if rc != 0:
+            raise ValueError("topk_sample: k must be in [1, n] and temperature >= 0")
+    return index, prob, token
 
 
 def i8_matvec(w, scale, x, rows=None, threads: int = 1, with_mag: bool = True):

@@ -425,6 +425,97 @@ ORC_API int64_t orc_argmax_f32(const float *y, int64_t n)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Top-k temperature sampling over one vector of head outputs (ds4f-6 work   */
+/* item 3: the head's logits feed top-k / temperature sampling; step 3: the  */
+/* sampler is a softmax driven by a seeded generator, so equal seeds give    */
+/* equal tokens).  The pages name the steps and give no formulas; the        */
+/* reading taken here, in their order:                                       */
+/*   1. the k best logits in the greedy order above (NaN first, then the     */
+/*      larger value, then the lower index), listed best first;              */
+/*   2. weights w_i = exp((l_i - l_0) / T), l_0 the best, so w_0 = 1;        */
+/*   3. probabilities p_i = w_i / S with S = w_0 + ... + w_{k-1};            */
+/*   4. the token is entry i for the smallest i with w_0 + ... + w_i above   */
+/*      u * S, u the caller's uniform draw (clamped into [0, 1], NaN read    */
+/*      as 0); when rounding leaves no such i, the last i with w_i > 0.      */
+/* Where the formula has no value the limit is taken: T = 0 is greedy        */
+/* (entry 0, p = 1, 0, 0, ...); a NaN l_0 gives entry 0 and NaN            */
+/* probabilities; l_0 = +inf shares the weight equally among the +inf        */
+/* entries; l_0 = -inf (every entry -inf) gives equal weights.               */
+/* Selection is k passes of the greedy scan with the chosen entries struck   */
+/* out.  Returns 0, or -1 for k outside [1, n] or T not >= 0 (incl. NaN).    */
+/* ------------------------------------------------------------------------ */
+
+ORC_API int orc_topk_sample(const float *y, int64_t n, int64_t k, double T, double u,
+                            int64_t *index, double *prob, int64_t *token)
+{
+    if (k < 1 || k > n || !(T >= 0))
+        return -1;
+    unsigned char *taken = (unsigned char *)calloc((size_t)n, 1);
+    double *w = (double *)malloc((size_t)k * sizeof(double));
+    if (!taken || !w) {
+        free(taken);
+        free(w);
+        return -2;
+    }
+    for (int64_t j = 0; j < k; j++) {
+        int64_t best = -1;
+        for (int64_t i = 0; i < n; i++) {
+            if (taken[i])
+                continue;
+            if (best < 0) {
+                best = i;
+                continue;
+            }
+            if (isnan(y[best]))
+                continue; /* an earlier NaN is never beaten */
+            if (isnan(y[i]) || y[i] > y[best])
+                best = i;
+        }
+        taken[best] = 1;
+        index[j] = best;
+    }
+    free(taken);
+
+    const double l0 = y[index[0]];
+    if (T == 0 || isnan(l0)) {
+        for (int64_t j = 0; j < k; j++)
+            prob[j] = isnan(l0) ? NAN : (j == 0 ? 1.0 : 0.0);
+        *token = index[0];
+        free(w);
+        return 0;
+    }
+    double S = 0;
+    for (int64_t j = 0; j < k; j++) {
+        const double l = y[index[j]];
+        if (isinf(l0) && l0 > 0)
+            w[j] = (l == l0) ? 1.0 : 0.0;
+        else if (isinf(l0))
+            w[j] = 1.0;
+        else
+            w[j] = exp((l - l0) / T);
+        S += w[j];
+    }
+    for (int64_t j = 0; j < k; j++)
+        prob[j] = w[j] / S;
+    const double uu = (u > 0) ? (u < 1 ? u : 1) : 0;
+    const double target = uu * S;
+    double c = 0;
+    int64_t pick = -1;
+    for (int64_t j = 0; j < k && pick < 0; j++) {
+        c += w[j];
+        if (c > target)
+            pick = j;
+    }
+    if (pick < 0)
+        for (int64_t j = 0; j < k; j++)
+            if (w[j] > 0)
+                pick = j;
+    *token = index[pick];
+    free(w);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Row-range threading for timing the oracle on many host cores.  Each       */
 /* thread runs the single-threaded function above on its own row range.      */
 /* ------------------------------------------------------------------------ */
