@@ -777,6 +777,24 @@ def run_configs(args):
                 med, best = _graph_time(torch, acalls, reps=10)
                 emit(name, batch, "f8_matvec_argmax", nb - 4 * batch * f.R + 12 * batch, med,
                      best, k)
+                # head + top-64 temperature sampling (logits stored)
+                tk = 64
+                wst = torch.empty(qmv.TOPK_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+                uu = torch.rand(batch, device=dev)
+                ti = torch.empty((batch, tk), dtype=torch.int64, device=dev)
+                tv = torch.empty((batch, tk), device=dev)
+                tp = torch.empty((batch, tk), device=dev)
+                tt = torch.empty(batch, dtype=torch.int64, device=dev)
+                tcalls = [(lambda wi: lambda sh: qmv.f8_matvec_topk_sample(
+                    wi.data_ptr(), f.R, f.C, s5.data_ptr(), f.SR, f.SC, x.data_ptr(), batch,
+                    y.data_ptr(), tk, 1.0, uu.data_ptr(), ti.data_ptr(), tv.data_ptr(),
+                    tp.data_ptr(), tt.data_ptr(), wst.data_ptr(), wst.numel(), sh))(wi)
+                    for wi in ws]
+                if k == 1:
+                    tcalls = tcalls * 8
+                med, best = _graph_time(torch, tcalls, reps=10)
+                emit(name, batch, "f8_matvec_topk_sample(k=64)",
+                     nb + batch * (4 + tk * 16 + 8), med, best, k)
                 del ws, w
 
 

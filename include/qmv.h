@@ -63,7 +63,8 @@ typedef enum {
     QMV_ERR_OVERFLOW = 7,  /* a size product does not fit the library's limits  */
     QMV_ERR_ALIAS = 8,     /* an output overlaps an input                        */
     QMV_ERR_CUDA = 9,      /* the CUDA runtime reported an error at launch       */
-    QMV_ERR_ROW_ID = 10    /* (device status) a gathered row id was out of range */
+    QMV_ERR_ROW_ID = 10,   /* (device status) a gathered row id was out of range */
+    QMV_ERR_ARG = 11       /* a scalar argument (a temperature) is out of range  */
 } qmv_status;
 
 /* Largest group the CQ kernels transform (one group must fit in shared
@@ -339,6 +340,79 @@ QMV_API qmv_status f8_matvec_argmax_noalloc(const uint8_t *w, int64_t R, int64_t
                                             const float *x, int32_t batch, float *y,
                                             int64_t *out_index, float *out_value,
                                             qmv_stream stream);
+
+/* Largest k of topk_sample and f8_matvec_topk_sample. */
+#define QMV_MAX_TOPK 64
+/* Most slices the first selection pass makes, over all vectors of a call. */
+#define QMV_TOPK_MAX_SLICES 1024
+/* Bytes of device workspace topk_sample needs, for any R, batch and k. */
+#define QMV_TOPK_WORKSPACE_BYTES ((int64_t)QMV_TOPK_MAX_SLICES * QMV_MAX_TOPK * 8)
+
+/*
+ * topk_sample -- top-k temperature sampling over head logits.  ds4f-disk
+ * issue #6, work item 3 (the head's logits feed top-k / temperature
+ * sampling) and step 3 (the sampler is a softmax driven by a seeded
+ * generator, so equal seeds give equal tokens).  The pages give no
+ * formulas; for each vector v this call computes:
+ *
+ *   1. the k best rows of y[v] in the greedy order of f8_matvec_argmax
+ *      (NaN above every number, then the larger value, then the lower row;
+ *      -0 equals +0), listed best first: rows i_0, ..., i_{k-1}, logits
+ *      l_j = y[v][i_j];
+ *   2. weights w_j = exp((l_j - l_0) / T) in float32 (so w_0 = 1);
+ *   3. cumulative sums c_j = w_0 + ... + w_j and S = c_{k-1}, in float32 by
+ *      one fixed-order scan (pairs (w_0, w_1), (w_2, w_3), ... added, then
+ *      a scan over the pairs); p_j = w_j / S;
+ *   4. the token i_j for the smallest j with c_j > u' * S, where u' is u[v]
+ *      clamped into [0, 1] (NaN read as 0); when rounding leaves no such j,
+ *      the last j with w_j > 0.
+ *
+ * Where the formula has no value its limit is used: T = 0 is greedy
+ * (token i_0, p = 1, 0, ...); a NaN l_0 gives token i_0 and NaN
+ * probabilities; l_0 = +inf shares the weight equally among the +inf
+ * entries; when every l_j is -inf the weights are equal.  The rows are
+ * exact; weights and probabilities are float32 (exp within a few ulp), so
+ * the token is the exact draw except when u' * S falls within rounding of
+ * a boundary between two entries.  The random draw is an input: u holds
+ * one uniform number per vector, produced by the caller's generator.
+ *
+ *   y            [batch, R] float32 logits, 1 <= R <= 2^31 - 1
+ *   k            1 <= k <= min(R, QMV_MAX_TOPK)
+ *   temperature  finite and >= 0, else QMV_ERR_ARG
+ *   u            [batch] float32 uniform draws
+ *   top_index    [batch, k] int64, written (i_0 .. i_{k-1})
+ *   top_value    [batch, k] float32 or NULL (l_0 .. l_{k-1})
+ *   top_prob     [batch, k] float32 or NULL (p_0 .. p_{k-1})
+ *   token        [batch] int64, written
+ *   workspace    device scratch of workspace_bytes >= QMV_TOPK_WORKSPACE_BYTES,
+ *                16-byte aligned, caller-owned; contents on entry ignored and
+ *                on exit unspecified.  Calls that overlap on the GPU must not
+ *                share a workspace.
+ * Errors: QMV_ERR_BATCH, QMV_ERR_SHAPE (R or k out of range, workspace too
+ * small), QMV_ERR_OVERFLOW (R above 2^31 - 1), QMV_ERR_ARG, QMV_ERR_NULL,
+ * QMV_ERR_ALIGN (float pointers 4-byte, int64 8-byte, workspace 16-byte),
+ * QMV_ERR_ALIAS (an output or the workspace overlaps an input or another
+ * output), QMV_ERR_CUDA.
+ */
+QMV_API qmv_status topk_sample(const float *y, int64_t R, int32_t batch, int32_t k,
+                               float temperature, const float *u, int64_t *top_index,
+                               float *top_value, float *top_prob, int64_t *token, void *workspace,
+                               int64_t workspace_bytes, qmv_stream stream);
+
+/*
+ * f8_matvec_topk_sample -- the head matvec then top-k temperature sampling:
+ * y = f8_matvec(w, scale, x) exactly as f8_matvec computes it (y is
+ * required and written), then topk_sample(y, ...).  The selection is made
+ * on the float32 logits this call writes.  Arguments and errors as the two
+ * calls; R >= 1.
+ */
+QMV_API qmv_status f8_matvec_topk_sample(const uint8_t *w, int64_t R, int64_t C,
+                                         const uint8_t *scale, int64_t SR, int64_t SC,
+                                         const float *x, int32_t batch, float *y, int32_t k,
+                                         float temperature, const float *u, int64_t *top_index,
+                                         float *top_value, float *top_prob, int64_t *token,
+                                         void *workspace, int64_t workspace_bytes,
+                                         qmv_stream stream);
 
 /* Human-readable name of a status code (static storage). */
 QMV_API const char *qmv_status_string(qmv_status status);

@@ -10,6 +10,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <climits>
 #include <cmath>
 
 #include <map>
@@ -189,6 +190,37 @@ int64_t cq_set_rows(const qmv_cq_matrix *mats, int32_t nmats) {
     return rows;
 }
 
+// Checks of the sampler's own arguments.  ins[0..nin) are the call's inputs
+// (u among them); y_out (y_out_bytes) is an output written before sampling,
+// or NULL.  Outputs and workspace must be apart from every input and from
+// each other.
+qmv_status check_topk(int64_t R, int32_t batch, int32_t k, float temperature, const float *u,
+                      const int64_t *top_index, const float *top_value, const float *top_prob,
+                      const int64_t *token, const void *workspace, int64_t workspace_bytes,
+                      const void *const *ins, const int64_t *inb, int nin, const void *y_out,
+                      int64_t y_out_bytes) {
+    if (R < 1) return QMV_ERR_SHAPE;
+    if (R > INT32_MAX) return QMV_ERR_OVERFLOW;
+    if (k < 1 || k > QMV_MAX_TOPK || k > R) return QMV_ERR_SHAPE;
+    if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return QMV_ERR_ARG;
+    if (!u || !top_index || !token || !workspace) return QMV_ERR_NULL;
+    if (!aligned(u, 4) || !aligned(top_index, 8) || !aligned(top_value, 4) ||
+        !aligned(top_prob, 4) || !aligned(token, 8) || !aligned(workspace, 16))
+        return QMV_ERR_ALIGN;
+    if (workspace_bytes < QMV_TOPK_WORKSPACE_BYTES) return QMV_ERR_SHAPE;
+    const int64_t bk = int64_t(batch) * k;
+    const void *outs[6] = {top_index, top_value, top_prob, token, workspace, y_out};
+    const int64_t outb[6] = {bk * 8, top_value ? bk * 4 : 0, top_prob ? bk * 4 : 0,
+                             int64_t(batch) * 8, workspace_bytes, y_out ? y_out_bytes : 0};
+    for (int i = 0; i < 6; i++) {
+        for (int j = 0; j < nin; j++)
+            if (overlaps(outs[i], outb[i], ins[j], inb[j])) return QMV_ERR_ALIAS;
+        for (int j = i + 1; j < 6; j++)
+            if (overlaps(outs[i], outb[i], outs[j], outb[j])) return QMV_ERR_ALIAS;
+    }
+    return QMV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -207,6 +239,7 @@ const char *qmv_status_string(qmv_status s) {
         case QMV_ERR_ALIAS: return "QMV_ERR_ALIAS: an output overlaps an input";
         case QMV_ERR_CUDA: return "QMV_ERR_CUDA: the CUDA runtime reported an error";
         case QMV_ERR_ROW_ID: return "QMV_ERR_ROW_ID: a gathered row id was out of range";
+        case QMV_ERR_ARG: return "QMV_ERR_ARG: a scalar argument is out of range";
     }
     return "unknown qmv_status";
 }
@@ -403,6 +436,51 @@ qmv_status f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scal
     if (R == 0) return QMV_OK;
     return qmv::launch_f8_matvec(w, R, C, scale, SR, SC, x, batch, y,
                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status topk_sample(const float *y, int64_t R, int32_t batch, int32_t k, float temperature,
+                       const float *u, int64_t *top_index, float *top_value, float *top_prob,
+                       int64_t *token, void *workspace, int64_t workspace_bytes, qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (R < 1) return QMV_ERR_SHAPE;
+    if (R > INT32_MAX) return QMV_ERR_OVERFLOW;
+    if (!y) return QMV_ERR_NULL;
+    if (!aligned(y, 4)) return QMV_ERR_ALIGN;
+    const void *ins[2] = {y, u};
+    const int64_t inb[2] = {int64_t(batch) * R * 4, int64_t(batch) * 4};
+    st = check_topk(R, batch, k, temperature, u, top_index, top_value, top_prob, token, workspace,
+                    workspace_bytes, ins, inb, 2, nullptr, 0);
+    if (st != QMV_OK) return st;
+    return qmv::launch_topk_sample(y, R, batch, k, temperature, u, top_index, top_value, top_prob,
+                                   token, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status f8_matvec_topk_sample(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                                 int64_t SR, int64_t SC, const float *x, int32_t batch, float *y,
+                                 int32_t k, float temperature, const float *u, int64_t *top_index,
+                                 float *top_value, float *top_prob, int64_t *token,
+                                 void *workspace, int64_t workspace_bytes, qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (R < 1 || R > kMaxDim || C < 1 || C > kMaxDim) return QMV_ERR_SHAPE;
+    if (SR < 1 || SR > R || SC < 1 || SC > C) return QMV_ERR_SHAPE;
+    int64_t wb = 0, sb = 0, xb = 0, yb = 0, t = 0;
+    if (!mul_ok(R, C, &wb) || !mul_ok(SR, SC, &sb) || !mul_ok(int64_t(batch) * 4, C, &xb) ||
+        !mul_ok(int64_t(batch) * 4, R, &yb) || !mul_ok(R, SR, &t) || !mul_ok(C, SC, &t))
+        return QMV_ERR_OVERFLOW;
+    if (!w || !scale || !x || !y) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(y, 4)) return QMV_ERR_ALIGN;
+    const void *ins[4] = {w, scale, x, u};
+    const int64_t inb[4] = {wb, sb, xb, int64_t(batch) * 4};
+    st = check_topk(R, batch, k, temperature, u, top_index, top_value, top_prob, token, workspace,
+                    workspace_bytes, ins, inb, 4, y, yb);
+    if (st != QMV_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = qmv::launch_f8_matvec(w, R, C, scale, SR, SC, x, batch, y, s);
+    if (st != QMV_OK) return st;
+    return qmv::launch_topk_sample(y, R, batch, k, temperature, u, top_index, top_value, top_prob,
+                                   token, workspace, s);
 }
 
 }  // extern "C"

@@ -94,4 +94,12 @@ qmv_status launch_f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const
                                    int64_t *out_index, float *out_value, void *workspace,
                                    cudaStream_t s);
 
+
+// ---- top-k sampling ----------------------------------------------------------
+// Slices per vector of the first selection pass (1 means a single launch).
+int topk_slices(int64_t R, int batch);
+qmv_status launch_topk_sample(const float *y, int64_t R, int batch, int k, float temperature,
+                              const float *u, int64_t *top_index, float *top_value, float *top_prob,
+                              int64_t *token, void *workspace, cudaStream_t s);
+
 }  // namespace qmv

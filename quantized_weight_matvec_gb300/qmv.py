@@ -20,10 +20,13 @@ QMV_OK = 0
 STATUS_NAMES = {0: "QMV_OK", 1: "QMV_ERR_NULL", 2: "QMV_ERR_SHAPE", 3: "QMV_ERR_BITS",
                 4: "QMV_ERR_GROUP", 5: "QMV_ERR_BATCH", 6: "QMV_ERR_ALIGN",
                 7: "QMV_ERR_OVERFLOW", 8: "QMV_ERR_ALIAS", 9: "QMV_ERR_CUDA",
-                10: "QMV_ERR_ROW_ID"}
+                10: "QMV_ERR_ROW_ID", 11: "QMV_ERR_ARG"}
 MAX_BATCH = 8
 MAX_GROUP = 32768
 ARGMAX_MAX_BLOCKS = 2048
+MAX_TOPK = 64
+TOPK_MAX_SLICES = 1024
+TOPK_WORKSPACE_BYTES = TOPK_MAX_SLICES * MAX_TOPK * 8
 
 
 def f8_argmax_workspace_bytes(batch: int) -> int:
@@ -79,9 +82,14 @@ def load() -> ctypes.CDLL:
     lib.f8_matvec_argmax.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P, I64, P]
     lib.f8_matvec_argmax_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P]
     lib.hadamard_mlp.argtypes = [P, I64, I64, P, P, P, P, P, I32, P, P]
+    F = ctypes.c_float
+    lib.topk_sample.argtypes = [P, I64, I32, I32, F, P, P, P, P, P, P, I64, P]
+    lib.f8_matvec_topk_sample.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, I32, F, P, P, P,
+                                          P, P, P, I64, P]
     for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.cq_matvec_multi,
                lib.cq_prepare_matvec, lib.f8_matvec, lib.i8_matvec, lib.f8_matvec_argmax,
-               lib.f8_matvec_argmax_noalloc, lib.hadamard_mlp):
+               lib.f8_matvec_argmax_noalloc, lib.hadamard_mlp, lib.topk_sample,
+               lib.f8_matvec_topk_sample):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
     lib.qmv_status_string.restype = ctypes.c_char_p
@@ -177,6 +185,24 @@ def f8_matvec_argmax_noalloc(w: int, R: int, C: int, scale: int, SR: int, SC: in
     return load().f8_matvec_argmax_noalloc(w or None, R, C, scale or None, SR, SC, x or None,
                                            batch, y or None, out_index or None,
                                            out_value or None, stream or None)
+
+
+def topk_sample(y: int, R: int, batch: int, k: int, temperature: float, u: int, top_index: int,
+                top_value: int, top_prob: int, token: int, workspace: int, workspace_bytes: int,
+                stream: int = 0) -> int:
+    return load().topk_sample(y or None, R, batch, k, temperature, u or None, top_index or None,
+                              top_value or None, top_prob or None, token or None,
+                              workspace or None, workspace_bytes, stream or None)
+
+
+def f8_matvec_topk_sample(w: int, R: int, C: int, scale: int, SR: int, SC: int, x: int,
+                          batch: int, y: int, k: int, temperature: float, u: int, top_index: int,
+                          top_value: int, top_prob: int, token: int, workspace: int,
+                          workspace_bytes: int, stream: int = 0) -> int:
+    return load().f8_matvec_topk_sample(w or None, R, C, scale or None, SR, SC, x or None, batch,
+                                        y or None, k, temperature, u or None, top_index or None,
+                                        top_value or None, top_prob or None, token or None,
+                                        workspace or None, workspace_bytes, stream or None)
 
 
 # --------------------------------------------------------------------------
@@ -394,3 +420,54 @@ def hadamard_mlp_t(x, D, d1, d2, d3, residual=None, u=None, out=None, stream=Non
     _check(hadamard_mlp(x.data_ptr(), n, D, d1.data_ptr(), d2.data_ptr(), d3.data_ptr(), ptrs[0],
                         ptrs[1], batch, out.data_ptr(), _stream(stream)), "hadamard_mlp")
     return out
+
+
+def _topk_outputs(batch, k, device, workspace):
+    torch = _torch()
+    idx = torch.empty((batch, k), dtype=torch.int64, device=device)
+    val = torch.empty((batch, k), dtype=torch.float32, device=device)
+    prob = torch.empty((batch, k), dtype=torch.float32, device=device)
+    tok = torch.empty(batch, dtype=torch.int64, device=device)
+    if workspace is None:
+        workspace = torch.empty(TOPK_WORKSPACE_BYTES, dtype=torch.uint8, device=device)
+    _dev(workspace, torch.uint8, "workspace")
+    return idx, val, prob, tok, workspace
+
+
+def topk_sample_t(y, k, temperature, u, workspace=None, stream=None):
+    """Top-k temperature sampling over logits y [B, R]: returns (top_index
+    [B, k] int64 best first, top_value [B, k], top_prob [B, k], token [B]
+    int64).  u [B] float32 holds one uniform draw per vector."""
+    torch = _torch()
+    y = _dev(y, torch.float32, "y")
+    u = _dev(u, torch.float32, "u")
+    batch, R = (y.shape[0], y.shape[1]) if y.dim() == 2 else (1, y.numel())
+    idx, val, prob, tok, workspace = _topk_outputs(batch, int(k), y.device, workspace)
+    _check(topk_sample(y.data_ptr(), R, batch, int(k), float(temperature), u.data_ptr(),
+                       idx.data_ptr(), val.data_ptr(), prob.data_ptr(), tok.data_ptr(),
+                       workspace.data_ptr(), workspace.numel(), _stream(stream)), "topk_sample")
+    return idx, val, prob, tok
+
+
+def f8_matvec_topk_sample_t(w, scale, x, k, temperature, u, y=None, workspace=None,
+                            stream=None):
+    """The F8 head then top-k temperature sampling: returns (y [B, R],
+    top_index, top_value, top_prob, token) as topk_sample_t."""
+    torch = _torch()
+    w = _dev(w, torch.uint8, "w")
+    scale = _dev(scale, torch.uint8, "scale")
+    x = _dev(x, torch.float32, "x")
+    u = _dev(u, torch.float32, "u")
+    R, C = w.shape
+    SR, SC = scale.shape
+    batch = x.shape[0] if x.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((batch, R), dtype=torch.float32, device=w.device)
+    _dev(y, torch.float32, "y")
+    idx, val, prob, tok, workspace = _topk_outputs(batch, int(k), w.device, workspace)
+    _check(f8_matvec_topk_sample(w.data_ptr(), R, C, scale.data_ptr(), SR, SC, x.data_ptr(),
+                                 batch, y.data_ptr(), int(k), float(temperature), u.data_ptr(),
+                                 idx.data_ptr(), val.data_ptr(), prob.data_ptr(), tok.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "f8_matvec_topk_sample")
+    return y, idx, val, prob, tok

@@ -29,7 +29,7 @@ def test_header_declares_every_entry_point():
     names = declared_functions()
     for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec", "f8_matvec_argmax",
               "cq_matvec_multi", "cq_prepare_matvec", "i8_matvec", "hadamard_mlp",
-              "qmv_status_string", "qmv_abi_version"):
+              "topk_sample", "f8_matvec_topk_sample", "qmv_status_string", "qmv_abi_version"):
         assert n in names
 
 
@@ -132,6 +132,41 @@ def test_f8_argmax_rejections():
     assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, W, need) == 8         # workspace over weights
     assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, Y + 4, K, need) == 8     # value inside y
     assert a(W, 16, 16, S, 1, 1, X, 9, Y, I, V, K, need) == 5
+
+
+def test_topk_rejections():
+    Y, U, I, V, P, T, K = (FAKE + (i << 30) for i in range(7))
+    need = qmv.TOPK_WORKSPACE_BYTES
+    assert need == 1024 * 64 * 8
+
+    def t(y=Y, R=1000, b=2, k=8, temp=1.0, u=U, i=I, v=V, p=P, tok=T, ws=K, wsb=need):
+        return qmv.topk_sample(y, R, b, k, temp, u, i, v, p, tok, ws, wsb)
+    assert t(b=0) == 5 and t(b=9) == 5
+    assert t(R=0) == 2                          # R >= 1
+    assert t(R=1 << 31) == 7                    # rows must fit in 31 bits
+    assert t(k=0) == 2 and t(k=65) == 2         # 1 <= k <= QMV_MAX_TOPK
+    assert t(R=5, k=6) == 2                     # k <= R
+    assert t(temp=-1.0) == 11 and t(temp=float("nan")) == 11 and t(temp=float("inf")) == 11
+    assert t(y=0) == 1 and t(u=0) == 1 and t(i=0) == 1 and t(tok=0) == 1 and t(ws=0) == 1
+    assert t(y=Y + 2) == 6 and t(u=U + 1) == 6 and t(i=I + 4) == 6 and t(tok=T + 4) == 6
+    assert t(v=V + 2) == 6 and t(p=P + 1) == 6 and t(ws=K + 8) == 6
+    assert t(wsb=need - 1) == 2                 # workspace too small
+    assert t(i=Y + 64) == 8                     # index inside the logits
+    assert t(p=U) == 8                          # probabilities over the draws
+    assert t(ws=I) == 8                         # workspace over an output
+    assert t(tok=V + 8) == 8                    # two outputs overlap
+    W, S, X = FAKE + (8 << 30), FAKE + (9 << 30), FAKE + (10 << 30)
+
+    def f(w=W, R=1000, C=64, SR=1, SC=1, y=Y, k=8, temp=0.5, i=I, ws=K):
+        return qmv.f8_matvec_topk_sample(w, R, C, S, SR, SC, X, 2, y, k, temp, U, i, V, P, T,
+                                         ws, need)
+    assert f(R=0) == 2 and f(C=0) == 2 and f(SR=1001) == 2
+    assert f(y=0) == 1 and f(w=0) == 1
+    assert f(temp=-0.5) == 11
+    assert f(y=W + 16) == 8                     # logits over the weights
+    assert f(i=Y + 8) == 8                      # index inside the logits
+    assert f(ws=X) == 8                         # workspace over x
+    assert f(k=1001) == 2
 
 
 def test_cq_set_rejections():
