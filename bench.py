@@ -608,6 +608,65 @@ def _graph_time(torch, calls, reps=20):
     return statistics.median(ts), min(ts)
 
 
+def _cold_single(torch, call, flush, reps=20):
+    """Median and best microseconds of one call timed alone: L2 flushed by a
+    write larger than it, then an event pair around the single launch."""
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if call(st.cuda_stream) != 0:
+            raise RuntimeError("call failed")
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return statistics.median(ts), min(ts)
+
+
+def oracle_config_lines(only=None):
+    """CPU baseline per workload: the oracle's time for one whole C3 matvec
+    (CQ 2-bit vocabulary, prepare + matvec) and one whole C4 matvec (F8
+    4096 x 4096, batch 1), on one host thread and on all of them."""
+    import oracle
+    from quantized_weight_matvec_gb300 import synth
+    cores = os.cpu_count() or 1
+    for name in ("cq2_vocab", "f8_4096"):
+        if only and only not in name:
+            continue
+        if name == "cq2_vocab":
+            c = synth.workload_inputs(name, batch=1)
+            om = oracle.CQMatrix(c.output, c.input, c.input_padded, c.group, c.bits, c.packed,
+                                 c.norms, c.codebook)
+            nb = (cq_prepare_bytes(c.input, c.input_padded)
+                  + cq_matvec_bytes(c.output, c.input_padded, c.group, c.bits))
+
+            def once(th):
+                p = oracle.cq_prepare(c.x, c.input_padded, c.group, mode="f32")
+                om.matvec(p, threads=th, with_mag=False)
+            op = "oracle cq_prepare + cq_matvec"
+        else:
+            f = synth.workload_inputs(name, batch=1)
+            nb = f8_bytes(f.R, f.C, f.SR, f.SC)
+
+            def once(th):
+                oracle.f8_matvec(f.w, f.scale, f.x, threads=th, with_mag=False)
+            op = "oracle f8_matvec"
+        once(cores)  # library load and first touches
+        for th in sorted({1, cores}):
+            ts = []
+            for _ in range(3):
+                t = time.perf_counter()
+                once(th)
+                ts.append(time.perf_counter() - t)
+            us = statistics.median(ts) * 1e6
+            print(json.dumps({"workload": name, "batch": 1, "op": op, "bytes": nb,
+                              "us_median": round(us, 1), "gbs": round(nb / us / 1e3, 3),
+                              "cpu_baseline": {"kind": "oracle", "cores": th}}), flush=True)
+
+
 def run_configs(args):
     import torch
     from quantized_weight_matvec_gb300 import qmv, synth
@@ -619,13 +678,20 @@ def run_configs(args):
     def copies_for(nbytes):
         return max(1, min(4096, -(-2 * l2 // max(nbytes, 1))))
 
-    def emit(name, batch, op, nbytes, us_med, us_best, ncopies):
-        print(json.dumps({"workload": name, "batch": batch, "op": op, "bytes": nbytes,
-                          "us_median": round(us_med, 3), "us_best": round(us_best, 3),
-                          "gbs": round(nbytes / us_med / 1e3, 1),
-                          "frac_of_measured_hbm": round(nbytes / us_med / 1e3 / peak, 4),
-                          "frac_of_8tbs": round(nbytes / us_med / 1e3 / NOMINAL_HBM_GBS, 4),
-                          "l2_cold_copies": ncopies}), flush=True)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def emit(name, batch, op, nbytes, us_med, us_best, ncopies, call=None):
+        rec = {"workload": name, "batch": batch, "op": op, "bytes": nbytes,
+               "us_median": round(us_med, 3), "us_best": round(us_best, 3),
+               "gbs": round(nbytes / us_med / 1e3, 1),
+               "frac_of_measured_hbm": round(nbytes / us_med / 1e3 / peak, 4),
+               "frac_of_8tbs": round(nbytes / us_med / 1e3 / NOMINAL_HBM_GBS, 4),
+               "l2_cold_copies": ncopies}
+        if call is not None:  # one call alone after an L2 flush, launch latency included
+            cm, cb = _cold_single(torch, call, flush)
+            rec["us_single_cold_median"] = round(cm, 3)
+            rec["us_single_cold_best"] = round(cb, 3)
+        print(json.dumps(rec), flush=True)
 
     # matrix sets: one activation, several matrices sharing it (needle-2
     # sections 6-7: phiPre/phiPost/phiResidual, Q/K/V).  Per set call, three
@@ -701,12 +767,14 @@ def run_configs(args):
                                                                   y.data_ptr(), sh))(m)
                              for m in mats]
                     med, best = _graph_time(torch, calls)
-                    emit("%s/%dbit" % (name, bits), batch, "cq_matvec", nb, med, best, k)
+                    emit("%s/%dbit" % (name, bits), batch, "cq_matvec", nb, med, best, k,
+                         call=calls[0])
                     pc = [lambda sh: qmv.cq_prepare(mats[0].struct, x.data_ptr(), batch,
                                                     p.data_ptr(), sh)] * 64
                     med, best = _graph_time(torch, pc)
                     emit("%s/%dbit" % (name, bits), batch, "cq_prepare",
-                         cq_prepare_bytes(c.input, c.input_padded, batch), med, best, 1)
+                         cq_prepare_bytes(c.input, c.input_padded, batch), med, best, 1,
+                         call=pc[0])
                     if wl.get("gather"):
                         ids = torch.from_numpy(c.rows).to(dev)
                         emb = torch.empty((len(c.rows), c.input), device=dev)
@@ -716,7 +784,7 @@ def run_configs(args):
                         med, best = _graph_time(torch, gc)
                         emit("%s/%dbit" % (name, bits), len(c.rows), "cq_dequantize_row",
                              cq_gather_bytes(len(c.rows), c.input, c.input_padded, c.group,
-                                             c.bits), med, best, k)
+                                             c.bits), med, best, k, call=gc[0])
                     del packed, norms, mats
             elif wl["kind"] == "hmlp":
                 f = synth.workload_inputs(name, batch=batch)
@@ -729,7 +797,8 @@ def run_configs(args):
                     hx.data_ptr(), f.n, f.D, hd[0].data_ptr(), hd[1].data_ptr(), hd[2].data_ptr(),
                     hr.data_ptr(), hu.data_ptr(), batch, ho.data_ptr(), sh)] * 64
                 med, best = _graph_time(torch, hcalls)
-                emit("%s/D%d" % (name, f.D), batch, "hadamard_mlp", nb, med, best, 1)
+                emit("%s/D%d" % (name, f.D), batch, "hadamard_mlp", nb, med, best, 1,
+                     call=hcalls[0])
             elif wl["kind"] == "i8":
                 f = synth.workload_inputs(name, batch=batch)
                 nb = f.R * f.C + f.R * ((f.C + 15) // 16) + 4 * batch * (f.C + f.R)
@@ -745,7 +814,7 @@ def run_configs(args):
                 if k == 1:
                     calls = calls * 8
                 med, best = _graph_time(torch, calls, reps=10)
-                emit(name, batch, "i8_matvec", nb, med, best, k)
+                emit(name, batch, "i8_matvec", nb, med, best, k, call=calls[0])
                 del ws, w
             else:
                 f = synth.workload_inputs(name, batch=batch)
@@ -762,7 +831,7 @@ def run_configs(args):
                 if k == 1:
                     calls = calls * 8
                 med, best = _graph_time(torch, calls, reps=10)
-                emit(name, batch, "f8_matvec", nb, med, best, k)
+                emit(name, batch, "f8_matvec", nb, med, best, k, call=calls[0])
                 # head + greedy selection (no logits stored)
                 wsp = torch.empty(qmv.f8_argmax_workspace_bytes(batch), dtype=torch.uint8,
                                   device=dev)
@@ -776,7 +845,7 @@ def run_configs(args):
                     acalls = acalls * 8
                 med, best = _graph_time(torch, acalls, reps=10)
                 emit(name, batch, "f8_matvec_argmax", nb - 4 * batch * f.R + 12 * batch, med,
-                     best, k)
+                     best, k, call=acalls[0])
                 # head + top-64 temperature sampling (logits stored)
                 tk = 64
                 wst = torch.empty(qmv.TOPK_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
@@ -794,8 +863,9 @@ def run_configs(args):
                     tcalls = tcalls * 8
                 med, best = _graph_time(torch, tcalls, reps=10)
                 emit(name, batch, "f8_matvec_topk_sample(k=64)",
-                     nb + batch * (4 + tk * 16 + 8), med, best, k)
+                     nb + batch * (4 + tk * 16 + 8), med, best, k, call=tcalls[0])
                 del ws, w
+    oracle_config_lines(args.only)
 
 
 def main(argv=None):
