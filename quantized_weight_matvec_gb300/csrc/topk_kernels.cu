@@ -34,6 +34,7 @@ constexpr int kCand = 1024;            // most entries ranked directly
 constexpr int kE = kTile / kThreads;   // entries per thread and tile
 
 static_assert(kMaxK <= kGroups && kGroups <= kThreads, "tau needs at least k groups");
+static_assert(kWarps <= 32, "one warp scans the warp totals");
 static_assert(kTile % kThreads == 0 && kCand % kThreads == 0, "loads and ranks per thread");
 
 // Greedy order as a uint32: NaN highest, then larger values, -0 equal to
@@ -231,12 +232,17 @@ __device__ __forceinline__ int select_tile(Smem &s, const uint32_t (&key)[kE], c
     }
     if (lane == 31) s.wsum[warp] = incl;
     __syncthreads();
-    int base = 0, C = 0;
+    int base, C;
+    {  // every warp scans the warp totals: its exclusive prefix and the sum
+        const int wv = lane < kWarps ? s.wsum[lane] : 0;
+        int sc = wv;
 #pragma unroll
-    for (int w2 = 0; w2 < kWarps; w2++) {
-        const int v = s.wsum[w2];
-        base += (w2 < warp) ? v : 0;
-        C += v;
+        for (int o = 1; o < kWarps; o <<= 1) {
+            const int t = __shfl_up_sync(kFull, sc, o);
+            if (lane >= o) sc += t;
+        }
+        C = __shfl_sync(kFull, sc, kWarps - 1);
+        base = __shfl_sync(kFull, sc - wv, warp);
     }
     if (C == 0) return kept;  // a tile of missing entries and nothing kept
     if (C <= kCand) {
@@ -256,9 +262,12 @@ __device__ __forceinline__ int select_tile(Smem &s, const uint32_t (&key)[kE], c
         C = k;
     }
     __syncthreads();
-    // rank = how many gathered entries beat this one (equal ones by their
-    // position), so ranks are distinct; only ranks below k stay.  With few
-    // entries, `parts` neighbouring lanes split each entry's count.
+    // rank = how many gathered entries beat this one; only ranks below k
+    // stay.  The gathered composites are distinct (each row of a vector
+    // enters once, and padding, key 0, is never gathered: tau >= 1 on the
+    // direct path, and the radix path takes k real entries out of more than
+    // kCand), so the ranks are too.  With few entries, `parts` neighbouring
+    // lanes split each entry's count.
     int parts = 1;  // a power of two, so a group of lanes adds its parts up
     while (parts < 32 && parts * 2 * C <= kThreads) parts *= 2;
 #pragma unroll
@@ -270,7 +279,7 @@ __device__ __forceinline__ int select_tile(Smem &s, const uint32_t (&key)[kE], c
 #pragma unroll 4
             for (int j = p; j < C; j += parts) {
                 const uint64_t o = s.cand[j];
-                r += (o > mine || (o == mine && j < i)) ? 1 : 0;
+                r += (o > mine) ? 1 : 0;
             }
         }
         for (int o = 1; o < parts; o <<= 1) r += __shfl_xor_sync(kFull, r, o);

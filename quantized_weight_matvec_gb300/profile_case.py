@@ -6,7 +6,8 @@ Kernels: f8 (E4M3 head-shaped rows x 4096, scales [rows/128, 32]), i8
 (int8 rows x 4096, per-16 E8M0 group scales), cq2
 (2-bit rows x 512, group 128, the table kernel), cqvec (--bits-bit rows x
 512, group 64, the vectorised kernel), gather (64 rows of a 32768 x 512
-2-bit matrix), prepare.  Inputs are seeded synthetic data; the case is chosen
+2-bit matrix), prepare, topk (top-64 temperature sampling over --rows
+normal logits per vector).  Inputs are seeded synthetic data; the case is chosen
 larger than L2 but a few hundred MB at most.  Prints one checksum line and
 no timings: numbers taken under a profiler are not measurements.
 """
@@ -21,7 +22,7 @@ from . import qmv, synth
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["f8", "i8", "cq2", "cqvec", "gather", "prepare"], required=True)
+    ap.add_argument("--kernel", choices=["f8", "i8", "cq2", "cqvec", "gather", "prepare", "topk"], required=True)
     ap.add_argument("--bits", type=int, default=4)
     ap.add_argument("--rows", type=int, default=65536)
     ap.add_argument("--batch", type=int, default=1)
@@ -44,6 +45,13 @@ def main(argv=None):
         for _ in range(args.iters):
             qmv.i8_matvec_t(w, s, x, out=y)
         out = y
+    elif args.kernel == "topk":
+        g = torch.Generator(device="cpu").manual_seed(0)
+        y = (torch.randn((args.batch, args.rows), generator=g) * 3).to(dev)
+        u = torch.rand(args.batch, generator=g).to(dev)
+        for _ in range(args.iters):
+            idx, val, prob, tok = qmv.topk_sample_t(y, 64, 1.0, u)
+        out = prob
     elif args.kernel == "cqvec":
         c = synth.cq_inputs(2, args.rows, 512, 64, args.bits, batch=args.batch)
         m = qmv.CQMatrix.from_numpy(c, device=dev)
