@@ -815,6 +815,23 @@ def run_configs(args):
                     calls = calls * 8
                 med, best = _graph_time(torch, calls, reps=10)
                 emit(name, batch, "i8_matvec", nb, med, best, k, call=calls[0])
+                # the I8 head then top-64 temperature sampling (logits stored)
+                tk = 64
+                wst = torch.empty(qmv.TOPK_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+                uu = torch.rand(batch, device=dev)
+                ti = torch.empty((batch, tk), dtype=torch.int64, device=dev)
+                tv = torch.empty((batch, tk), device=dev)
+                tp = torch.empty((batch, tk), device=dev)
+                tt = torch.empty(batch, dtype=torch.int64, device=dev)
+                tcalls = [(lambda wi: lambda sh: qmv.i8_matvec_topk_sample(
+                    wi.data_ptr(), f.R, f.C, s8.data_ptr(), x.data_ptr(), batch, y.data_ptr(), tk,
+                    1.0, uu.data_ptr(), ti.data_ptr(), tv.data_ptr(), tp.data_ptr(),
+                    tt.data_ptr(), wst.data_ptr(), wst.numel(), sh))(wi) for wi in ws]
+                if k == 1:
+                    tcalls = tcalls * 8
+                med, best = _graph_time(torch, tcalls, reps=10)
+                emit(name, batch, "i8_matvec_topk_sample(k=64)", nb + batch * (4 + tk * 16 + 8),
+                     med, best, k, call=tcalls[0])
                 del ws, w
             else:
                 f = synth.workload_inputs(name, batch=batch)

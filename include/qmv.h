@@ -414,6 +414,20 @@ QMV_API qmv_status f8_matvec_topk_sample(const uint8_t *w, int64_t R, int64_t C,
                                          void *workspace, int64_t workspace_bytes,
                                          qmv_stream stream);
 
+/*
+ * i8_matvec_topk_sample -- the I8 head then top-k temperature sampling, the
+ * token loop of ds4f-disk issue #6 after step 4 (I8 head over the ~246k
+ * vocabulary, then the deterministic sampler): y = i8_matvec(w, scale, x)
+ * exactly as i8_matvec computes it (y is required and written), then
+ * topk_sample(y, ...).  Arguments and errors as the two calls; R >= 1.
+ */
+QMV_API qmv_status i8_matvec_topk_sample(const int8_t *w, int64_t R, int64_t C,
+                                         const uint8_t *scale, const float *x, int32_t batch,
+                                         float *y, int32_t k, float temperature, const float *u,
+                                         int64_t *top_index, float *top_value, float *top_prob,
+                                         int64_t *token, void *workspace,
+                                         int64_t workspace_bytes, qmv_stream stream);
+
 /* Human-readable name of a status code (static storage). */
 QMV_API const char *qmv_status_string(qmv_status status);
 

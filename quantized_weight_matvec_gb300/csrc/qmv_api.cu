@@ -483,4 +483,30 @@ qmv_status f8_matvec_topk_sample(const uint8_t *w, int64_t R, int64_t C, const u
                                    token, workspace, s);
 }
 
+qmv_status i8_matvec_topk_sample(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                                 const float *x, int32_t batch, float *y, int32_t k,
+                                 float temperature, const float *u, int64_t *top_index,
+                                 float *top_value, float *top_prob, int64_t *token,
+                                 void *workspace, int64_t workspace_bytes, qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (R < 1 || R > kMaxDim || C < 1 || C > kMaxDim) return QMV_ERR_SHAPE;
+    int64_t wb = 0, sb = 0, xb = 0, yb = 0;
+    if (!mul_ok(R, C, &wb) || !mul_ok(R, (C + 15) / 16, &sb) || !mul_ok(int64_t(batch) * 4, C, &xb) ||
+        !mul_ok(int64_t(batch) * 4, R, &yb))
+        return QMV_ERR_OVERFLOW;
+    if (!w || !scale || !x || !y) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(y, 4)) return QMV_ERR_ALIGN;
+    const void *ins[4] = {w, scale, x, u};
+    const int64_t inb[4] = {wb, sb, xb, int64_t(batch) * 4};
+    st = check_topk(R, batch, k, temperature, u, top_index, top_value, top_prob, token, workspace,
+                    workspace_bytes, ins, inb, 4, y, yb);
+    if (st != QMV_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = qmv::launch_i8_matvec(w, R, C, scale, x, batch, y, s);
+    if (st != QMV_OK) return st;
+    return qmv::launch_topk_sample(y, R, batch, k, temperature, u, top_index, top_value, top_prob,
+                                   token, workspace, s);
+}
+
 }  // extern "C"

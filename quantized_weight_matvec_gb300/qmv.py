@@ -86,10 +86,12 @@ def load() -> ctypes.CDLL:
     lib.topk_sample.argtypes = [P, I64, I32, I32, F, P, P, P, P, P, P, I64, P]
     lib.f8_matvec_topk_sample.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, I32, F, P, P, P,
                                           P, P, P, I64, P]
+    lib.i8_matvec_topk_sample.argtypes = [P, I64, I64, P, P, I32, P, I32, F, P, P, P, P, P, P,
+                                          I64, P]
     for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.cq_matvec_multi,
                lib.cq_prepare_matvec, lib.f8_matvec, lib.i8_matvec, lib.f8_matvec_argmax,
                lib.f8_matvec_argmax_noalloc, lib.hadamard_mlp, lib.topk_sample,
-               lib.f8_matvec_topk_sample):
+               lib.f8_matvec_topk_sample, lib.i8_matvec_topk_sample):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
     lib.qmv_status_string.restype = ctypes.c_char_p
@@ -200,6 +202,16 @@ def f8_matvec_topk_sample(w: int, R: int, C: int, scale: int, SR: int, SC: int, 
                           top_value: int, top_prob: int, token: int, workspace: int,
                           workspace_bytes: int, stream: int = 0) -> int:
     return load().f8_matvec_topk_sample(w or None, R, C, scale or None, SR, SC, x or None, batch,
+                                        y or None, k, temperature, u or None, top_index or None,
+                                        top_value or None, top_prob or None, token or None,
+                                        workspace or None, workspace_bytes, stream or None)
+
+
+def i8_matvec_topk_sample(w: int, R: int, C: int, scale: int, x: int, batch: int, y: int, k: int,
+                          temperature: float, u: int, top_index: int, top_value: int,
+                          top_prob: int, token: int, workspace: int, workspace_bytes: int,
+                          stream: int = 0) -> int:
+    return load().i8_matvec_topk_sample(w or None, R, C, scale or None, x or None, batch,
                                         y or None, k, temperature, u or None, top_index or None,
                                         top_value or None, top_prob or None, token or None,
                                         workspace or None, workspace_bytes, stream or None)
@@ -470,4 +482,27 @@ def f8_matvec_topk_sample_t(w, scale, x, k, temperature, u, y=None, workspace=No
                                  idx.data_ptr(), val.data_ptr(), prob.data_ptr(), tok.data_ptr(),
                                  workspace.data_ptr(), workspace.numel(), _stream(stream)),
            "f8_matvec_topk_sample")
+    return y, idx, val, prob, tok
+
+
+def i8_matvec_topk_sample_t(w, scale, x, k, temperature, u, y=None, workspace=None,
+                            stream=None):
+    """The I8 head then top-k temperature sampling: returns (y [B, R],
+    top_index, top_value, top_prob, token) as topk_sample_t."""
+    torch = _torch()
+    w = _dev(w, torch.int8, "w")
+    scale = _dev(scale, torch.uint8, "scale")
+    x = _dev(x, torch.float32, "x")
+    u = _dev(u, torch.float32, "u")
+    R, C = w.shape
+    batch = x.shape[0] if x.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((batch, R), dtype=torch.float32, device=w.device)
+    _dev(y, torch.float32, "y")
+    idx, val, prob, tok, workspace = _topk_outputs(batch, int(k), w.device, workspace)
+    _check(i8_matvec_topk_sample(w.data_ptr(), R, C, scale.data_ptr(), x.data_ptr(), batch,
+                                 y.data_ptr(), int(k), float(temperature), u.data_ptr(),
+                                 idx.data_ptr(), val.data_ptr(), prob.data_ptr(), tok.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "i8_matvec_topk_sample")
     return y, idx, val, prob, tok

@@ -29,7 +29,8 @@ def test_header_declares_every_entry_point():
     names = declared_functions()
     for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec", "f8_matvec_argmax",
               "cq_matvec_multi", "cq_prepare_matvec", "i8_matvec", "hadamard_mlp",
-              "topk_sample", "f8_matvec_topk_sample", "qmv_status_string", "qmv_abi_version"):
+              "topk_sample", "f8_matvec_topk_sample", "i8_matvec_topk_sample",
+              "qmv_status_string", "qmv_abi_version"):
         assert n in names
 
 
@@ -167,6 +168,15 @@ def test_topk_rejections():
     assert f(i=Y + 8) == 8                      # index inside the logits
     assert f(ws=X) == 8                         # workspace over x
     assert f(k=1001) == 2
+
+    def g(w=W, R=1000, C=64, y=Y, k=8, temp=0.5, i=I, ws=K):
+        return qmv.i8_matvec_topk_sample(w, R, C, S, X, 2, y, k, temp, U, i, V, P, T, ws, need)
+    assert g(R=0) == 2 and g(C=0) == 2 and g(k=0) == 2
+    assert g(y=0) == 1 and g(w=0) == 1
+    assert g(temp=float("nan")) == 11
+    assert g(y=W + 16) == 8                     # logits over the weights
+    assert g(i=Y + 8) == 8                      # index inside the logits
+    assert g(y=Y + 2) == 6
 
 
 def test_cq_set_rejections():

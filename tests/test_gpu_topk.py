@@ -212,3 +212,22 @@ def test_f8_head_topk_greedy_matches_argmax():
     torch.cuda.synchronize()
     assert torch.equal(tok, am_idx)
     assert torch.equal(val[:, 0], am_val)
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_i8_head_topk_sample(batch):
+    """The I8 head (245760 x 4096, per-16 E8M0 group scales) then sampling,
+    the token loop of the I8 head: y is i8_matvec's output bit for bit and
+    the sampler works on exactly that y."""
+    f = synth.i8_inputs(7, 245760, 4096, 110, 124, batch=batch)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    u = np.random.default_rng(batch + 10).random(batch).astype(np.float32)
+    y, idx, val, prob, tok = qmv.i8_matvec_topk_sample_t(w, s, x, 64, 0.7, dev(u))
+    y_plain = qmv.i8_matvec_t(w, s, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), y_plain.view(torch.int32))
+    yh = y.cpu().numpy()
+    check(yh, 64, 0.7, u, (idx, val, prob, tok))
+    for r in np.unique(idx.cpu().numpy().ravel())[:64]:
+        ref, mag = oracle.i8_matvec(f.w, f.scale, f.x, rows=(int(r), int(r) + 1))
+        assert np.all(np.abs(yh[:, r] - ref[:, r]) <= 1e-4 * mag[:, r] + 1e-6)
