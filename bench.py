@@ -572,7 +572,7 @@ def run_reference(args):
 
 # --------------------------------------------------------------------------
 # per-workload sweep (--configs): every workload and batch of the pages'
-# shapes, one JSON line each; not the default bench line
+# shapes, one JSON line each (the default run prints the one step line)
 # --------------------------------------------------------------------------
 
 def _graph_time(torch, calls, reps=20):
