@@ -231,3 +231,29 @@ def test_i8_head_topk_sample(batch):
     for r in np.unique(idx.cpu().numpy().ravel())[:64]:
         ref, mag = oracle.i8_matvec(f.w, f.scale, f.x, rows=(int(r), int(r) + 1))
         assert np.all(np.abs(yh[:, r] - ref[:, r]) <= 1e-4 * mag[:, r] + 1e-6)
+
+
+@pytest.mark.parametrize("R,k", [(64, 64), (65, 64), (4096, 64), (4160, 64), (8192, 33)])
+def test_topk_k_near_R_and_tile_edges(R, k):
+    """k equal to R, one row more than k, and R at and just past the
+    4096-entry tile (one slice, then two slices with a ragged second)."""
+    y = logits(R * 7 + k, 3, R, "ties")
+    u = np.array([0.05, 0.5, 0.95], np.float32)
+    check(y, k, 0.6, u, run(y, k, 0.6, u))
+
+
+@pytest.mark.parametrize("batch", [2, 3, 5])
+def test_f8_topk_sample_tensor_core_batches(batch):
+    """The fused call where the head runs on the tensor-core kernels with a
+    partly used vector group (batch 3, 5)."""
+    f = synth.f8_inputs(9, 20000, 1024, 40, 8, 118, 132, batch=batch)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    u = np.random.default_rng(batch + 20).random(batch).astype(np.float32)
+    y, idx, val, prob, tok = qmv.f8_matvec_topk_sample_t(w, s, x, 16, 1.5, dev(u))
+    y_plain = qmv.f8_matvec_t(w, s, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), y_plain.view(torch.int32))
+    yh = y.cpu().numpy()
+    check(yh, 16, 1.5, u, (idx, val, prob, tok))
+    ref, mag = oracle.f8_matvec(f.w, f.scale, f.x)
+    assert np.all(np.abs(yh - ref) <= 1e-4 * mag + 1e-6)
