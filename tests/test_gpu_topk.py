@@ -214,7 +214,7 @@ def test_f8_head_topk_greedy_matches_argmax():
     assert torch.equal(val[:, 0], am_val)
 
 
-@pytest.mark.parametrize("batch", [1, 4])
+@pytest.mark.parametrize("batch", [1, 4, 8])
 def test_i8_head_topk_sample(batch):
     """The I8 head (245760 x 4096, per-16 E8M0 group scales) then sampling,
     the token loop of the I8 head: y is i8_matvec's output bit for bit and
