@@ -301,6 +301,26 @@ def test_dequantize_row_matches_hadamard(bits, group):
     assert np.allclose(got, want, rtol=0, atol=tol)
 
 
+def test_dequantize_row_scale_rounding_golden():
+    """needle-2 "Row gather" with section 2's scaling: levels times the norm
+    rounded to float32, float32 butterflies, then RN32(RN64(v * s)) with
+    s = 1 / sqrt(group) in float64.  The golden values are derived by hand in
+    the file; a float32 scale product, or an unrounded level * norm, gives a
+    different bit pattern."""
+    for case, group, inp, code, l1, l2, even, odd in read_golden("dequantize_scale_rounding.txt"):
+        group, inp = int(group), int(inp)
+        packed = np.zeros((1, (group * 2 + 7) // 8), np.uint8)
+        packed[0, 0] = 1 | (2 << 2)  # column 0 -> index 1, column 1 -> index 2
+        norms = np.array([[int(code, 16)]], np.uint16)
+        cb = np.array([0.0, parse_float(l1), parse_float(l2), 0.0], np.float32)
+        m = oracle.CQMatrix(1, inp, group, group, 2, packed, norms, cb)
+        got, bad = m.dequantize_rows(np.array([0], np.int32))
+        assert not bad
+        want = np.where(np.arange(inp) % 2 == 0, np.float32(parse_float(even)),
+                        np.float32(parse_float(odd))).astype(np.float32)
+        assert np.array_equal(got[0].view(np.uint32), want.view(np.uint32)), case
+
+
 def test_dequantize_row_out_of_range_gives_zero_row():
     c, m = _cq(2, output=4, inp=32, group=32)
     got, bad = m.dequantize_rows(np.array([1, 4, -1, 0], np.int32))
@@ -458,10 +478,15 @@ def test_hadamard_mlp_f64_matches_dense_hadamard(D, n):
     z[:, :n] = x
     z = (z * d1) @ Hn.T
     z = d2 * z
-    z = z * expit(z)
-    z = (z @ Hn.T) * d3
+    silu = z * expit(z)
+    z = (silu @ Hn.T) * d3
     want = (res + z[:, :n]) - u
     assert np.all(np.abs(got - want) <= 1e-12 * mag + 1e-300)
+    # mag is the size of exactly the terms the last transform and the
+    # epilogue add: sum_j |Hn[i, j] * silu_j * d3_i| + |residual_i| + |u_i|
+    want_mag = (np.abs(silu) @ np.abs(Hn).T) * np.abs(d3)
+    want_mag = want_mag[:, :n] + np.abs(res) + np.abs(u)
+    assert np.allclose(mag, want_mag, rtol=1e-12, atol=0)
 
 
 def test_hadamard_mlp_tanh_closed_form():
@@ -529,6 +554,53 @@ def test_hadamard_mlp_pads_before_the_first_diagonal():
     d1[25] = np.inf
     got, _ = oracle.hadamard_mlp(x, D, d1, d2, d3)
     assert np.all(np.isnan(got))
+
+
+def test_hadamard_mlp_silu_on_the_float64_product():
+    """needle-2 section 8 stores silu(d2 * z) into a Float32Array from JS
+    numbers: the product d2 * z is the exact float64 one and silu is
+    evaluated in float64, then rounded once.  At D = 1 both normalised
+    transforms are the identity (1/sqrt(1) = 1), so with d1 = d3 = 1 the block
+    returns RN32(silu(d2 * x)).  Expected values use scipy's logistic function
+    (v * expit(v)); inputs whose float64 value lies within 2^-40 relative of a
+    float32 rounding midpoint are skipped, so the two float64 formulations
+    round the same way."""
+    from scipy.special import expit
+    rng = np.random.default_rng(77)
+    x = rng.uniform(-6, 6, 512).astype(np.float32)
+    d2 = rng.uniform(0.5, 3.0, 512).astype(np.float32)
+    one = np.ones(1, np.float32)
+    checked = 0
+    for xi, gi in zip(x, d2):
+        v = float(gi) * float(xi)  # exact: two float32 factors
+        w = v * float(expit(v))
+        lo = float(np.float32(w))
+        nxt = float(np.nextafter(np.float32(lo), np.float32(np.inf if w > lo else -np.inf)))
+        mid = (lo + nxt) / 2
+        if abs(w - mid) <= 2.0 ** -40 * abs(w):
+            continue
+        got, _ = oracle.hadamard_mlp(np.array([[xi]], np.float32), 1, one,
+                                     np.array([gi], np.float32), one, mode="f32")
+        assert got[0, 0] == np.float32(w), (xi, gi)
+        checked += 1
+    assert checked > 500
+
+
+def test_hadamard_mlp_scale_rounding_golden():
+    """needle-2 section 8 with the normalized FWHT of sections 1-2 at D = 2 and
+    D = 8, where 1/sqrt(D) is not a power of two: both transforms scale by the
+    float64 product rounded to float32.  Values derived by hand in the file
+    (silu is the identity there); a float32 scale in either transform changes
+    an output bit pattern."""
+    cases = {}
+    for row in read_golden("hadamard_mlp_scale_rounding.txt"):
+        cases.setdefault(row[0], {})[row[1]] = np.array([parse_float(t) for t in row[2:]],
+                                                        np.float32)
+    for name, c in cases.items():
+        D = c["d1"].size
+        got, _ = oracle.hadamard_mlp(c["x"][None, :], D, c["d1"], c["d2"], c["d3"],
+                                     c["residual"][None, :], c["u"][None, :], mode="f32")
+        assert np.array_equal(got[0].view(np.uint32), c["out"].view(np.uint32)), name
 
 
 @pytest.mark.parametrize("D,n", [(256, 256), (2048, 512)])
