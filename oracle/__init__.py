@@ -14,6 +14,8 @@ Every function cites the page section it follows:
   dot) and "Row gather" (dequantizeRow).
 * ``needle-1`` -- needle.js tutorial "Inference engine, part 1: loader and
   tokenizer": section 3 (FP16 decode) and section 4 (CqMatrix).
+* ``mnemonic`` -- Mnemonic "In the browser", "Dot products and math"
+  (int8 activations quantized per group of 32, exact int32 dot sums).
 * ``ds4f-6`` -- ds4f-disk issue #6 "attention + tokenizer + sampling",
   work item 1 / step 1 (F8 E4M3 + E8M0 block-scaled matvec), step 4 (I8
   matvec with per-16 E8M0 group scales), work item 3 /
@@ -91,6 +93,12 @@ def _load():
     lib.orc_i8_matvec.restype = ctypes.c_int
     lib.orc_i8_matvec_mt.argtypes = [P, I64, I64, P, P, I64, P, P, I64, I64, ctypes.c_int]
     lib.orc_i8_matvec_mt.restype = ctypes.c_int
+    lib.orc_i8_quantize_x.argtypes = [P, I64, I64, P, P]
+    lib.orc_i8_quantize_x.restype = ctypes.c_int
+    lib.orc_i8_matvec_q8.argtypes = [P, I64, I64, P, P, P, I64, P, P, I64, I64]
+    lib.orc_i8_matvec_q8.restype = ctypes.c_int
+    lib.orc_i8_matvec_q8_mt.argtypes = [P, I64, I64, P, P, P, I64, P, P, I64, I64, ctypes.c_int]
+    lib.orc_i8_matvec_q8_mt.restype = ctypes.c_int
     lib.orc_silu_f64.argtypes, lib.orc_silu_f64.restype = [ctypes.c_double], ctypes.c_double
     lib.orc_hadamard_mlp.argtypes = [P, I64, I64, P, P, P, P, P, I64, ctypes.c_int, P, P, P]
     lib.orc_hadamard_mlp.restype = ctypes.c_int
@@ -312,6 +320,49 @@ def i8_matvec(w, scale, x, rows=None, threads: int = 1, with_mag: bool = True):
         lib.orc_i8_matvec_mt(*args, threads)
     else:
         lib.orc_i8_matvec(*args)
+    return y, mag
+
+
+def i8_quantize_x(x):
+    """Activations quantized to int8 per group of 32 columns (Mnemonic "In
+    the browser", "Dot products and math"): d = max|x| / 127 and
+    q = rint(x / d) clamped to [-127, 127], in float32 (see oracle.c).
+
+    ``x`` [batch, C] float32.  Returns (q [batch, C] int8,
+    d [batch, ceil(C/32)] float32)."""
+    x = _c(np.atleast_2d(x), np.float32)
+    batch, C = x.shape
+    q = np.zeros((batch, C), dtype=np.int8)
+    d = np.zeros((batch, (C + 31) // 32), dtype=np.float32)
+    assert _load().orc_i8_quantize_x(_ptr(x), C, batch, _ptr(q), _ptr(d)) == 0
+    return q, d
+
+
+def i8_matvec_q8(w, scale, q, d, rows=None, threads: int = 1, with_mag: bool = True):
+    """int8 weights (per-16 E8M0 group scales, ds4f-6 step 4) times int8
+    activations with per-32 float32 scales (Mnemonic "In the browser"), in
+    float64: y[v, r] = sum_c w[r, c] e8m0(scale[r, c/16]) q[v, c] d[v, c/32].
+
+    ``w`` [R, C] int8, ``scale`` [R, ceil(C/16)] uint8, ``q`` [batch, C] int8,
+    ``d`` [batch, ceil(C/32)] float32.  Returns (y, mag) [batch, R] float64."""
+    w = _c(w, np.int8)
+    scale = _c(scale, np.uint8)
+    q = _c(np.atleast_2d(q), np.int8)
+    d = _c(np.atleast_2d(d), np.float32)
+    R, C = w.shape
+    batch = q.shape[0]
+    assert scale.shape == (R, (C + 15) // 16)
+    assert q.shape == (batch, C) and d.shape == (batch, (C + 31) // 32)
+    r0, r1 = (0, R) if rows is None else rows
+    y = np.zeros((batch, R), dtype=np.float64)
+    mag = np.zeros((batch, R), dtype=np.float64) if with_mag else None
+    args = (_ptr(w), R, C, _ptr(scale), _ptr(q), _ptr(d), batch, _ptr(y),
+            _ptr(mag) if with_mag else None, r0, r1)
+    lib = _load()
+    if threads > 1:
+        lib.orc_i8_matvec_q8_mt(*args, threads)
+    else:
+        lib.orc_i8_matvec_q8(*args)
     return y, mag
 
 

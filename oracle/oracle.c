@@ -309,6 +309,80 @@ ORC_API int orc_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *
 }
 
 /* ------------------------------------------------------------------------ */
+/* I8 matvec over int8 activations quantized per group of 32, Mnemonic "In  */
+/* the browser", "Dot products and math": activations are quantized to int8 */
+/* per group of 32 with one scale per group, the int8 x int8 dot products   */
+/* are exact int32 sums, and only then become floats scaled by the          */
+/* activation group's scale.  The weights are the I8 format above (int8     */
+/* with per-16 E8M0 group scales, ds4f-6 step 4).                           */
+/*                                                                           */
+/* Quantizer (the page gives no rounding; the plainest reading): group j of  */
+/* vector v covers columns [32 j, 32 j + 32) (the last may be shorter);      */
+/* m = max |x| over it, d = m / 127 and q = rint(x / d) clamped to           */
+/* [-127, 127], both divisions in float32 and rint to nearest-even.  d = 0   */
+/* (all zeros, or m so small that m / 127 underflows) gives q = 0; a group   */
+/* holding Inf or NaN gives d = NaN and q = 0, so every output it meets is   */
+/* NaN.  x is [batch, C]; q is [batch, C]; d is [batch, ceil(C / 32)].       */
+/* ------------------------------------------------------------------------ */
+
+ORC_API int orc_i8_quantize_x(const float *x, int64_t C, int64_t batch, int8_t *q, float *d)
+{
+    int64_t ngroups = (C + 31) / 32;
+    for (int64_t v = 0; v < batch; v++)
+        for (int64_t g = 0; g < ngroups; g++) {
+            int64_t c0 = g * 32, c1 = (g * 32 + 32 < C) ? g * 32 + 32 : C;
+            const float *xv = x + v * C;
+            float m = 0.0f;
+            int finite = 1;
+            for (int64_t c = c0; c < c1; c++) {
+                if (!isfinite(xv[c]))
+                    finite = 0;
+                else if (fabsf(xv[c]) > m)
+                    m = fabsf(xv[c]);
+            }
+            float dg = finite ? m / 127.0f : NAN;
+            d[v * ngroups + g] = dg;
+            for (int64_t c = c0; c < c1; c++) {
+                int code = 0;
+                if (finite && dg != 0.0f) {
+                    float t = rintf(xv[c] / dg);
+                    if (t > 127.0f)
+                        t = 127.0f;
+                    if (t < -127.0f)
+                        t = -127.0f;
+                    code = (int)t;
+                }
+                q[v * C + c] = (int8_t)code;
+            }
+        }
+    return 0;
+}
+
+/*   y[v,r] = sum_c w[r,c] * e8m0(scale[r][c/16]) * q[v,c] * d[v][c/32]
+ * in float64 for rows [r0, r1); mag = sum_c |w * s * q * d|. */
+ORC_API int orc_i8_matvec_q8(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                             const int8_t *q, const float *d, int64_t batch, double *y,
+                             double *mag, int64_t r0, int64_t r1)
+{
+    int64_t wgroups = (C + 15) / 16, xgroups = (C + 31) / 32;
+    for (int64_t r = r0; r < r1; r++)
+        for (int64_t v = 0; v < batch; v++) {
+            double sum = 0.0, abs_sum = 0.0;
+            for (int64_t c = 0; c < C; c++) {
+                double term = (double)w[r * C + c] *
+                              (double)orc_e8m0_to_f32(scale[r * wgroups + c / 16]) *
+                              (double)q[v * C + c] * (double)d[v * xgroups + c / 32];
+                sum += term;
+                abs_sum += fabs(term);
+            }
+            y[v * R + r] = sum;
+            if (mag)
+                mag[v * R + r] = abs_sum;
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Hadamard MLP block, [needle-2] section 8, from the padded normalised     */
 /* block input on:                                                            */
 /*   z = pad(x, D); z *= d1; normalizedFwht(z); z = silu(d2 * z);             */
@@ -521,10 +595,12 @@ ORC_API int orc_topk_sample(const float *y, int64_t n, int64_t k, double T, doub
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
-    int kind; /* 0 = cq, 1 = f8, 2 = i8 */
+    int kind; /* 0 = cq, 1 = f8, 2 = i8, 3 = i8 over int8 activations */
     const orc_cq *m;
     const double *prepared;
     const uint8_t *w, *scale;
+    const int8_t *xq;
+    const float *xd;
     int64_t R, C, SR, SC;
     const float *x;
     int64_t batch;
@@ -540,9 +616,12 @@ static void *orc_run_job(void *arg)
     else if (j->kind == 1)
         orc_f8_matvec(j->w, j->R, j->C, j->scale, j->SR, j->SC, j->x, j->batch, j->y, j->mag,
                       j->r0, j->r1);
-    else
+    else if (j->kind == 2)
         orc_i8_matvec((const int8_t *)j->w, j->R, j->C, j->scale, j->x, j->batch, j->y, j->mag,
                       j->r0, j->r1);
+    else
+        orc_i8_matvec_q8((const int8_t *)j->w, j->R, j->C, j->scale, j->xq, j->xd, j->batch,
+                         j->y, j->mag, j->r0, j->r1);
     return NULL;
 }
 
@@ -617,6 +696,25 @@ ORC_API int orc_i8_matvec_mt(const int8_t *w, int64_t R, int64_t C, const uint8_
     j.C = C;
     j.scale = scale;
     j.x = x;
+    j.batch = batch;
+    j.y = y;
+    j.mag = mag;
+    return orc_run_threads(j, r0, r1, nthreads);
+}
+
+ORC_API int orc_i8_matvec_q8_mt(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                                const int8_t *q, const float *d, int64_t batch, double *y,
+                                double *mag, int64_t r0, int64_t r1, int nthreads)
+{
+    orc_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 3;
+    j.w = (const uint8_t *)w;
+    j.R = R;
+    j.C = C;
+    j.scale = scale;
+    j.xq = q;
+    j.xd = d;
     j.batch = batch;
     j.y = y;
     j.mag = mag;
