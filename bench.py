@@ -51,6 +51,26 @@ FALLBACK_HBM_GBS = 6800.0
 # algorithmic bytes
 # --------------------------------------------------------------------------
 
+# The pages' own CPU figures, quoted with their hardware as context only
+# (none is a GPU number, and none measures this metric on this workload).
+PAGES_CPU_CONTEXT = [
+    {"figure": "0.19 s/token", "what": "structural decode of the MoE path only (no attention, "
+     "no head), at the read floor", "hardware": "the 'acer' box (CPU)",
+     "source": "ds4f-disk issue #6, milestone summary"},
+    {"figure": "0.1-0.2 s/token", "what": "projected ~246k x 4096 F8 head (~2 GFLOP/token), "
+     "threaded, resident", "hardware": "the 'acer' box (CPU)",
+     "source": "ds4f-disk issue #6, 'Expected cost on the acer'"},
+    {"figure": "1.5-2 tok/s (0.5-0.8 s/token)", "what": "projected full single-stream decode",
+     "hardware": "the 'acer' box (CPU)", "source": "ds4f-disk issue #6, 'Expected cost on the acer'"},
+    {"figure": "0.29 s/token; head ~0.05 s/token", "what": "measured decode after the SIMD "
+     "I8/F8 matvecs", "hardware": "the 'acer' box (CPU)", "source": "ds4f-disk issue #6, step 4"},
+    {"figure": "4.06 GFLOP/s (scalar 1.32)", "what": "F8 E4M3 + E8M0 matvec, NEON, "
+     "'decode-bound'", "hardware": "Apple M4 (CPU)", "source": "ds4f-disk issue #6, step 4"},
+    {"figure": "27.1 GFLOP/s (scalar 1.94)", "what": "I8 matvec with per-16 E8M0 scales, NEON",
+     "hardware": "Apple M4 (CPU)", "source": "ds4f-disk issue #6, step 4"},
+]
+
+
 def cq_matvec_bytes(out, P, G, bits, batch=1):
     rb = (P * bits + 7) // 8
     return out * rb + out * (P // G) * 2 + (1 << bits) * 4 + batch * P * 4 + batch * out * 4
@@ -224,6 +244,25 @@ def ncu_traffic():
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
+
+def cq_matvec_alone_us(torch, qmv, cq, dev, prepared, logits):
+    """Median microseconds per cq_matvec call (the CQ 2-bit vocabulary
+    projection), L2-cold: a CUDA graph of back-to-back calls, each over its
+    own copy of the packed rows and norms (copies totalling > 2x L2)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per = cq.packed.nbytes + cq.norms.nbytes
+    k = max(2, -(-2 * l2 // per))
+    packed = torch.from_numpy(cq.packed).to(dev).unsqueeze(0).repeat(k, 1, 1)
+    norms = torch.from_numpy(cq.norms.view(np.int16)).to(dev).unsqueeze(0).repeat(k, 1, 1)
+    cb = torch.from_numpy(cq.codebook).to(dev)
+    mats = [qmv.CQMatrix(cq.output, cq.input, cq.input_padded, cq.group, cq.bits, packed[i],
+                         norms[i], cb) for i in range(k)]
+    calls = [(lambda m: lambda sh: qmv.cq_matvec(m.struct, prepared.data_ptr(), 1,
+                                                  logits.data_ptr(), sh))(m) for m in mats]
+    med, _ = _graph_time(torch, calls)
+    del packed, norms, mats
+    return med, k
+
 
 def run_ours(args):
     import torch
@@ -410,6 +449,12 @@ def run_ours(args):
     barrier(d)
     f8_alone_ms = h0.elapsed_time(h1) / nh
 
+    # the CQ vocabulary projection alone: back-to-back cq_matvec calls over
+    # distinct copies of the matrix totalling more than twice the L2 (each
+    # call L2-cold), captured in a CUDA graph and replayed, since at ~us per
+    # call the host's launch rate would otherwise be what is measured
+    cq_alone_us, cq_copies = cq_matvec_alone_us(torch, qmv, cq, dev, prepared, logits)
+
     # end to end through the C-ABI: the same steps with every step's inputs
     # copied from pinned host memory and its three results copied back
     fork_ev = torch.cuda.Event()
@@ -440,6 +485,7 @@ def run_ours(args):
     elapsed_s = max_over_ranks(elapsed_ms / 1e3, d)
     e2e_s = max_over_ranks(e2e_ms / 1e3, d)
     f8_s = max_over_ranks(f8_alone_ms / 1e3, d)
+    cq_s = max_over_ranks(cq_alone_us / 1e6, d)
     cpu = cpu_baseline(cq, f8) if (rank == 0 and world == 1) else None
     if rank != 0:
         if d is not None:
@@ -447,6 +493,7 @@ def run_ours(args):
         return
     peak, peak_kind = measured_hbm_gbs()
     f8_achieved = nbytes["f8_matvec"] / f8_s / 1e9
+    cq_achieved = nbytes["cq_matvec"] / cq_s / 1e9
     value = world * total_bytes * args.steps / elapsed_s / 1e9
     line = {
         "metric": METRIC,
@@ -477,7 +524,18 @@ def run_ours(args):
                      "peak_kind": peak_kind + " copy bandwidth", "unit": "GB/s",
                      "frac": round(f8_achieved / peak, 4), "traffic": ncu_traffic(),
                      "algorithmic_bytes": nbytes["f8_matvec"]},
+        "roofline_cq": {"kernel": "cq_matvec (CQ 2-bit 32768x512, input 500, batch 1)",
+                        "bound": "hbm",
+                        "timing": "CUDA graph of %d back-to-back calls over %d distinct copies "
+                                  "(L2-cold), median of 20 replays" % (cq_copies, cq_copies),
+                        "achieved": round(cq_achieved, 1), "peak": peak,
+                        "peak_kind": peak_kind + " copy bandwidth", "unit": "GB/s",
+                        "frac": round(cq_achieved / peak, 4), "traffic": None,
+                        "us_per_call": round(cq_s * 1e6, 3),
+                        "algorithmic_bytes": nbytes["cq_matvec"]},
         "cpu_baseline": cpu,
+        "context": {"pages_cpu_figures": PAGES_CPU_CONTEXT,
+                    "this_run_head_s_per_token": round(f8_s, 6)},
         "e2e": {"value": round(world * total_bytes * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clock_info,
@@ -815,6 +873,23 @@ def run_configs(args):
                     calls = calls * 8
                 med, best = _graph_time(torch, calls, reps=10)
                 emit(name, batch, "i8_matvec", nb, med, best, k, call=calls[0])
+                # int8 activations with per-32 scales (Mnemonic "In the
+                # browser"): the quantizer, then the int8 x int8 matvec
+                xq, xsc = qmv.i8_quantize_x_t(x)
+                xg = (f.C + 31) // 32
+                qc = [lambda sh: qmv.i8_quantize_x(x.data_ptr(), f.C, batch, xq.data_ptr(),
+                                                   xsc.data_ptr(), sh)] * 64
+                med, best = _graph_time(torch, qc)
+                emit(name, batch, "i8_quantize_x", batch * (5 * f.C + 4 * xg), med, best, 1,
+                     call=qc[0])
+                nbq = f.R * f.C + f.R * ((f.C + 15) // 16) + batch * (f.C + 4 * xg) + 4 * batch * f.R
+                qcalls = [(lambda wi: lambda sh: qmv.i8_matvec_q8(
+                    wi.data_ptr(), f.R, f.C, s8.data_ptr(), xq.data_ptr(), xsc.data_ptr(), batch,
+                    y.data_ptr(), sh))(wi) for wi in ws]
+                if k == 1:
+                    qcalls = qcalls * 8
+                med, best = _graph_time(torch, qcalls, reps=10)
+                emit(name, batch, "i8_matvec_q8", nbq, med, best, k, call=qcalls[0])
                 # the I8 head then top-64 temperature sampling (logits stored)
                 tk = 64
                 wst = torch.empty(qmv.TOPK_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)

@@ -245,6 +245,55 @@ QMV_API qmv_status i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_
                              const float *x, int32_t batch, float *y, qmv_stream stream);
 
 /*
+ * i8_quantize_x -- Mnemonic "In the browser", "Dot products and math": the
+ * activations quantized to int8 per group of 32, with one float scale per
+ * group, once per vector.  For vector v and group j (columns [32 j, 32 j + 32),
+ * the last group shorter when C % 32 != 0):
+ *
+ *   d[v][j] = m / 127,  m = max |x[v][c]| over the group
+ *   q[v][c] = clamp(rint(x[v][c] / d[v][j]), -127, 127)
+ *
+ * Both divisions are IEEE float32 and rint rounds to nearest even (the page
+ * gives no rounding rule; this is the plainest reading), so the codes are
+ * exactly those of any IEEE float32 evaluation.  d = 0 (all zeros, or m / 127
+ * underflows) gives q = 0; a group holding Inf or NaN gives d = NaN, q = 0.
+ *
+ *   x       [batch, C] float32, C >= 1
+ *   xq      [batch, C] int8, written
+ *   xscale  [batch, ceil(C / 32)] float32, written
+ * Errors: QMV_ERR_BATCH, QMV_ERR_SHAPE, QMV_ERR_OVERFLOW, QMV_ERR_NULL,
+ * QMV_ERR_ALIGN (x or xscale not 4-byte aligned), QMV_ERR_ALIAS, QMV_ERR_CUDA.
+ */
+QMV_API qmv_status i8_quantize_x(const float *x, int64_t C, int32_t batch, int8_t *xq,
+                                 float *xscale, qmv_stream stream);
+
+/*
+ * i8_matvec_q8 -- int8 weights times int8 activations, the dot product of
+ * Mnemonic "In the browser", "Dot products and math" (exact int32 sums of
+ * int8 x int8 products, then floats scaled by the activation group's scale)
+ * over the I8 weights of ds4f-disk issue #6, step 4:
+ *
+ *   y[v][r] = sum_c w[r][c] * e8m0(scale[r][c / 16]) * xq[v][c] * xscale[v][c / 32]
+ *
+ * Each 16-column group's int8 x int8 sum is exact in int32; the sum times its
+ * two scales is accumulated in float32, within 1e-4 * sum_c |w * s * q * d|
+ * + 1e-6 of the exact value.  xq and xscale are i8_quantize_x's output (any
+ * int8 codes and float scales are accepted).
+ *
+ *   w       [R, C] int8, R >= 0, C >= 1
+ *   scale   [R, ceil(C / 16)] E8M0 bytes (code 255 is NaN)
+ *   xq      [batch, C] int8
+ *   xscale  [batch, ceil(C / 32)] float32
+ *   y       [batch, R] float32, written; must not overlap any input
+ * Errors: QMV_ERR_BATCH, QMV_ERR_SHAPE, QMV_ERR_OVERFLOW, QMV_ERR_NULL,
+ * QMV_ERR_ALIGN (xscale or y not 4-byte aligned), QMV_ERR_ALIAS,
+ * QMV_ERR_CUDA.
+ */
+QMV_API qmv_status i8_matvec_q8(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                                const int8_t *xq, const float *xscale, int32_t batch, float *y,
+                                qmv_stream stream);
+
+/*
  * hadamard_mlp -- the Hadamard MLP block of "part 2", section 8, from the
  * normalised block input on.  For each of `batch` vectors:
  *
@@ -329,8 +378,10 @@ QMV_API qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, cons
  * workspace: the scratch is a fixed 256 KiB array inside the library (one
  * per GPU, held until the process exits), enough for batch <= QMV_MAX_BATCH;
  * anything beyond that returns QMV_ERR_BATCH.  The call allocates nothing.
- * Its first call on each device looks up that array's device address (with
- * the device current), so make that first call before any stream capture.
+ * Its first call in each CUDA context (per device, and again after
+ * cudaDeviceReset or any other teardown of the device's context) looks up
+ * that array's device address with the device current, so make that first
+ * call before any stream capture.
  * Every call uses the same array: calls that may run at the same time on the
  * GPU (for example on two streams) race and must be ordered by the caller.
  * The array's previous contents never matter.

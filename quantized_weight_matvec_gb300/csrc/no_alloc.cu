@@ -15,6 +15,8 @@
 // address, so the device address is looked up once per device with
 // cudaGetSymbolAddress (while that device is current) and passed to the
 // kernels like any other workspace pointer.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "qmv_internal.h"
@@ -27,24 +29,63 @@ constexpr size_t kScratchBytes = size_t(QMV_ARGMAX_MAX_BLOCKS) * QMV_MAX_BATCH *
 
 static __device__ __align__(256) unsigned char g_argmax_scratch[kScratchBytes];
 
-// Device address of g_argmax_scratch on each device, looked up on the first
-// call made while that device is current.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Unique id of the calling thread's current CUDA context (the device's
+// primary context under the runtime), or 0 when the driver cannot say.  A
+// context that is destroyed and created again (cudaDeviceReset, a primary
+// context reset) gets a new id, so an address cached under the old id is
+// never reused.  The driver functions are fetched through the runtime, so the
+// library needs no link against the driver library.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(fn);
+        (void)cudaGetLastError();
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_argmax_scratch in the current context.  It is looked
+// up with cudaGetSymbolAddress on the first call made in each context (with
+// the device current; the lookup initialises the device's primary context if
+// nothing has yet) and cached under the context's id; while the id cannot be
+// read (no context yet, or an old driver) it is looked up on every call.
 void *scratch_address(qmv_status *status) {
     static std::mutex mu;
     static void *addr[64] = {nullptr};
+    static unsigned long long ctx_of[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
         *status = QMV_ERR_CUDA;
         return nullptr;
     }
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || id == 0 || ctx_of[dev] != id) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_argmax_scratch) != cudaSuccess || !p) {
             *status = QMV_ERR_CUDA;
             return nullptr;
         }
         addr[dev] = p;
+        ctx_of[dev] = id;
     }
     *status = QMV_OK;
     return addr[dev];

@@ -396,6 +396,42 @@ qmv_status i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale
     return qmv::launch_i8_matvec(w, R, C, scale, x, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
+qmv_status i8_quantize_x(const float *x, int64_t C, int32_t batch, int8_t *xq, float *xscale,
+                         qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (C < 1 || C > kMaxDim) return QMV_ERR_SHAPE;
+    int64_t xb = 0, qb = 0, db = 0;
+    if (!mul_ok(int64_t(batch) * 4, C, &xb) || !mul_ok(int64_t(batch), C, &qb) ||
+        !mul_ok(int64_t(batch) * 4, (C + 31) / 32, &db))
+        return QMV_ERR_OVERFLOW;
+    if (!x || !xq || !xscale) return QMV_ERR_NULL;
+    if (!aligned(x, 4) || !aligned(xscale, 4)) return QMV_ERR_ALIGN;
+    if (overlaps(xq, qb, x, xb) || overlaps(xscale, db, x, xb) || overlaps(xq, qb, xscale, db))
+        return QMV_ERR_ALIAS;
+    return qmv::launch_i8_quantize_x(x, C, batch, xq, xscale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qmv_status i8_matvec_q8(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale, const int8_t *xq,
+                        const float *xscale, int32_t batch, float *y, qmv_stream stream) {
+    qmv_status st = check_batch(batch);
+    if (st != QMV_OK) return st;
+    if (R < 0 || R > kMaxDim || C < 1 || C > kMaxDim) return QMV_ERR_SHAPE;
+    int64_t wb = 0, sb = 0, qb = 0, db = 0, yb = 0;
+    if (!mul_ok(R, C, &wb) || !mul_ok(R, (C + 15) / 16, &sb) || !mul_ok(int64_t(batch), C, &qb) ||
+        !mul_ok(int64_t(batch) * 4, (C + 31) / 32, &db) || !mul_ok(int64_t(batch) * 4, R, &yb))
+        return QMV_ERR_OVERFLOW;
+    if (!xq || !xscale) return QMV_ERR_NULL;
+    if (R > 0 && (!w || !scale || !y)) return QMV_ERR_NULL;
+    if (!aligned(xscale, 4) || !aligned(y, 4)) return QMV_ERR_ALIGN;
+    if (overlaps(y, yb, w, wb) || overlaps(y, yb, scale, sb) || overlaps(y, yb, xq, qb) ||
+        overlaps(y, yb, xscale, db))
+        return QMV_ERR_ALIAS;
+    if (R == 0) return QMV_OK;
+    return qmv::launch_i8_matvec_q8(w, R, C, scale, xq, xscale, batch, y,
+                                    reinterpret_cast<cudaStream_t>(stream));
+}
+
 qmv_status hadamard_mlp(const float *x, int64_t n, int64_t D, const float *d1, const float *d2,
                         const float *d3, const float *residual, const float *u, int32_t batch,
                         float *out, qmv_stream stream) {

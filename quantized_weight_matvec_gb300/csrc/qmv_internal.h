@@ -80,6 +80,13 @@ bool cq_fused_fits(const qmv_cq_matrix &m, int batch);
 qmv_status launch_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                             const float *x, int batch, float *y, cudaStream_t s);
 
+// ---- I8 over int8 activations (i8q_kernels.cu) --------------------------------
+qmv_status launch_i8_quantize_x(const float *x, int64_t C, int batch, int8_t *xq, float *xd,
+                                cudaStream_t s);
+qmv_status launch_i8_matvec_q8(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                               const int8_t *xq, const float *xd, int batch, float *y,
+                               cudaStream_t s);
+
 // ---- Hadamard MLP ----------------------------------------------------------
 qmv_status launch_hadamard_mlp(const float *x, int64_t n, int D, const float *d1, const float *d2,
                                const float *d3, const float *residual, const float *u, int batch,

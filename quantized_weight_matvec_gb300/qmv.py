@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
     lib.cq_prepare_matvec.argtypes = [CQP, I32, P, I32, P, P, P]
     lib.f8_matvec.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P]
     lib.i8_matvec.argtypes = [P, I64, I64, P, P, I32, P, P]
+    lib.i8_quantize_x.argtypes = [P, I64, I32, P, P, P]
+    lib.i8_matvec_q8.argtypes = [P, I64, I64, P, P, P, I32, P, P]
     lib.f8_matvec_argmax.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P, I64, P]
     lib.f8_matvec_argmax_noalloc.argtypes = [P, I64, I64, P, I64, I64, P, I32, P, P, P, P]
     lib.hadamard_mlp.argtypes = [P, I64, I64, P, P, P, P, P, I32, P, P]
@@ -91,7 +93,8 @@ def load() -> ctypes.CDLL:
     for fn in (lib.cq_prepare, lib.cq_matvec, lib.cq_dequantize_row, lib.cq_matvec_multi,
                lib.cq_prepare_matvec, lib.f8_matvec, lib.i8_matvec, lib.f8_matvec_argmax,
                lib.f8_matvec_argmax_noalloc, lib.hadamard_mlp, lib.topk_sample,
-               lib.f8_matvec_topk_sample, lib.i8_matvec_topk_sample):
+               lib.f8_matvec_topk_sample, lib.i8_matvec_topk_sample, lib.i8_quantize_x,
+               lib.i8_matvec_q8):
         fn.restype = ctypes.c_int
     lib.qmv_status_string.argtypes = [ctypes.c_int]
     lib.qmv_status_string.restype = ctypes.c_char_p
@@ -163,6 +166,16 @@ def i8_matvec(w: int, R: int, C: int, scale: int, x: int, batch: int, y: int,
               stream: int = 0) -> int:
     return load().i8_matvec(w or None, R, C, scale or None, x or None, batch, y or None,
                             stream or None)
+
+
+def i8_quantize_x(x: int, C: int, batch: int, xq: int, xscale: int, stream: int = 0) -> int:
+    return load().i8_quantize_x(x or None, C, batch, xq or None, xscale or None, stream or None)
+
+
+def i8_matvec_q8(w: int, R: int, C: int, scale: int, xq: int, xscale: int, batch: int, y: int,
+                 stream: int = 0) -> int:
+    return load().i8_matvec_q8(w or None, R, C, scale or None, xq or None, xscale or None, batch,
+                               y or None, stream or None)
 
 
 def hadamard_mlp(x: int, n: int, D: int, d1: int, d2: int, d3: int, residual: int, u: int,
@@ -403,6 +416,47 @@ def i8_matvec_t(w, scale, x, out=None, stream=None):
     _dev(out, torch.float32, "out")
     _check(i8_matvec(w.data_ptr(), R, C, scale.data_ptr(), x.data_ptr(), batch, out.data_ptr(),
                      _stream(stream)), "i8_matvec")
+    return out
+
+
+def i8_quantize_x_t(x, xq=None, xscale=None, stream=None):
+    """(xq [B, C] int8, xscale [B, ceil(C/32)] float32) = i8_quantize_x(x [B, C])."""
+    torch = _torch()
+    x = _dev(x, torch.float32, "x")
+    batch = x.shape[0] if x.dim() == 2 else 1
+    C = x.shape[-1]
+    if xq is None:
+        xq = torch.empty((batch, C), dtype=torch.int8, device=x.device)
+    if xscale is None:
+        xscale = torch.empty((batch, (C + 31) // 32), dtype=torch.float32, device=x.device)
+    _dev(xq, torch.int8, "xq")
+    _dev(xscale, torch.float32, "xscale")
+    if xq.numel() != batch * C or xscale.numel() != batch * ((C + 31) // 32):
+        raise ValueError("xq must be [B, C] and xscale [B, ceil(C/32)]")
+    _check(i8_quantize_x(x.data_ptr(), C, batch, xq.data_ptr(), xscale.data_ptr(),
+                         _stream(stream)), "i8_quantize_x")
+    return xq, xscale
+
+
+def i8_matvec_q8_t(w, scale, xq, xscale, out=None, stream=None):
+    """y[B, R] = i8_matvec_q8(w[R, C] int8, scale[R, ceil(C/16)] uint8,
+    xq[B, C] int8, xscale[B, ceil(C/32)] float32)."""
+    torch = _torch()
+    w = _dev(w, torch.int8, "w")
+    scale = _dev(scale, torch.uint8, "scale")
+    xq = _dev(xq, torch.int8, "xq")
+    xscale = _dev(xscale, torch.float32, "xscale")
+    R, C = w.shape
+    batch = xq.shape[0] if xq.dim() == 2 else 1
+    if tuple(scale.shape) != (R, (C + 15) // 16):
+        raise ValueError("scale must be [R, ceil(C/16)]")
+    if xq.numel() != batch * C or xscale.numel() != batch * ((C + 31) // 32):
+        raise ValueError("xq must be [B, C] and xscale [B, ceil(C/32)]")
+    if out is None:
+        out = torch.empty((batch, R), dtype=torch.float32, device=w.device)
+    _dev(out, torch.float32, "out")
+    _check(i8_matvec_q8(w.data_ptr(), R, C, scale.data_ptr(), xq.data_ptr(), xscale.data_ptr(),
+                        batch, out.data_ptr(), _stream(stream)), "i8_matvec_q8")
     return out
 
 

@@ -30,7 +30,7 @@ def test_header_declares_every_entry_point():
     for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec", "f8_matvec_argmax",
               "cq_matvec_multi", "cq_prepare_matvec", "i8_matvec", "hadamard_mlp",
               "topk_sample", "f8_matvec_topk_sample", "i8_matvec_topk_sample",
-              "qmv_status_string", "qmv_abi_version"):
+              "i8_quantize_x", "i8_matvec_q8", "qmv_status_string", "qmv_abi_version"):
         assert n in names
 
 
@@ -211,6 +211,43 @@ def test_i8_rejections():
     assert f(W, 16, 16, S, X, 1, W + 8) == 8
     assert f(W, 16, 16, S, X, 1, S) == 8
     assert f(W, 0, 16, S, X, 1, 0) == 0
+
+
+def test_i8_quantize_x_rejections():
+    X, Q, D = FAKE, FAKE + (1 << 30), FAKE + (1 << 31)
+    f = qmv.i8_quantize_x
+    assert f(X, 64, 0, Q, D) == 5                  # batch
+    assert f(X, 64, 9, Q, D) == 5
+    assert f(X, 0, 1, Q, D) == 2                   # C
+    assert f(0, 64, 1, Q, D) == 1                  # NULL
+    assert f(X, 64, 1, 0, D) == 1
+    assert f(X, 64, 1, Q, 0) == 1
+    assert f(X + 2, 64, 1, Q, D) == 6              # alignment
+    assert f(X, 64, 1, Q, D + 2) == 6
+    assert f(X, 64, 2, X + 256, D) == 8            # codes overlap x
+    assert f(X, 64, 1, Q, X + 252) == 8            # scales overlap x
+    assert f(X, 64, 1, Q, Q + 60) == 8             # scales overlap codes
+
+
+def test_i8_matvec_q8_rejections():
+    W, S, Q, D, Y = FAKE, FAKE + (1 << 30), FAKE + (1 << 31), FAKE + (3 << 30), FAKE + (1 << 32)
+    f = qmv.i8_matvec_q8
+    assert f(W, 16, 64, S, Q, D, 0, Y) == 5        # batch
+    assert f(W, 16, 64, S, Q, D, 9, Y) == 5
+    assert f(W, 16, 0, S, Q, D, 1, Y) == 2         # shapes
+    assert f(W, -1, 64, S, Q, D, 1, Y) == 2
+    assert f(0, 16, 64, S, Q, D, 1, Y) == 1        # NULL
+    assert f(W, 16, 64, 0, Q, D, 1, Y) == 1
+    assert f(W, 16, 64, S, 0, D, 1, Y) == 1
+    assert f(W, 16, 64, S, Q, 0, 1, Y) == 1
+    assert f(W, 16, 64, S, Q, D, 1, 0) == 1
+    assert f(W, 16, 64, S, Q, D + 2, 1, Y) == 6    # alignment
+    assert f(W, 16, 64, S, Q, D, 1, Y + 2) == 6
+    assert f(W, 16, 64, S, Q, D, 1, W + 64) == 8   # y overlaps w
+    assert f(W, 16, 64, S, Q, D, 1, S) == 8        # y overlaps scale
+    assert f(W, 16, 64, S, Q, D, 1, Q + 32) == 8   # y overlaps codes
+    assert f(W, 16, 64, S, Q, D, 1, D) == 8        # y overlaps activation scales
+    assert f(W, 0, 64, S, Q, D, 1, 0) == 0         # no rows: nothing to do
 
 
 def test_hadamard_mlp_rejections():

@@ -8,6 +8,8 @@ Bars (from the method's definitions on the pages):
   sum of the terms the method adds (sum_g |norm| sum_k |level * p| for CQ,
   sum_c |w * s * x| for F8).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -294,17 +296,62 @@ def head():
     return f, dev(f.w), dev(f.scale)
 
 
+@pytest.fixture(scope="module")
+def head_ref(head):
+    """The oracle over every row of the head for all 8 vectors (threaded on
+    the host cores); vectors are independent, so ref[:b] serves batch b."""
+    f, _, _ = head
+    return oracle.f8_matvec(f.w, f.scale, f.x, threads=os.cpu_count() or 8)
+
+
 @pytest.mark.parametrize("batch", [1, 2, 4, 8])
-def test_f8_head_full_size_sampled_rows(head, batch):
+def test_f8_head_full_size_every_row(head, head_ref, batch):
+    """All 245760 rows of the 245760 x 4096 head (ds4f-disk issue #6, work
+    item 3) against the oracle, at each batch the head runs: batch 1 on the
+    streaming kernel, 2-8 on the tensor-core kernel."""
     f, w_dev, s_dev = head
-    x = f.x[:batch]
-    y = host(qmv.f8_matvec_t(w_dev, s_dev, dev(x)))
-    rng = np.random.default_rng(batch)
-    sample = np.unique(np.concatenate([rng.integers(0, f.R, 300), np.arange(8),
-                                       np.arange(f.R - 8, f.R), np.arange(120, 136)]))
-    for r in sample:
-        ref, mag = oracle.f8_matvec(f.w, f.scale, x, rows=(int(r), int(r) + 1))
-        assert_close(y[:, r], ref[:, r], mag[:, r])
+    y = host(qmv.f8_matvec_t(w_dev, s_dev, dev(f.x[:batch])))
+    ref, mag = head_ref
+    assert_close(y, ref[:batch], mag[:batch])
+
+
+@pytest.mark.parametrize("batch", [1, 8])
+def test_f8_head_argmax_full_size_every_row(head, head_ref, batch):
+    """The fused greedy head at full size: its y is f8_matvec's bit for bit
+    and within tolerance of the oracle on every row; the index is the greedy
+    choice over that y and the value is y at that row."""
+    f, w_dev, s_dev = head
+    x = dev(f.x[:batch])
+    y_buf = torch.empty((batch, f.R), dtype=torch.float32, device="cuda")
+    idx, val = qmv.f8_matvec_argmax_t(w_dev, s_dev, x, y=y_buf)
+    y_plain = qmv.f8_matvec_t(w_dev, s_dev, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y_buf.view(torch.int32), y_plain.view(torch.int32))
+    y = host(y_buf)
+    ref, mag = head_ref
+    assert_close(y, ref[:batch], mag[:batch])
+    idx = idx.cpu().numpy()
+    assert np.array_equal(idx, oracle.argmax_rows(y))
+    assert bits_equal(val.cpu().numpy(), y[np.arange(batch), idx])
+
+
+@pytest.mark.parametrize("batch", [1, 8])
+def test_f8_head_topk_full_size_every_row(head, head_ref, batch):
+    """The fused top-64 sampling head at full size: y within tolerance of the
+    oracle on every row, and the 64 rows and their order equal to the
+    oracle's selection over that y (probabilities and the draw are checked
+    in the top-k tests)."""
+    f, w_dev, s_dev = head
+    u = np.random.default_rng(batch + 40).random(batch).astype(np.float32)
+    y, idx, val, _, _ = qmv.f8_matvec_topk_sample_t(w_dev, s_dev, dev(f.x[:batch]), 64, 1.0,
+                                                     dev(u))
+    y = host(y)
+    ref, mag = head_ref
+    assert_close(y, ref[:batch], mag[:batch])
+    ref_idx, _, _ = oracle.topk_sample(y, 64, 1.0, u)
+    idx = idx.cpu().numpy()
+    assert np.array_equal(idx, ref_idx)
+    assert bits_equal(val.cpu().numpy(), np.take_along_axis(y, idx, 1))
 
 
 def test_f8_deterministic_guarded_and_on_a_side_stream():
