@@ -32,6 +32,14 @@
  *     pick its vectorised kernels; other layouts take a general kernel
  *     with the same results.
  *   - Errors of the CUDA runtime at launch are reported as QMV_ERR_CUDA.
+ *   - Calls may start on the GPU before the kernel queued just ahead of them
+ *     on the same stream has finished (programmatic dependent launch).
+ *     Activations are read and outputs written only once everything ahead
+ *     in the stream has completed.  Weight matrices are treated as
+ *     read-only model weights and may be read earlier: write a matrix with
+ *     a copy, or with a kernel followed by a stream or event
+ *     synchronisation, before its first use -- never with a kernel still
+ *     queued ahead of the call on the same stream.
  */
 #ifndef QMV_H
 #define QMV_H

@@ -370,20 +370,33 @@ __global__ void __launch_bounds__(256) cq_matvec_general_kernel(CqSet c) {
 // page's 2-bit loop looks up four levels per byte (section 3); here each
 // table entry already holds the two products of one nibble:
 //   T[nib][c2] = codebook[nib & 3] * p[2*c2] + codebook[nib >> 2] * p[2*c2+1]
-// so every 4-bit code pair costs one shared-memory load and one add.
+// so every 4-bit code pair costs one shared-memory load and half a packed
+// add (add.f32x2 sums two lookups at once).
 //
-// Layout.  A row of P columns is CPR = P/64 chunks of 16 bytes (64 codes).
+// Lanes.  A row of P columns is CPR = P/64 chunks of 16 bytes (64 codes).
 // Lane l of a warp owns chunk q = l % CPR of row rho = l / CPR (RPW = 32/CPR
-// rows per warp) and walks its 32 nibbles in the order rho, rho+1, ...
-// (its 16 bytes rotated right by 4*rho bits).  Chunk q's entries are stored
-// with a bank skew of RPW*q and twice (slots s and s+32), so at step t lane
-// (rho, q) reads slot t + rho + RPW*q: the 32 lanes of a warp always hit 32
-// distinct banks and the address is a per-lane constant plus 4*t.
+// rows per warp, one "unit") and walks its 32 nibbles in the order rho,
+// rho+1, ... (its 16 bytes rotated right by 4*rho bits).
 //
-// Shared memory: 16 nibbles x CPR chunks x 64 slots x 4 B = 64*P bytes (plus
-// 4*P for the prepared vector when FUSED).  Requirements (checked by the
-// launcher): bits == 2, batch == 1, P in {256, 512, 1024, 2048}, group >= 64,
-// 16-byte aligned packed rows.  Units are row groups of RPW rows per matrix.
+// Table layout (bytes): page q at 4096 q, nibble row nib at 256 nib inside
+// it, slot s (0..63) at 4 s; chunk q's column pair j is stored at slots
+// (j + RPW q) % 32 and that + 32.  At step t lane (rho, q) reads slot
+// t + rho + RPW q, so the 32 lanes of a warp always hit 32 distinct banks,
+// and its address is one byte permute of the nibble (byte 1, with q's low
+// bits pre-set in the high half of the byte) and a per-lane word (slot base
+// in byte 0, q's high bit in byte 2), plus the immediate 4 t.
+//
+// Work split.  One block of 512 threads per SM (kCq2Threads, <= 64
+// registers), so a second call's block fits beside it; the units are split
+// evenly over the blocks and, inside a block, warp w takes units w, w + 16,
+// ....  The first kCq2Pre units of every warp are loaded into registers
+// before the dependency wait -- while the preceding call is still running --
+// and the block lets its dependents launch at once.  After the wait: the
+// prepared vector and codebook, the table build, the lookups.
+//
+// Shared memory: 64*P bytes (4 KB per chunk) plus 4*P for the prepared vector
+// when FUSED.  Requirements (checked by the launcher): bits == 2, batch == 1,
+// P in {256, 512, 1024, 2048}, group >= 64, 16-byte aligned packed rows.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void cq2_load(uint4 &d, float &n, const CqSet &c, int mi, int64_t r, int q, int g) {
@@ -398,36 +411,46 @@ __device__ __forceinline__ void cq2_load(uint4 &d, float &n, const CqSet &c, int
     }
 }
 
+constexpr int kCq2Threads = 512;
+constexpr int kCq2Warps = kCq2Threads / 32;
+constexpr int kCq2Pre = 4;  // units per warp loaded before the dependency wait
+
 template <int CPR, bool FUSED>
-__global__ void __launch_bounds__(1024, 1) cq2_table_kernel(CqSet c) {
+__global__ void __launch_bounds__(kCq2Threads, FUSED ? 1 : 2) cq2_table_kernel(CqSet c, int64_t upb) {
     constexpr int RPW = 32 / CPR;
     constexpr int P = CPR * 64;
-    constexpr int NIB_STRIDE = 4 * P;  // bytes per nibble block
     extern __shared__ __align__(16) unsigned char table_raw[];
     float *table = reinterpret_cast<float *>(table_raw);
     float *sp = reinterpret_cast<float *>(table_raw + 64 * P);  // FUSED: prepared vector
 
-    pdl_wait();
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int rho = lane / CPR, q = lane % CPR;
     const int g = (q * 64) / int(c.G);
     const int64_t nunits = c.first[c.nmats];
-    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
-    int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t ub0 = int64_t(blockIdx.x) * upb;
+    const int64_t ub1 = min(nunits, ub0 + upb);
 
-    // the loads of this warp's first two units go out before the table is
-    // built (most warps of a launch have one or two units: their weights then
-    // cost one DRAM round trip, not two)
-    int mi = set_matrix(c, u, 0);
-    uint4 d = make_uint4(0, 0, 0, 0), dn = make_uint4(0, 0, 0, 0);
-    float n = 0.0f, nn = 0.0f;
-    if (u < nunits) cq2_load(d, n, c, mi, (u - c.first[mi]) * RPW + rho, q, g);
-    int mn = mi;
-    if (u + nwarps < nunits) {
-        mn = set_matrix(c, u + nwarps, mi);
-        cq2_load(dn, nn, c, mn, (u + nwarps - c.first[mn]) * RPW + rho, q, g);
+    // this warp's first units, into registers while the preceding call runs
+    uint4 d[kCq2Pre];
+    float n[kCq2Pre];
+    int mis[kCq2Pre];
+    {
+        int mi = set_matrix(c, ub0, 0);
+#pragma unroll
+        for (int k = 0; k < kCq2Pre; k++) {
+            const int64_t u = ub0 + warp + int64_t(k) * kCq2Warps;
+            d[k] = make_uint4(0, 0, 0, 0);
+            n[k] = 0.0f;
+            mis[k] = mi;
+            if (u < ub1) {
+                mi = set_matrix(c, u, mi);
+                mis[k] = mi;
+                cq2_load(d[k], n[k], c, mi, (u - c.first[mi]) * RPW + rho, q, g);
+            }
+        }
     }
+    pdl_wait();
 
     const float *pv = c.p;
     if (FUSED) {
@@ -435,28 +458,32 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(CqSet c) {
         __syncthreads();
         pv = sp;
     }
-    // ---- build the table (one pass per block): one thread per column pair
-    // (chunk q, pair j) loads p once and writes all 16 nibble entries ----
+    // ---- build the table: a job is one column pair and half of its 16
+    // entries; consecutive lanes take consecutive pairs, so every store of a
+    // warp hits 32 distinct banks ----
     {
         float cbv[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) cbv[i] = __ldg(c.codebook + i);
-        for (int uu = threadIdx.x; uu < CPR * 32; uu += blockDim.x) {
-            const int qq = uu >> 5, j = uu & 31;
+        constexpr int NPAIR = CPR * 32;
+        for (int job = threadIdx.x; job < 2 * NPAIR; job += blockDim.x) {
+            const int pair = job % NPAIR, half = job / NPAIR;
+            const int qq = pair >> 5, j = pair & 31;
             const int col = qq * 64 + 2 * j;
             const float p0 = FUSED ? pv[col] : __ldg(pv + col);
             const float p1 = FUSED ? pv[col + 1] : __ldg(pv + col + 1);
             float lo_prod[4];
 #pragma unroll
             for (int i = 0; i < 4; i++) lo_prod[i] = cbv[i] * p0;
-            const int slot = (j + RPW * qq) & 31;
-            float *blk = table + (qq * 256) / 4 + slot;
+            float *blk = table + qq * 1024 + ((j + RPW * qq) & 31);
 #pragma unroll
-            for (int hi = 0; hi < 4; hi++) {
+            for (int h = 0; h < 2; h++) {
+                const int hi = 2 * half + h;
+                const float chi = half ? cbv[2 + h] : cbv[h];
 #pragma unroll
                 for (int lo = 0; lo < 4; lo++) {
-                    const float v = fmaf(cbv[hi], p1, lo_prod[lo]);
-                    float *e = blk + (lo | (hi << 2)) * (NIB_STRIDE / 4);
+                    const float v = fmaf(chi, p1, lo_prod[lo]);
+                    float *e = blk + (lo | (hi << 2)) * 64;
                     e[0] = v;
                     e[32] = v;
                 }
@@ -465,59 +492,64 @@ __global__ void __launch_bounds__(1024, 1) cq2_table_kernel(CqSet c) {
     }
     __syncthreads();
 
-    // per-lane part of every table address (shared-window base included)
-    const unsigned lane_base = unsigned(__cvta_generic_to_shared(table_raw)) +
-                               unsigned(q * 256 + 4 * (rho + RPW * q));
+    const unsigned q4 = (unsigned(q & 15) << 4) * 0x01010101u;
+    const unsigned lane_word = unsigned(4 * (rho + RPW * q)) | (unsigned(q >> 4) << 16);
+    const char *tb = reinterpret_cast<const char *>(table);
     const unsigned sh = 4u * unsigned(rho);
-
-    for (; u < nunits; u += nwarps) {
-        const int64_t r = (u - c.first[mi]) * RPW + rho;
-        const int64_t out = c.output[mi];
-        float *y = c.y[mi];
-        // the unit after next: its loads before this unit's lookups
-        uint4 dnn = make_uint4(0, 0, 0, 0);
-        float nnn = 0.0f;
-        const int64_t unn = u + 2 * nwarps;
-        int mnn = mn;
-        if (unn < nunits) {
-            mnn = set_matrix(c, unn, mn);
-            cq2_load(dnn, nnn, c, mnn, (unn - c.first[mnn]) * RPW + rho, q, g);
-        }
-        // rotate the 128-bit chunk right by 4*rho bits, then split every word
-        // into its even nibbles (one per byte) and its odd nibbles
+    auto unit = [&](const uint4 &dd, float nv, int mi, int64_t u) {
+        // rotate the 128-bit chunk right by 4*rho bits; every word then gives
+        // its even nibbles (one per byte) and its odd nibbles
         unsigned w[4];
-        w[0] = __funnelshift_r(d.x, d.y, sh);
-        w[1] = __funnelshift_r(d.y, d.z, sh);
-        w[2] = __funnelshift_r(d.z, d.w, sh);
-        w[3] = __funnelshift_r(d.w, d.x, sh);
-        float part0 = 0.0f, part1 = 0.0f;
+        w[0] = __funnelshift_r(dd.x, dd.y, sh);
+        w[1] = __funnelshift_r(dd.y, dd.z, sh);
+        w[2] = __funnelshift_r(dd.z, dd.w, sh);
+        w[3] = __funnelshift_r(dd.w, dd.x, sh);
+        float2 s2 = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            const unsigned ev = w[i] & 0x0f0f0f0fu, od = (w[i] >> 4) & 0x0f0f0f0fu;
+            const unsigned ev = (w[i] & 0x0f0f0f0fu) | q4, od = ((w[i] >> 4) & 0x0f0f0f0fu) | q4;
 #pragma unroll
-            for (int k = 0; k < 8; k++) {
-                const int t = 8 * i + k;
-                const unsigned nib = __byte_perm((k & 1) ? od : ev, 0u, 0x4440u | unsigned(k >> 1));
-                const unsigned addr = nib * unsigned(NIB_STRIDE) + lane_base + 4u * unsigned(t);
-                float tv;
-                asm("ld.shared.f32 %0, [%1];" : "=f"(tv) : "r"(addr));
-                if (k & 1)
-                    part1 += tv;
-                else
-                    part0 += tv;
+            for (int kk = 0; kk < 4; kk++) {
+                const int t = 8 * i + 2 * kk;
+                const unsigned ae = __byte_perm(ev, lane_word, 0x7604u | (unsigned(kk) << 4));
+                const unsigned ao = __byte_perm(od, lane_word, 0x7604u | (unsigned(kk) << 4));
+                const float te = *reinterpret_cast<const float *>(tb + ae + 4 * t);
+                const float to = *reinterpret_cast<const float *>(tb + ao + 4 * (t + 1));
+                s2 = __fadd2_rn(s2, make_float2(te, to));
             }
         }
-        const float part = part0 + part1;
-        float acc = n * part;
+        float acc = nv * (s2.x + s2.y);
 #pragma unroll
-        for (int dd = CPR / 2; dd >= 1; dd >>= 1) acc += __shfl_xor_sync(kFull, acc, dd);
-        if (q == 0 && r < out) y[r] = acc;
-        d = dn;
-        n = nn;
-        mi = mn;
-        dn = dnn;
-        nn = nnn;
-        mn = mnn;
+        for (int dd2 = CPR / 2; dd2 >= 1; dd2 >>= 1) acc += __shfl_xor_sync(kFull, acc, dd2);
+        const int64_t r = (u - c.first[mi]) * RPW + rho;
+        if (q == 0 && r < c.output[mi]) c.y[mi][r] = acc;
+    };
+#pragma unroll
+    for (int k = 0; k < kCq2Pre; k++) {
+        const int64_t u = ub0 + warp + int64_t(k) * kCq2Warps;
+        if (u < ub1) unit(d[k], n[k], mis[k], u);  // warp-uniform
+    }
+    // larger matrices: the remaining units, kCq2Pre at a time
+    for (int64_t base = ub0 + warp + int64_t(kCq2Pre) * kCq2Warps; base < ub1;
+         base += int64_t(kCq2Pre) * kCq2Warps) {
+        int mi = mis[kCq2Pre - 1];
+#pragma unroll
+        for (int k = 0; k < kCq2Pre; k++) {
+            const int64_t u = base + int64_t(k) * kCq2Warps;
+            d[k] = make_uint4(0, 0, 0, 0);
+            n[k] = 0.0f;
+            mis[k] = mi;
+            if (u < ub1) {
+                mi = set_matrix(c, u, mi);
+                mis[k] = mi;
+                cq2_load(d[k], n[k], c, mi, (u - c.first[mi]) * RPW + rho, q, g);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kCq2Pre; k++) {
+            const int64_t u = base + int64_t(k) * kCq2Warps;
+            if (u < ub1) unit(d[k], n[k], mis[k], u);
+        }
     }
 }
 
@@ -529,10 +561,14 @@ qmv_status launch_cq2_table(CqSet c, cudaStream_t s) {
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
     c.first[0] = 0;
     for (int i = 0; i < c.nmats; i++) c.first[i + 1] = c.first[i] + (c.output[i] + RPW - 1) / RPW;
-    int64_t blocks = (c.first[c.nmats] + 31) / 32;  // 32 warps per block
+    const int64_t nunits = c.first[c.nmats];
+    // one block per SM at most (leaving room for the next call's block), and
+    // no more blocks than a warp's worth of units each
+    int64_t blocks = (nunits + kCq2Warps - 1) / kCq2Warps;
     if (blocks > sm_count()) blocks = sm_count();
     if (blocks < 1) blocks = 1;
-    return from_cuda(launch_pdl(cq2_table_kernel<CPR, FUSED>, dim3(unsigned(blocks)), dim3(1024), smem, s, c));
+    const int64_t upb = (nunits + blocks - 1) / blocks;
+    return from_cuda(launch_pdl(cq2_table_kernel<CPR, FUSED>, dim3(unsigned(blocks)), dim3(kCq2Threads), smem, s, c, upb));
 }
 
 template <int B, bool FUSED>

@@ -32,13 +32,18 @@ inline int grid_blocks(const void *kernel, int threads, size_t smem, int64_t war
     return int(need < cap ? need : cap);
 }
 
-// Programmatic dependent launch.  Every kernel of the library starts with
-// pdl_wait(), which returns once all work that precedes it in the stream has
-// completed and its memory is visible, and only then touches global memory;
-// so stream order is preserved whatever the preceding kernel is.  Launched
-// with launch_pdl(), a kernel may be scheduled while the previous kernel in
-// the stream is still running (that kernel calls pdl_trigger()), which hides
-// the launch latency between the back-to-back calls of a decode step.
+// Programmatic dependent launch.  pdl_wait() returns once all work that
+// precedes the kernel in the stream has completed and its memory is
+// visible.  Launched with launch_pdl(), a kernel may be scheduled while the
+// previous kernel in the stream is still running (once that kernel has
+// called pdl_trigger()), which hides the launch latency between the
+// back-to-back calls of a decode step.  Every kernel of the library reads
+// activations and writes outputs only after pdl_wait(), so stream order holds
+// for them whatever the preceding kernel is.  The matrices are model
+// weights, read-only for the library's calls: the CQ 2-bit table kernel
+// loads its first rows before pdl_wait() (and triggers its dependents at
+// once), so a matrix must not be written by kernels still queued ahead of a
+// call on its stream (see qmv.h).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
