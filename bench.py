@@ -925,7 +925,7 @@ def run_configs(args):
                 med, best = _graph_time(torch, calls, reps=10)
                 emit(name, batch, "f8_matvec", nb, med, best, k, call=calls[0])
                 # head + greedy selection (no logits stored)
-                wsp = torch.empty(qmv.f8_argmax_workspace_bytes(batch), dtype=torch.uint8,
+                wsp = torch.zeros(qmv.f8_argmax_workspace_bytes(batch), dtype=torch.uint8,
                                   device=dev)
                 oi = torch.empty(batch, dtype=torch.int64, device=dev)
                 ov = torch.empty(batch, device=dev)

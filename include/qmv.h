@@ -340,11 +340,13 @@ QMV_API qmv_status hadamard_mlp(const float *x, int64_t n, int64_t D, const floa
                                 const float *d2, const float *d3, const float *residual,
                                 const float *u, int32_t batch, float *out, qmv_stream stream);
 
-/* Bytes of device workspace f8_matvec_argmax needs for `batch` vectors: one
- * (value, row) partial result per block and vector, for at most
- * QMV_ARGMAX_MAX_BLOCKS blocks. */
+/* Bytes of device workspace f8_matvec_argmax needs for `batch` vectors: a
+ * 16-byte arrival counter, then one (value, row) partial result per block
+ * and vector, for at most QMV_ARGMAX_MAX_BLOCKS blocks. */
 #define QMV_ARGMAX_MAX_BLOCKS 2048
-#define QMV_F8_ARGMAX_WORKSPACE_BYTES(batch) ((int64_t)QMV_ARGMAX_MAX_BLOCKS * (int64_t)(batch) * 16)
+#define QMV_ARGMAX_COUNTER_BYTES 16
+#define QMV_F8_ARGMAX_WORKSPACE_BYTES(batch) \
+    ((int64_t)QMV_ARGMAX_COUNTER_BYTES + (int64_t)QMV_ARGMAX_MAX_BLOCKS * (int64_t)(batch) * 16)
 
 /*
  * f8_matvec_argmax -- the head matvec followed by greedy selection, fused.
@@ -365,9 +367,13 @@ QMV_API qmv_status hadamard_mlp(const float *x, int64_t n, int64_t D, const floa
  *   out_value  [batch] float32, written (y[v][out_index[v]])
  *   workspace  device scratch of workspace_bytes >=
  *              QMV_F8_ARGMAX_WORKSPACE_BYTES(batch), 16-byte aligned,
- *              caller-owned; its contents on entry are ignored and on exit
- *              are unspecified.  Calls that overlap on the GPU must not share
- *              a workspace.
+ *              caller-owned.  Its first QMV_ARGMAX_COUNTER_BYTES bytes are a
+ *              counter with which the blocks of a call find the last one to
+ *              finish (that block reduces the partial results, so the call is
+ *              one launch): fill them with zeros once before the workspace's
+ *              first use; every call leaves them zero again.  The rest is
+ *              scratch, its contents on entry ignored.  Calls that overlap
+ *              on the GPU must not share a workspace.
  * R >= 1.  Other arguments and errors as f8_matvec.
  */
 QMV_API qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
@@ -383,8 +389,10 @@ QMV_API qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, cons
  * plug-in interface that hands over inputs and outputs but no workspace.
  *
  * Same arguments, results and errors as f8_matvec_argmax, minus the
- * workspace: the scratch is a fixed 256 KiB array inside the library (one
- * per GPU, held until the process exits), enough for batch <= QMV_MAX_BATCH;
+ * workspace: the scratch is a fixed array of
+ * QMV_F8_ARGMAX_WORKSPACE_BYTES(QMV_MAX_BATCH) bytes (256 KiB and 16 bytes)
+ * inside the library (one per GPU, held until the process exits), enough
+ * for batch <= QMV_MAX_BATCH;
  * anything beyond that returns QMV_ERR_BATCH.  The call allocates nothing.
  * Its first call in each CUDA context (per device, and again after
  * cudaDeviceReset or any other teardown of the device's context) looks up
@@ -392,7 +400,8 @@ QMV_API qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, cons
  * call before any stream capture.
  * Every call uses the same array: calls that may run at the same time on the
  * GPU (for example on two streams) race and must be ordered by the caller.
- * The array's previous contents never matter.
+ * The array starts zeroed when the library is loaded, and every call leaves
+ * its counter (the first QMV_ARGMAX_COUNTER_BYTES bytes) zero again.
  */
 QMV_API qmv_status f8_matvec_argmax_noalloc(const uint8_t *w, int64_t R, int64_t C,
                                             const uint8_t *scale, int64_t SR, int64_t SC,

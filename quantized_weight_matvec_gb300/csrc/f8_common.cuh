@@ -32,7 +32,12 @@ struct F8Args {
     const float *x;
     float *y;  // may be NULL for the argmax variant (then not stored)
     int64_t R, C, SR, SC;
-    ArgBest *ws;  // argmax variant: [gridDim.x, B] partial results
+    // argmax variant: [gridDim.x, B] partial results, the blocks' arrival
+    // counter (zero between calls) and the final outputs
+    ArgBest *ws;
+    unsigned *ctr;
+    int64_t *out_index;
+    float *out_value;
 };
 
 // Total order of the greedy choice: NaN above every number (as numpy and
@@ -93,6 +98,105 @@ __device__ __forceinline__ void block_best_store(const WarpBest<B> &wb, ArgBest 
         r.pad = 0;
         r.i = bi;
         ws[int64_t(blockIdx.x) * B + k] = r;
+    }
+}
+
+// Completion of the argmax, called by every thread of every block once the
+// block's partial bests are stored in ws[blockIdx.x * B + k].  Each block
+// makes its partials visible device-wide and counts itself in; the last
+// block to arrive (the counter then wraps back to zero, ready for the next
+// call) reduces all gridDim.x * B partials and writes the outputs.  The
+// vectors go in rounds of vpr = min(B, warps) vectors, vector k0 + j of a
+// round taking warps [j wpv, (j + 1) wpv) with wpv = warps / vpr; each
+// thread loads its partials four at a time from L2 before comparing them,
+// then shuffles and a shared-memory pass reduce them.  The order of
+// arg_better is total, so the result is the greatest element whatever the
+// order of reduction.
+//
+// `scratch` is shared memory of at least sizeof(ArgScratch) bytes, 8-byte
+// aligned, that no thread touches after the kernel's last barrier before
+// this call (the tensor-core kernels pass their epilogue buffer, so their
+// dynamic shared-memory layout keeps its alignment).
+struct ArgScratch {
+    int64_t si[32];
+    float sv[32];
+    unsigned is_last;
+};
+
+__device__ __forceinline__ void argmax_complete(const F8Args &a, int B, void *scratch) {
+    ArgScratch &sc = *static_cast<ArgScratch *>(scratch);
+    int64_t *si = sc.si;
+    float *sv = sc.sv;
+    // the barrier orders the block's partial stores before thread 0's fence,
+    // which makes them visible device-wide before the count (and, in the
+    // last block, orders the count before the reads of every partial)
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        sc.is_last = (atomicInc(a.ctr, gridDim.x - 1) == gridDim.x - 1) ? 1u : 0u;
+        __threadfence();
+    }
+    __syncthreads();
+    if (!sc.is_last) return;  // block-uniform
+    const int nblocks = int(gridDim.x);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = int(blockDim.x >> 5);
+    const int vpr = B < nw ? B : nw;
+    const int wpv = nw / vpr;
+    const int j = warp / wpv, sub = warp - j * wpv;
+    const int stride = wpv * 32, first = sub * 32 + lane;
+    for (int k0 = 0; k0 < B; k0 += vpr) {
+        const int k = k0 + j;
+        float bv = -INFINITY;
+        int64_t bi = INT64_MAX;
+        if (j < vpr && k < B) {  // warp-uniform
+            for (int b0 = first; b0 < nblocks; b0 += 4 * stride) {
+                ArgBest e[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int b = b0 + q * stride;
+                    if (b < nblocks) {
+                        const ArgBest *src = a.ws + int64_t(b) * B + k;
+                        e[q].v = __ldcg(&src->v);
+                        e[q].i = __ldcg(&src->i);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int b = b0 + q * stride;
+                    if (b < nblocks && arg_better(e[q].v, e[q].i, bv, bi)) {
+                        bv = e[q].v;
+                        bi = e[q].i;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bv, d);
+            const int64_t oi = __shfl_xor_sync(kFull, bi, d);
+            if (arg_better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == 0) {
+            sv[warp] = bv;
+            si[warp] = bi;
+        }
+        __syncthreads();
+        if (int(threadIdx.x) < vpr && k0 + int(threadIdx.x) < B) {
+            const int jj = threadIdx.x;
+            float v = sv[jj * wpv];
+            int64_t i = si[jj * wpv];
+            for (int w2 = 1; w2 < wpv; w2++)
+                if (arg_better(sv[jj * wpv + w2], si[jj * wpv + w2], v, i)) {
+                    v = sv[jj * wpv + w2];
+                    i = si[jj * wpv + w2];
+                }
+            a.out_index[k0 + jj] = i;
+            a.out_value[k0 + jj] = v;
+        }
+        __syncthreads();
     }
 }
 

@@ -42,7 +42,11 @@ __global__ void __launch_bounds__(256) f8_general_kernel(F8Args a) {
             if (lane == 0 && (!AM || a.y)) a.y[int64_t(v) * a.R + r] = val;
         }
     }
-    if (AM) block_best_store<B>(best, a.ws);
+    if (AM) {
+        __shared__ __align__(16) unsigned char arg_scratch[sizeof(ArgScratch)];
+        block_best_store<B>(best, a.ws);
+        argmax_complete(a, B, arg_scratch);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -209,9 +213,18 @@ struct SmemBest {
 
 // Tile epilogue: reduce each row's sums across the warp (fixed order), fall
 // back to the exact per-element evaluation for rows that came out NaN, store.
+// With AM, the tile's best row per vector is found in registers first (the
+// values are warp-uniform, so every lane agrees), and offered once.
 template <int B, int T, bool AM, typename Best>
 __device__ __forceinline__ void finish_tile(typename AccOf<B>::type (&acc)[T][B], const F8Args &a, int64_t r0,
                                             int rows, int lane, Best &best) {
+    float tv[B];
+    int ti[B];
+#pragma unroll
+    for (int v = 0; v < B; v++) {
+        tv[v] = -INFINITY;
+        ti[v] = T;
+    }
 #pragma unroll
     for (int t = 0; t < T; t++) {
 #pragma unroll
@@ -220,10 +233,18 @@ __device__ __forceinline__ void finish_tile(typename AccOf<B>::type (&acc)[T][B]
             acc_zero(acc[t][v]);
             if (t < rows) {
                 if (isnan(val)) val = f8_row_exact(a, r0 + t, v, nullptr);
-                if (AM) best.offer(v, val, r0 + t);
+                if (AM && arg_better(val, t, tv[v], ti[v])) {
+                    tv[v] = val;
+                    ti[v] = t;
+                }
                 if (lane == 0 && (!AM || a.y)) a.y[int64_t(v) * a.R + r0 + t] = val;
             }
         }
+    }
+    if (AM) {
+#pragma unroll
+        for (int v = 0; v < B; v++)
+            if (ti[v] < T) best.offer(v, tv[v], r0 + ti[v]);
     }
 }
 
@@ -271,7 +292,7 @@ __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kern
     const int64_t tile_stride = GS ? nwarps * T : T;
     // the argmax's running best of each warp lives in shared memory (lane 0
     // keeps it; the values it is offered are warp-uniform), which leaves the
-    // registers to the streaming accumulators
+    // registers to the streaming accumulators; each tile offers only its best
     SmemBest<B> best;
     best.init();
     if (r0 < row_end) {  // (no early return: the argmax epilogue has a barrier)
@@ -330,7 +351,11 @@ __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kern
         if (new_tile) setup_tile();
     }
     }
-    if (AM) best.store_block(a.ws);
+    if (AM) {
+        __shared__ __align__(16) unsigned char arg_scratch[sizeof(ArgScratch)];
+        best.store_block(a.ws);
+        argmax_complete(a, B, arg_scratch);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -386,42 +411,12 @@ __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
         }
         finish_tile<B, T, AM>(acc, a, r0, rows, lane, best);
     }
-    if (AM) block_best_store<B>(best, a.ws);
-}
-
-// Final pass of the argmax: warp k reduces the nblocks partials of vector k
-// (lane-strided, then a shuffle tree).  The order of arg_better is total, so
-// the result is the unique greatest element whatever the order of reduction.
-__global__ void __launch_bounds__(256) argmax_reduce_kernel(const ArgBest *ws, int nblocks, int B,
-                                                            int64_t *out_index, float *out_value) {
-    pdl_wait();
-    pdl_trigger();
-    const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (k >= B) return;  // whole warps
-    float bv = -INFINITY;
-    int64_t bi = INT64_MAX;
-    for (int b = lane; b < nblocks; b += 32) {
-        const ArgBest e = ws[int64_t(b) * B + k];
-        if (arg_better(e.v, e.i, bv, bi)) {
-            bv = e.v;
-            bi = e.i;
-        }
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, d);
-        const int64_t oi = __shfl_xor_sync(kFull, bi, d);
-        if (arg_better(ov, oi, bv, bi)) {
-            bv = ov;
-            bi = oi;
-        }
-    }
-    if (lane == 0) {
-        out_index[k] = bi;
-        out_value[k] = bv;
+    if (AM) {
+        __shared__ __align__(16) unsigned char arg_scratch[sizeof(ArgScratch)];
+        block_best_store<B>(best, a.ws);
+        argmax_complete(a, B, arg_scratch);
     }
 }
-
 
 template <int B, bool AM, int T = (B <= 2) ? 8 : 4, bool PF = false, bool GS = true>
 qmv_status launch_fast(const F8Args &a, cudaStream_t s, int &blocks_out) {
@@ -496,7 +491,7 @@ qmv_status launch_any(const F8Args &a, int batch, cudaStream_t s, int &blocks) {
 
 qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
                             int64_t SC, const float *x, int batch, float *y, cudaStream_t s) {
-    f8::F8Args a{w, scale, x, y, R, C, SR, SC, nullptr};
+    f8::F8Args a{w, scale, x, y, R, C, SR, SC, nullptr, nullptr, nullptr, nullptr};
     int blocks = 0;
     return f8::launch_any<false>(a, batch, s, blocks);
 }
@@ -504,12 +499,12 @@ qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_
 qmv_status launch_f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
                                    int64_t SC, const float *x, int batch, float *y, int64_t *out_index,
                                    float *out_value, void *workspace, cudaStream_t s) {
-    f8::F8Args a{w, scale, x, y, R, C, SR, SC, reinterpret_cast<f8::ArgBest *>(workspace)};
+    // workspace: the arrival counter in its first 16 bytes, then the partials
+    unsigned char *base = static_cast<unsigned char *>(workspace);
+    f8::F8Args a{w,     scale, x, y, R, C, SR, SC, reinterpret_cast<f8::ArgBest *>(base + QMV_ARGMAX_COUNTER_BYTES),
+                 reinterpret_cast<unsigned *>(base), out_index, out_value};
     int blocks = 0;
-    qmv_status st = f8::launch_any<true>(a, batch, s, blocks);
-    if (st != QMV_OK) return st;
-    return from_cuda(launch_pdl(f8::argmax_reduce_kernel, dim3(1), dim3(32 * batch), 0, s,
-                                static_cast<const f8::ArgBest *>(a.ws), blocks, batch, out_index, out_value));
+    return f8::launch_any<true>(a, batch, s, blocks);
 }
 
 }  // namespace qmv

@@ -186,25 +186,30 @@ struct F8Exact {
 // Argmax epilogue of the mma kernels: the 16 reducer threads of vector v
 // (lanes 16*(v%2) .. +15 of one warp) reduce their bests, and the block's
 // best for every vector goes to ws[blockIdx.x * batch + v].
-__device__ __forceinline__ void mma_argmax_store(float best_v, int64_t best_i, const F8Args &a, int batch) {
+// Every thread of the block calls it (argmax_complete follows with barriers);
+// `scratch` is the kernel's epilogue buffer, idle by then.
+__device__ __forceinline__ void mma_argmax_store(float best_v, int64_t best_i, const F8Args &a, int batch,
+                                                 void *scratch) {
     const int warp = threadIdx.x >> 5, o = threadIdx.x;
-    if (warp >= (16 * batch + 31) / 32) return;
+    if (warp < (16 * batch + 31) / 32) {  // warp-uniform
 #pragma unroll
-    for (int d = 8; d >= 1; d >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, best_v, d);
-        const int64_t oi = __shfl_xor_sync(kFull, best_i, d);
-        if (arg_better(ov, oi, best_v, best_i)) {
-            best_v = ov;
-            best_i = oi;
+        for (int d = 8; d >= 1; d >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, best_v, d);
+            const int64_t oi = __shfl_xor_sync(kFull, best_i, d);
+            if (arg_better(ov, oi, best_v, best_i)) {
+                best_v = ov;
+                best_i = oi;
+            }
+        }
+        if (o < 16 * batch && (o & 15) == 0) {
+            ArgBest r;
+            r.v = best_v;
+            r.pad = 0;
+            r.i = best_i;
+            a.ws[int64_t(blockIdx.x) * batch + (o >> 4)] = r;
         }
     }
-    if (o < 16 * batch && (o & 15) == 0) {
-        ArgBest r;
-        r.v = best_v;
-        r.pad = 0;
-        r.i = best_i;
-        a.ws[int64_t(blockIdx.x) * batch + (o >> 4)] = r;
-    }
+    argmax_complete(a, batch, scratch);
 }
 
 template <int NJ, bool AM>
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_kernel(F8Args a, int batch) {
             srb = srbn;
         }
     }
-    if (AM) mma_argmax_store(best_v, best_i, a, batch);
+    if (AM) mma_argmax_store(best_v, best_i, a, batch, red);
 }
 
 // ---------------------------------------------------------------------------
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
         }
         cp_async_wait<0>();  // (only empty groups can remain)
     }
-    if (AM) mma_argmax_store(best_v, best_i, a, batch);
+    if (AM) mma_argmax_store(best_v, best_i, a, batch, red);
 }
 
 // The tensor-core kernel: C % 64 == 0 with at least four 64-column blocks

@@ -1,8 +1,8 @@
 // no_alloc.cu -- f8_matvec_argmax_noalloc: the fused head matvec + greedy
 // selection for callers that cannot allocate device memory.
 //
-// f8_matvec_argmax needs a small scratch buffer (one partial result per
-// block and vector) that its caller provides.  Some callers have no way to
+// f8_matvec_argmax needs a small scratch buffer (an arrival counter and one
+// partial result per block and vector) that its caller provides.  Some callers have no way to
 // get one: an engine that has handed the whole device to its own memory pool
 // at start-up and treats any further cudaMalloc as an error, or a plug-in
 // interface that passes tensors in and out but offers no workspace and no
@@ -10,7 +10,7 @@
 // that lives in the library itself, so it never allocates.
 //
 // The array below is a file-scope __device__ variable: every GPU that loads
-// the library holds its 256 KiB until the process exits.  In host code its
+// the library holds its 256 KiB (and 16 bytes) until the process exits.  In host code its
 // name is only a host-side stand-in for the device symbol, not a device
 // address, so the device address is looked up once per device with
 // cudaGetSymbolAddress (while that device is current) and passed to the
@@ -23,9 +23,11 @@
 
 namespace {
 
-// Enough for every launch the argmax kernels make: at most
-// QMV_ARGMAX_MAX_BLOCKS blocks x QMV_MAX_BATCH vectors x 16 bytes.
-constexpr size_t kScratchBytes = size_t(QMV_ARGMAX_MAX_BLOCKS) * QMV_MAX_BATCH * 16;
+// Enough for every launch the argmax kernels make: the arrival counter and
+// at most QMV_ARGMAX_MAX_BLOCKS blocks x QMV_MAX_BATCH vectors x 16 bytes.
+// A __device__ array starts zeroed, so the counter is ready for the first
+// call, and every call leaves it zero.
+constexpr size_t kScratchBytes = size_t(QMV_F8_ARGMAX_WORKSPACE_BYTES(QMV_MAX_BATCH));
 
 static __device__ __align__(256) unsigned char g_argmax_scratch[kScratchBytes];
 
@@ -106,9 +108,7 @@ extern "C" qmv_status f8_matvec_argmax_noalloc(const uint8_t *w, int64_t R, int6
     qmv_status st = QMV_OK;
     void *ws = scratch_address(&st);
     if (st != QMV_OK) return st;
-    // All checks of the regular entry point still apply; the scratch does not
-    // need to start at any particular value (every block writes its partial
-    // result before the final pass reads it).
+    // All checks of the regular entry point still apply.
     return f8_matvec_argmax(w, R, C, scale, SR, SC, x, batch, y, out_index, out_value, ws,
                             int64_t(kScratchBytes), stream);
 }

@@ -29,9 +29,13 @@ TOPK_MAX_SLICES = 1024
 TOPK_WORKSPACE_BYTES = TOPK_MAX_SLICES * MAX_TOPK * 8
 
 
+ARGMAX_COUNTER_BYTES = 16
+
+
 def f8_argmax_workspace_bytes(batch: int) -> int:
-    """QMV_F8_ARGMAX_WORKSPACE_BYTES(batch)."""
-    return ARGMAX_MAX_BLOCKS * int(batch) * 16
+    """QMV_F8_ARGMAX_WORKSPACE_BYTES(batch): the arrival counter, then the
+    per-block partial results."""
+    return ARGMAX_COUNTER_BYTES + ARGMAX_MAX_BLOCKS * int(batch) * 16
 
 
 class QmvError(RuntimeError):
@@ -353,7 +357,9 @@ def f8_matvec_argmax_t(w, scale, x, y=None, workspace=None, stream=None):
     """(index[B] int64, value[B] float32) of the row maximising y = f8_matvec(...).
 
     ``y`` (optional) receives the full [B, R] result; ``workspace`` (optional)
-    is a uint8 CUDA tensor of at least f8_argmax_workspace_bytes(B) bytes."""
+    is a uint8 CUDA tensor of at least f8_argmax_workspace_bytes(B) bytes whose
+    first ARGMAX_COUNTER_BYTES bytes were zeroed before its first use (every
+    call leaves them zero)."""
     torch = _torch()
     w = _dev(w, torch.uint8, "w")
     scale = _dev(scale, torch.uint8, "scale")
@@ -362,7 +368,7 @@ def f8_matvec_argmax_t(w, scale, x, y=None, workspace=None, stream=None):
     SR, SC = scale.shape
     batch = x.shape[0] if x.dim() == 2 else 1
     if workspace is None:
-        workspace = torch.empty(f8_argmax_workspace_bytes(batch), dtype=torch.uint8, device=w.device)
+        workspace = torch.zeros(f8_argmax_workspace_bytes(batch), dtype=torch.uint8, device=w.device)
     _dev(workspace, torch.uint8, "workspace")
     idx = torch.empty(batch, dtype=torch.int64, device=w.device)
     val = torch.empty(batch, dtype=torch.float32, device=w.device)

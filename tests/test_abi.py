@@ -122,7 +122,7 @@ def test_f8_argmax_rejections():
     W, S, X, Y = FAKE, FAKE + (1 << 30), FAKE + (1 << 31), FAKE + (1 << 32)
     I, V, K = FAKE + (1 << 33), FAKE + (1 << 34), FAKE + (1 << 35)
     need = qmv.f8_argmax_workspace_bytes(2)
-    assert need == 2048 * 2 * 16
+    assert need == 16 + 2048 * 2 * 16
     a = qmv.f8_matvec_argmax
     assert a(W, 0, 16, S, 1, 1, X, 2, Y, I, V, K, need) == 2          # R >= 1
     assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, K, need - 1) == 2     # workspace too small
