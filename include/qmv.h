@@ -285,8 +285,11 @@ QMV_API qmv_status i8_quantize_x(const float *x, int64_t C, int32_t batch, int8_
  *
  * Each 16-column group's int8 x int8 sum is exact in int32; the sum times its
  * two scales is accumulated in float32, within 1e-4 * sum_c |w * s * q * d|
- * + 1e-6 of the exact value.  xq and xscale are i8_quantize_x's output (any
- * int8 codes and float scales are accepted).
+ * + 1e-6 of the exact value.  From batch 4 on, matrices large enough to
+ * stream (C a multiple of 64, 256 <= C <= 4096) run on the tensor cores
+ * instead, with q * d split into f16 hi + lo as i8_matvec splits x (same
+ * bound).  xq and xscale are i8_quantize_x's output (any int8 codes and
+ * float scales are accepted).
  *
  *   w       [R, C] int8, R >= 0, C >= 1
  *   scale   [R, ceil(C / 16)] E8M0 bytes (code 255 is NaN)

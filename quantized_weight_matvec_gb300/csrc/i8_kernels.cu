@@ -32,7 +32,20 @@ struct I8Args {
     const float *x;
     float *y;
     int64_t R, C, SG;  // SG = ceil(C / 16) scale groups per row
+    // tensor-core kernel only: when xq is set, the activations are the int8
+    // codes xq [batch, C] times their per-32-column scales xd [batch, XG]
+    // (i8_matvec_q8), and x is unused
+    const int8_t *xq;
+    const float *xd;
+    int64_t XG;
 };
+
+// Activation (v, c) of an I8Args: x, or (Q8) the code times its group scale.
+template <bool Q8>
+__device__ __forceinline__ float act_of(const I8Args &a, int v, int64_t c) {
+    if constexpr (Q8) return float(__ldg(a.xq + int64_t(v) * a.C + c)) * __ldg(a.xd + int64_t(v) * a.XG + (c >> 5));
+    return __ldg(a.x + int64_t(v) * a.C + c);
+}
 
 __device__ __forceinline__ float e8m0_scale(unsigned e) {
     if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, subnormal
@@ -491,22 +504,23 @@ constexpr size_t kDotSmemMax = 160 * 1024;
 // ---------------------------------------------------------------------------
 
 // Exact per-element value of output (r, v) (warp-collective).
+template <bool Q8>
 __device__ float i8_row_exact(const I8Args &a, int64_t r, int v) {
     const int lane = threadIdx.x & 31;
     const int8_t *wr = a.w + r * a.C;
     const uint8_t *sr = a.scale + r * a.SG;
-    const float *xv = a.x + int64_t(v) * a.C;
     float acc = 0.0f;
     for (int64_t c = lane; c < a.C; c += 32) {
         const float ws = float(__ldg(wr + c)) * e8m0_scale(__ldg(sr + (c >> 4)));
-        acc = fmaf(ws, __ldg(xv + c), acc);
+        acc = fmaf(ws, act_of<Q8>(a, v, c), acc);
     }
     return warp_sum(acc);
 }
 
+template <bool Q8>
 struct I8Exact {
     const I8Args &a;
-    __device__ __forceinline__ float operator()(int64_t r, int v) const { return i8_row_exact(a, r, v); }
+    __device__ __forceinline__ float operator()(int64_t r, int v) const { return i8_row_exact<Q8>(a, r, v); }
 };
 
 __device__ __forceinline__ bool no_better(float, int64_t, float, int64_t) { return false; }
@@ -530,7 +544,7 @@ __device__ __forceinline__ void i8x4_fold(uint32_t w, uint32_t s2, uint32_t c2, 
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(hi) : "r"(m23), "r"(s2), "r"(c2));
 }
 
-template <int NJ, int NK>
+template <int NJ, int NK, bool Q8>
 __global__ void __launch_bounds__(512, 1) i8_mma_staged_kernel(I8Args a, int batch) {
     extern __shared__ __align__(16) unsigned char st_smem[];
     using namespace mma;
@@ -572,7 +586,19 @@ __global__ void __launch_bounds__(512, 1) i8_mma_staged_kernel(I8Args a, int bat
         unsigned sa[NK], sb[NK];
         load_scales(blockIdx.x, sa, sb);
         StagedB<NJ> B;
-        build_b<NJ>(B, a.x, a.C, batch, kb_lo, NK, lane);
+        if constexpr (Q8) {
+            // q * d of the chunk's 32-column group (16-byte aligned codes)
+            auto load16 = [&](int v, int64_t c0, float (&xs)[16]) {
+                const uint4 qv = __ldg(reinterpret_cast<const uint4 *>(a.xq + int64_t(v) * a.C + c0));
+                const float dv = __ldg(a.xd + int64_t(v) * a.XG + (c0 >> 5));
+                const unsigned wq[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int e = 0; e < 16; e++) xs[e] = float(int8_t(wq[e >> 2] >> (8 * (e & 3)))) * dv;
+            };
+            build_b_from<NJ>(B, load16, batch, kb_lo, NK, lane);
+        } else {
+            build_b<NJ>(B, a.x, a.C, batch, kb_lo, NK, lane);
+        }
 
         float tot[NJ][2];
 #pragma unroll
@@ -631,7 +657,7 @@ __global__ void __launch_bounds__(512, 1) i8_mma_staged_kernel(I8Args a, int bat
                     tot[j][1] = fmaf(hb, f, tot[j][1]);
                 }
             }
-            tile_epilogue<NJ, false>(tot, red, buf, NW, batch, a.R, a.y, tl * 16, best_v, best_i, I8Exact{a},
+            tile_epilogue<NJ, false>(tot, red, buf, NW, batch, a.R, a.y, tl * 16, best_v, best_i, I8Exact<Q8>{a},
                                      no_better);
             buf ^= 1;
             if (++slot == kRing) slot = 0;
@@ -645,11 +671,11 @@ __global__ void __launch_bounds__(512, 1) i8_mma_staged_kernel(I8Args a, int bat
     }
 }
 
-template <int NJ, int NK>
+template <int NJ, int NK, bool Q8 = false>
 qmv_status launch_i8_mma(const I8Args &a, int batch, cudaStream_t s) {
     const int NW = int(a.C / 64 / NK);
     const size_t smem = mma::staged_smem_bytes(NW, NK, NJ, 0);
-    auto kern = i8_mma_staged_kernel<NJ, NK>;
+    auto kern = i8_mma_staged_kernel<NJ, NK, Q8>;
     const void *kp = reinterpret_cast<const void *>(kern);
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
     const int64_t ntiles = (a.R + 15) / 16;
@@ -658,12 +684,12 @@ qmv_status launch_i8_mma(const I8Args &a, int batch, cudaStream_t s) {
     return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(32 * NW), smem, s, a, batch));
 }
 
-template <int NJ>
+template <int NJ, bool Q8 = false>
 qmv_status launch_i8_mma_any(const I8Args &a, int batch, int nk, cudaStream_t s) {
     switch (nk) {
-        case 4: return launch_i8_mma<NJ, 4>(a, batch, s);
-        case 2: return launch_i8_mma<NJ, 2>(a, batch, s);
-        default: return launch_i8_mma<NJ, 1>(a, batch, s);
+        case 4: return launch_i8_mma<NJ, 4, Q8>(a, batch, s);
+        case 2: return launch_i8_mma<NJ, 2, Q8>(a, batch, s);
+        default: return launch_i8_mma<NJ, 1, Q8>(a, batch, s);
     }
 }
 
@@ -702,6 +728,18 @@ qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool launch_i8_matvec_q8_mma(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale, const int8_t *xq,
+                             const float *xd, int batch, float *y, cudaStream_t s, qmv_status &st) {
+    if (batch < 2 || C < 256 || (reinterpret_cast<uintptr_t>(w) % 16) != 0 ||
+        (reinterpret_cast<uintptr_t>(xq) % 16) != 0)
+        return false;
+    const int nk = mma::staged_nk(C, batch);
+    if (!nk) return false;
+    I8Args a{w, scale, nullptr, y, R, C, (C + 15) / 16, xq, xd, (C + 31) / 32};
+    st = (batch <= 4) ? launch_i8_mma_any<1, true>(a, batch, nk, s) : launch_i8_mma_any<2, true>(a, batch, nk, s);
+    return true;
+}
 
 qmv_status launch_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale, const float *x,
                             int batch, float *y, cudaStream_t s) {

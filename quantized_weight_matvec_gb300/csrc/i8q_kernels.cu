@@ -255,6 +255,14 @@ qmv_status launch_i8q(const I8QArgs &a, cudaStream_t s) {
     const int64_t capacity = int64_t(occupancy(kp, 256, stage_bytes(B, a.C))) * sm_count() * 8;
     // too few tiles for a streaming grid: shorter tiles, several steps per load
     if ((a.R + T - 1) / T < 4 * capacity) return launch_stream<B, 2, (B <= 2) ? 8 : 4>(a, s);
+    // A streaming matrix from batch 4 on: the dp4a and float work per weight
+    // outgrows the weight stream, so the I8 tensor-core kernel takes the call
+    // when it fits, with the activations q * d split into f16 hi + lo like
+    // float x.
+    if (B >= 4) {
+        qmv_status st = QMV_OK;
+        if (launch_i8_matvec_q8_mma(a.w, a.R, a.C, a.scale, a.xq, a.xd, B, a.y, s, st)) return st;
+    }
     return launch_stream<B, T, 1>(a, s);
 }
 

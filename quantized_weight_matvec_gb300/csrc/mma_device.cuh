@@ -75,7 +75,8 @@ struct StagedB {
     float f[4][NJ];
 };
 
-// Builds StagedB from x [batch, C] for column blocks kb_lo .. kb_lo+nk-1.
+// Builds StagedB for column blocks kb_lo .. kb_lo+nk-1 of the activations,
+// whose 16 values at column c0 of vector v come from load16(v, c0, xs).
 // Lane (g, t)'s fragments of column block kb all come from its own 16-column
 // chunk 64*kb + 16*t of vector 4j + g/2 (hi part for even g, lo for odd g),
 // so each lane loads that chunk and splits it itself; the block's largest
@@ -83,9 +84,9 @@ struct StagedB {
 // split as split_block: m, E = min(14 - floor(log2 m), 127), hi, lo, 2^-E
 // (NaN when the block holds Inf or NaN).  f of vector 4j+t (the lane's
 // accumulator) comes from lane 8t, which split that vector.
-template <int NJ>
-__device__ __forceinline__ void build_b(StagedB<NJ> &B, const float *x, int64_t C, int batch, int kb_lo, int nk,
-                                        int lane) {
+template <int NJ, typename Load16>
+__device__ __forceinline__ void build_b_from(StagedB<NJ> &B, Load16 load16, int batch, int kb_lo, int nk,
+                                             int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int k = 0; k < 4; k++) {
@@ -95,15 +96,7 @@ __device__ __forceinline__ void build_b(StagedB<NJ> &B, const float *x, int64_t 
             const int v = 4 * j + (g >> 1);
             float xs[16];
             if (v < batch) {
-                const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(v) * C + int64_t(kb_lo + k) * 64 + 16 * t);
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const float4 f4 = __ldg(src + q);
-                    xs[4 * q] = f4.x;
-                    xs[4 * q + 1] = f4.y;
-                    xs[4 * q + 2] = f4.z;
-                    xs[4 * q + 3] = f4.w;
-                }
+                load16(v, int64_t(kb_lo + k) * 64 + 16 * t, xs);
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; e++) xs[e] = 0.0f;
@@ -145,6 +138,24 @@ __device__ __forceinline__ void build_b(StagedB<NJ> &B, const float *x, int64_t 
             B.f[k][j] = __shfl_sync(kFull, f, 8 * t);
         }
     }
+}
+
+// StagedB from float activations x [batch, C].
+template <int NJ>
+__device__ __forceinline__ void build_b(StagedB<NJ> &B, const float *x, int64_t C, int batch, int kb_lo, int nk,
+                                        int lane) {
+    auto load16 = [&](int v, int64_t c0, float (&xs)[16]) {
+        const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(v) * C + c0);
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const float4 f4 = __ldg(src + q);
+            xs[4 * q] = f4.x;
+            xs[4 * q + 1] = f4.y;
+            xs[4 * q + 2] = f4.z;
+            xs[4 * q + 3] = f4.w;
+        }
+    };
+    build_b_from<NJ>(B, load16, batch, kb_lo, nk, lane);
 }
 
 // Copies this warp's part of tile `tl` of the byte matrix w [R, C] -- 16 rows

@@ -91,6 +91,12 @@ qmv_status launch_i8_quantize_x(const float *x, int64_t C, int batch, int8_t *xq
 qmv_status launch_i8_matvec_q8(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                                const int8_t *xq, const float *xd, int batch, float *y,
                                cudaStream_t s);
+// The I8 tensor-core kernel over q * d activations (i8_kernels.cu): false when
+// it does not take the call (batch < 2, C not a multiple of 64 in
+// [256, 4096], unaligned w or xq); else launches it and sets st.
+bool launch_i8_matvec_q8_mma(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,
+                             const int8_t *xq, const float *xd, int batch, float *y, cudaStream_t s,
+                             qmv_status &st);
 
 // ---- Hadamard MLP ----------------------------------------------------------
 qmv_status launch_hadamard_mlp(const float *x, int64_t n, int D, const float *d1, const float *d2,

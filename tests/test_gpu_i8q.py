@@ -8,8 +8,9 @@ bit-identical to the oracle's (both divide in IEEE float32 and round to
 nearest even).  The matvec's inputs come from the oracle's quantizer, never
 from the GPU's; its outputs must be within 1e-4 * sum_c |w s q d| + 1e-6 of
 the oracle's float64 value.  The shapes cover the streaming kernel (many
-rows), the small-matrix kernel (few rows), the general kernel (C % 16 != 0)
-and ragged tails (C % 32 == 16, a short last tile of rows)."""
+rows), the small-matrix kernel (few rows), the general kernel (C % 16 != 0),
+the tensor-core route of large matrices at batch 4-8, and ragged tails
+(C % 32 == 16, a short last tile of rows)."""
 import os
 
 import numpy as np
@@ -104,6 +105,26 @@ def test_matvec_q8_extreme_scales_codes_and_nan():
     y = check_matvec(f, q, d)
     assert np.isnan(y[:, 9]).all() and np.isnan(y[1]).all()
     assert not np.isnan(np.delete(y[[0, 2]], 9, axis=1)).any()
+
+
+@pytest.mark.parametrize("batch,C", [(4, 256), (5, 1024), (8, 4096)])
+def test_matvec_q8_tensor_core_route(batch, C):
+    """Matrices large enough to stream take the tensor-core kernel from batch 4
+    on (q * d split into f16 hi + lo); weight scales outside the range it folds
+    exactly (2^-24 .. 2^5), the NaN scale code and a NaN activation scale take
+    its exact per-element fix-up."""
+    R = 50000
+    f = synth.i8_inputs(60 + batch, R, C, 110, 124, batch=batch)
+    q, d = oracle.i8_quantize_x(f.x)
+    check_matvec(f, q, d)
+    f.scale[5, 0] = 140          # 2^13: outside the folded range
+    f.scale[7, 1] = 90           # 2^-37
+    f.scale[9, 2] = 255          # NaN
+    d = d.copy()
+    d[batch - 1, 1] = np.nan
+    y = check_matvec(f, q, d)
+    assert np.isnan(y[:, 9]).all() and np.isnan(y[batch - 1]).all()
+    assert np.isfinite(y[:batch - 1, 5]).all() and np.isfinite(y[:batch - 1, 7]).all()
 
 
 def test_quantize_then_matvec_composite():
