@@ -216,7 +216,7 @@ def measured_hbm_gbs():
 
 
 # What the batch-1 head kernel (f8_fast_kernel) is compiled from.
-TRAFFIC_SOURCES = ("f8_kernels.cu", "f8_common.cuh", "qmv_internal.h")
+TRAFFIC_SOURCES = ("f8_kernels.cu", "f8_common.cuh", "device_common.cuh", "qmv_internal.h")
 
 
 def kernel_source_hash():
@@ -960,6 +960,76 @@ def run_configs(args):
     oracle_config_lines(args.only)
 
 
+# --------------------------------------------------------------------------
+# one kernel on a small case, for ncu captures (--case): no timings are
+# printed, since numbers taken under a profiler are not measurements
+# --------------------------------------------------------------------------
+
+def run_case(args):
+    """Run one kernel of the path --iters times on a seeded synthetic case
+    and print a checksum.  Cases: f8 (E4M3 rows x 4096, scales [rows/128,
+    32]), f8am (the same with greedy selection), i8 (int8 rows x 4096,
+    per-16 E8M0 scales), i8q (the same weights x int8 activations), cq2
+    (2-bit rows x 512, input 500, group 128: the table kernel), cqvec
+    (--bits-bit rows x 512, group 64: the vectorised kernel), gather (64 rows
+    of a 32768 x 512 2-bit matrix), prepare, topk (top-64 temperature
+    sampling over --rows normal logits per vector)."""
+    import torch
+    from quantized_weight_matvec_gb300 import qmv, synth
+    qmv.load()
+    dev = torch.device("cuda", 0)
+    k, rows, batch = args.case, args.rows, args.batch
+    if k in ("f8", "f8am"):
+        f = synth.f8_inputs(5, rows, 4096, max(1, rows // 128), 32, 118, 132, batch=batch)
+        w, s, x = (torch.from_numpy(a).to(dev) for a in (f.w, f.scale, f.x))
+        y = torch.empty((batch, rows), device=dev)
+        for _ in range(args.iters):
+            if k == "f8":
+                qmv.f8_matvec_t(w, s, x, out=y)
+            else:
+                qmv.f8_matvec_argmax_t(w, s, x, y=y)
+        out = y
+    elif k in ("i8", "i8q"):
+        f = synth.i8_inputs(7, rows, 4096, 110, 124, batch=batch)
+        w, s, x = (torch.from_numpy(a).to(dev) for a in (f.w, f.scale, f.x))
+        y = torch.empty((batch, rows), device=dev)
+        xq, xs = qmv.i8_quantize_x_t(x)
+        for _ in range(args.iters):
+            if k == "i8":
+                qmv.i8_matvec_t(w, s, x, out=y)
+            else:
+                qmv.i8_matvec_q8_t(w, s, xq, xs, out=y)
+        out = y
+    elif k == "topk":
+        g = torch.Generator(device="cpu").manual_seed(0)
+        y = (torch.randn((batch, rows), generator=g) * 3).to(dev)
+        u = torch.rand(batch, generator=g).to(dev)
+        for _ in range(args.iters):
+            idx, val, prob, tok = qmv.topk_sample_t(y, 64, 1.0, u)
+        out = prob
+    elif k == "cqvec":
+        c = synth.cq_inputs(2, rows, 512, 64, args.bits, batch=batch)
+        m = qmv.CQMatrix.from_numpy(c, device=dev)
+        p = qmv.cq_prepare_t(m, torch.from_numpy(c.x).to(dev))
+        for _ in range(args.iters):
+            out = qmv.cq_matvec_t(m, p)
+    else:
+        n = rows if k == "cq2" else 32768
+        c = synth.cq_inputs(3, n, 500, 128, 2, batch=batch, x_scale=3.0, gather=64)
+        m = qmv.CQMatrix.from_numpy(c, device=dev)
+        x = torch.from_numpy(c.x).to(dev)
+        p = qmv.cq_prepare_t(m, x)
+        for _ in range(args.iters):
+            if k == "cq2":
+                out = qmv.cq_matvec_t(m, p)
+            elif k == "gather":
+                out = qmv.cq_dequantize_row_t(m, torch.from_numpy(c.rows).to(dev))
+            else:
+                out = qmv.cq_prepare_t(m, x, out=p)
+    torch.cuda.synchronize()
+    print("checksum %.6e" % float(out.double().abs().sum()))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -970,9 +1040,18 @@ def main(argv=None):
                     help="per-workload sweep (one JSON line per workload, batch and op)")
     ap.add_argument("--only", default="",
                     help="with --configs: only the workloads whose name contains this text")
+    ap.add_argument("--case", choices=["f8", "f8am", "i8", "i8q", "cq2", "cqvec", "gather",
+                                       "prepare", "topk"],
+                    help="run one kernel on a small case for an ncu capture (no timings)")
+    ap.add_argument("--rows", type=int, default=65536, help="with --case: matrix rows")
+    ap.add_argument("--bits", type=int, default=4, help="with --case cqvec: index width")
+    ap.add_argument("--batch", type=int, default=1, help="with --case: activation vectors")
+    ap.add_argument("--iters", type=int, default=3, help="with --case: calls")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.configs:
+    if args.case:
+        run_case(args)
+    elif args.configs:
         run_configs(args)
     elif args.impl == "reference":
         run_reference(args)

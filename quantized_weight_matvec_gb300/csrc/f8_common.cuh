@@ -12,6 +12,7 @@
 #include <cuda_fp8.h>
 #include <stdint.h>
 
+#include "device_common.cuh"
 #include "qmv_internal.h"
 
 namespace qmv {
@@ -214,18 +215,7 @@ __device__ __forceinline__ float e4m3_exact(unsigned b) {
     return (b & 0x80u) ? -mag : mag;
 }
 
-// E8M0 byte -> 2^(e-127) as float32; 255 -> NaN.
-__device__ __forceinline__ float e8m0_value(unsigned e) {
-    if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, subnormal
-    if (e == 255) return __uint_as_float(0x7fc00000u);
-    return __uint_as_float(e << 23);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
-    return v;  // every lane holds the same bits (a + b == b + a)
-}
+using dev::warp_sum;
 
 // Exact per-element evaluation of one output, shared by the general kernel
 // and by the fast kernel's fix-up of rows that hit a saturated code.  The
@@ -238,22 +228,13 @@ static __device__ float f8_row_exact(const F8Args &a, int64_t r, int v, const fl
     float acc = 0.0f;
     for (int64_t c = threadIdx.x & 31; c < a.C; c += 32) {
         const float wv = lut ? lut[__ldg(wr + c)] : e4m3_exact(__ldg(wr + c));
-        const float sv = e8m0_value(__ldg(sr + c * a.SC / a.C));
+        const float sv = dev::e8m0(__ldg(sr + c * a.SC / a.C));
         acc = fmaf(wv * sv, __ldg(xv + c), acc);
     }
     return warp_sum(acc);
 }
 
-// Streaming 16-byte load of read-only weights, not kept in L1.  Not volatile:
-// the weights are never written while a matvec runs, so the compiler may
-// schedule these loads freely.
-__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
-    uint4 d;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
-        : "l"(p));
-    return d;
-}
+using dev::ld_stream;
 
 __device__ __forceinline__ unsigned word_of(const uint4 &d, int q) {
     return q == 0 ? d.x : q == 1 ? d.y : q == 2 ? d.z : d.w;

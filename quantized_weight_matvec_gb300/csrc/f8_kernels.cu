@@ -116,9 +116,9 @@ __device__ __forceinline__ void compute_step(typename AccOf<B>::type (&acc)[T][B
                                              const F8Args &a, const uint8_t *srow0, uint32_t dpack, int cb,
                                              int64_t ch) {
     // scale of row t for this chunk
-    const float s0 = e8m0_value(__ldg(srow0 + cb));
+    const float s0 = dev::e8m0(__ldg(srow0 + cb));
     auto scale_of = [&](int t) -> float {
-        return UNIFORM ? s0 : e8m0_value(__ldg(srow0 + int64_t((dpack >> (4 * t)) & 15u) * a.SC + cb));
+        return UNIFORM ? s0 : dev::e8m0(__ldg(srow0 + int64_t((dpack >> (4 * t)) & 15u) * a.SC + cb));
     };
 #pragma unroll
     for (int q = 0; q < 4; q++) {

@@ -134,7 +134,7 @@ __device__ __forceinline__ void mma_compute(float (&tot)[NJ][2], const MmaStep &
                 mma_16816(acc[0], a0, a1, a2, a3, b.x, b.y);
             }
         }
-        const float sa = e8m0_value(st.s[0][k]), sb = e8m0_value(st.s[1][k]);
+        const float sa = dev::e8m0(st.s[0][k]), sb = dev::e8m0(st.s[1][k]);
 #pragma unroll
         for (int j = 0; j < NJ; j++) {
             const float f = fv[kb * 4 * NJ + 4 * j + t];
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
                     for (int j = 0; j < NJ; j++)
                         mma_16816(acc[i % NA][j], a0, a1, a2, a3, B.b[k][i][j][0], B.b[k][i][j][1]);
                 }
-                const float s_a = e8m0_value(sa[k]), s_b = e8m0_value(sb[k]);
+                const float s_a = dev::e8m0(sa[k]), s_b = dev::e8m0(sb[k]);
 #pragma unroll
                 for (int j = 0; j < NJ; j++) {
                     const float f = B.f[k][j];

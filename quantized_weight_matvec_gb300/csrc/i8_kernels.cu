@@ -18,6 +18,7 @@
 // subtracted) and multiplied in float32.
 #include <stdint.h>
 
+#include "device_common.cuh"
 #include "mma_device.cuh"
 #include "qmv_internal.h"
 
@@ -47,17 +48,7 @@ __device__ __forceinline__ float act_of(const I8Args &a, int v, int64_t c) {
     return __ldg(a.x + int64_t(v) * a.C + c);
 }
 
-__device__ __forceinline__ float e8m0_scale(unsigned e) {
-    if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, subnormal
-    if (e == 255) return __uint_as_float(0x7fc00000u);
-    return __uint_as_float(e << 23);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
-    return v;
-}
+using dev::warp_sum;
 
 // The four int8 weights of a word as exact floats.
 __device__ __forceinline__ void widen4(unsigned word, float (&f)[4]) {
@@ -67,13 +58,7 @@ __device__ __forceinline__ void widen4(unsigned word, float (&f)[4]) {
         f[k] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u | unsigned(k))) - 8388736.0f;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const int8_t *p) {
-    uint4 d;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(d.x), "=r"(d.y), "=r"(d.z), "=r"(d.w)
-        : "l"(p));
-    return d;
-}
+using dev::ld_stream;
 
 __device__ __forceinline__ unsigned word_of(const uint4 &d, int q) {
     return q == 0 ? d.x : q == 1 ? d.y : q == 2 ? d.z : d.w;
@@ -158,7 +143,7 @@ __device__ __forceinline__ void compute_step(typename Acc<B>::type (&acc)[T][B],
     }
 #pragma unroll
     for (int t = 0; t < T; t++) {
-        const float s = e8m0_scale(e[t]);
+        const float s = dev::e8m0(e[t]);
 #pragma unroll
         for (int v = 0; v < B; v++) {
             if constexpr (SCALAR)
@@ -274,7 +259,7 @@ __global__ void __launch_bounds__(256) i8_general_kernel(I8Args a) {
 #pragma unroll
         for (int v = 0; v < B; v++) acc[v] = 0.0f;
         for (int64_t c = lane; c < a.C; c += 32) {
-            const float ws = float(__ldg(wr + c)) * e8m0_scale(__ldg(sr + (c >> 4)));
+            const float ws = float(__ldg(wr + c)) * dev::e8m0(__ldg(sr + (c >> 4)));
 #pragma unroll
             for (int v = 0; v < B; v++) acc[v] = fmaf(ws, __ldg(a.x + v * a.C + c), acc[v]);
         }
@@ -406,7 +391,7 @@ __global__ void __launch_bounds__(256) i8_dot_kernel(I8Args a, int nj) {
         if (ch < nchunk) {
             float sw[T];
 #pragma unroll
-            for (int t = 0; t < T; t++) sw[t] = e8m0_scale(e[t]);
+            for (int t = 0; t < T; t++) sw[t] = dev::e8m0(e[t]);
 #pragma unroll
             for (int v = 0; v < B; v++) {
                 const uint4 *lp = limbs + (int64_t(v * nj + j) * 4) * 32 + lane;
@@ -511,7 +496,7 @@ __device__ float i8_row_exact(const I8Args &a, int64_t r, int v) {
     const uint8_t *sr = a.scale + r * a.SG;
     float acc = 0.0f;
     for (int64_t c = lane; c < a.C; c += 32) {
-        const float ws = float(__ldg(wr + c)) * e8m0_scale(__ldg(sr + (c >> 4)));
+        const float ws = float(__ldg(wr + c)) * dev::e8m0(__ldg(sr + (c >> 4)));
         acc = fmaf(ws, act_of<Q8>(a, v, c), acc);
     }
     return warp_sum(acc);

@@ -28,6 +28,7 @@
 // two, barring underflow), and one FMA adds it times d to the accumulator.
 #include <stdint.h>
 
+#include "device_common.cuh"
 #include "qmv_internal.h"
 
 namespace qmv {
@@ -44,17 +45,7 @@ struct I8QArgs {
     int64_t R, C, SG, XG;  // SG = ceil(C/16) weight groups, XG = ceil(C/32) activation groups
 };
 
-__device__ __forceinline__ float e8m0_scale(unsigned e) {
-    if (e == 0) return __uint_as_float(0x00400000u);  // 2^-127, subnormal
-    if (e == 255) return __uint_as_float(0x7fc00000u);
-    return __uint_as_float(e << 23);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(kFull, v, d);
-    return v;
-}
+using dev::warp_sum;
 
 // ---------------------------------------------------------------------------
 // Quantizer: one warp per (vector, group of 32); lane l holds column 32 j + l.
@@ -157,7 +148,7 @@ __global__ void __launch_bounds__(256) i8q_kernel(I8QArgs a) {
                 if (ch >= nchunk) continue;
                 float sw[T];
 #pragma unroll
-                for (int t = 0; t < T; t++) sw[t] = e8m0_scale(e[st][t]);
+                for (int t = 0; t < T; t++) sw[t] = dev::e8m0(e[st][t]);
 #pragma unroll
                 for (int v = 0; v < B; v++) {
                     const uint4 xv = *reinterpret_cast<const uint4 *>(xs + int64_t(v) * a.C + ch * 16);
@@ -209,7 +200,7 @@ __global__ void __launch_bounds__(256) i8q_general_kernel(I8QArgs a) {
         for (int v = 0; v < B; v++) acc[v] = 0.0f;
         for (int64_t c = lane; c < a.C; c += 32) {
             const int wv = __ldg(wr + c);
-            const float s = e8m0_scale(__ldg(sr + (c >> 4)));
+            const float s = dev::e8m0(__ldg(sr + (c >> 4)));
 #pragma unroll
             for (int v = 0; v < B; v++) {
                 const int p = wv * int(__ldg(a.xq + int64_t(v) * a.C + c));
