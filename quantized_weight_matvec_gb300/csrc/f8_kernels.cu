@@ -274,13 +274,11 @@ struct FastMinBlocks {
 template <int B, int T, bool PF, bool GS, bool AM>
 __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kernel(F8Args a) {
     extern __shared__ int chunk_cb[];
+    pdl_trigger();
     const int64_t nchunk = a.C >> 4;
     // (depends only on the shapes: runs before the wait)
     for (int64_t ch = threadIdx.x; ch < nchunk; ch += blockDim.x)
         chunk_cb[ch] = int((ch * 16 * a.SC) / a.C);
-    pdl_wait();
-    pdl_trigger();
-    __syncthreads();
 
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -290,6 +288,13 @@ __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kern
     const int64_t row_end = GS ? a.R : a.R * (wid + 1) / nwarps;
     int64_t r0 = GS ? wid * T : a.R * wid / nwarps;
     const int64_t tile_stride = GS ? nwarps * T : T;
+    // the first step of the first tile goes out before the dependency wait
+    // (the weights never depend on the preceding kernel); the argmax variant,
+    // tighter on registers, loads it after the wait
+    uint4 cur[T];
+    if (!AM && r0 < row_end) load_step<T>(cur, a, r0, int(min(int64_t(T), row_end - r0)), lane, nchunk);
+    pdl_wait();
+    __syncthreads();
     // the argmax's running best of each warp lives in shared memory (lane 0
     // keeps it; the values it is offered are warp-uniform), which leaves the
     // registers to the streaming accumulators; each tile offers only its best
@@ -300,8 +305,7 @@ __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kern
 
     int rows = int(min(int64_t(T), row_end - r0));
     int j = 0;
-    uint4 cur[T];
-    load_step<T>(cur, a, r0, rows, lane, nchunk);
+    if (AM) load_step<T>(cur, a, r0, rows, lane, nchunk);
 
     typename AccOf<B>::type acc[T][B];
 #pragma unroll
@@ -369,16 +373,25 @@ __global__ void __launch_bounds__(256, FastMinBlocks<B, AM>::value) f8_fast_kern
 template <int B, int T, int NSTEP, bool AM>
 __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
     extern __shared__ int chunk_cb[];
+    pdl_trigger();
     const int64_t nchunk = a.C >> 4;
     for (int64_t ch = threadIdx.x; ch < nchunk; ch += blockDim.x)
         chunk_cb[ch] = int((ch * 16 * a.SC) / a.C);
-    pdl_wait();
-    pdl_trigger();
-    __syncthreads();
-
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
     const int64_t ntiles = (a.R + T - 1) / T;
+    const int64_t tile0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    // the first steps of this warp's first tile go out before the wait (the
+    // weights never depend on the preceding kernel)
+    uint4 d[NSTEP][T];
+    if (tile0 < ntiles) {
+        const int rows0 = int(min(int64_t(T), a.R - tile0 * T));
+#pragma unroll
+        for (int st = 0; st < NSTEP; st++) load_step<T>(d[st], a, tile0 * T, rows0, lane + 32 * st, nchunk);
+    }
+    pdl_wait();
+    __syncthreads();
+
     typename AccOf<B>::type acc[T][B];
 #pragma unroll
     for (int t = 0; t < T; t++)
@@ -387,17 +400,17 @@ __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
 
     WarpBest<B> best;
     best.init();
-    for (int64_t tile = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; tile < ntiles;
-         tile += nwarps) {
+    for (int64_t tile = tile0; tile < ntiles; tile += nwarps) {
         const int64_t r0 = tile * T;
         const int rows = int(min(int64_t(T), a.R - r0));
         const uint8_t *srow0;
         uint32_t dpack;
         const bool uniform = setup_scale<T>(a, r0, rows, srow0, dpack);
         for (int64_t base = 0; base < nchunk; base += 32 * NSTEP) {
-            uint4 d[NSTEP][T];
+            if (tile != tile0 || base != 0) {
 #pragma unroll
-            for (int st = 0; st < NSTEP; st++) load_step<T>(d[st], a, r0, rows, base + lane + 32 * st, nchunk);
+                for (int st = 0; st < NSTEP; st++) load_step<T>(d[st], a, r0, rows, base + lane + 32 * st, nchunk);
+            }
 #pragma unroll
             for (int st = 0; st < NSTEP; st++) {
                 const int64_t ch = base + lane + 32 * st;

@@ -25,8 +25,6 @@
 namespace qmv {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
-
 struct I8Args {
     const int8_t *w;
     const uint8_t *scale;
@@ -365,7 +363,6 @@ __global__ void __launch_bounds__(256) i8_dot_kernel(I8Args a, int nj) {
     extern __shared__ uint4 dsm[];
     uint4 *limbs = dsm;
     float *xs = reinterpret_cast<float *>(dsm + int64_t(B) * nj * 128);
-    pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nchunk = a.C >> 4;
@@ -374,10 +371,12 @@ __global__ void __launch_bounds__(256) i8_dot_kernel(I8Args a, int nj) {
     const int64_t tile_stride = nwarps * T;
     int64_t r0 = ((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5) * T;
     int rows = int(min(int64_t(T), a.R - max(r0, int64_t(0))));
-    // first step's weights in flight while x is converted
+    // first step's weights in flight before the dependency wait (they never
+    // depend on the preceding kernel) and while x is converted
     uint4 d[T];
     unsigned e[T];
     if (r0 < a.R) load_step<T>(d, e, a, r0, rows, lane, nchunk);
+    pdl_wait();
     prep_x_limbs(a, B, nj, limbs, xs);
     __syncthreads();
     if (r0 >= a.R) return;
@@ -544,8 +543,7 @@ __global__ void __launch_bounds__(512, 1) i8_mma_staged_kernel(I8Args a, int bat
     float *red = reinterpret_cast<float *>(st_smem + size_t(NW) * kRing * SLOT);
     const uint8_t *w8 = reinterpret_cast<const uint8_t *>(a.w);
 
-    pdl_wait();
-    pdl_trigger();
+    if (NJ == 1) pdl_trigger();
 
     const int64_t ntiles = (a.R + 15) >> 4;
     const int64_t gstride = gridDim.x;
@@ -561,15 +559,29 @@ __global__ void __launch_bounds__(512, 1) i8_mma_staged_kernel(I8Args a, int bat
             sb[k] = __ldg(pb + 4 * k);
         }
     };
-    if (int64_t(blockIdx.x) < ntiles) {  // block-uniform
+    // the first kRing - 1 tiles of weights and the first tile's scale codes
+    // go out before the dependency wait (they never depend on the preceding
+    // kernel); at batch 5-8 (NJ = 2), where the kernel sits at its register
+    // limit, after it (as for the F8 kernel)
+    unsigned sa[NK], sb[NK];
+    auto issue_first = [&]() {
+        if (int64_t(blockIdx.x) < ntiles) {  // block-uniform
 #pragma unroll
-        for (int st = 0; st < kRing - 1; st++) {
-            const int64_t tl = blockIdx.x + st * gstride;
-            if (tl < ntiles) issue_tile<NK>(ring + uint32_t(st * SLOT), w8, a.R, a.C, tl, kb_lo, lane);
-            cp_async_commit();
+            for (int st = 0; st < kRing - 1; st++) {
+                const int64_t tl = blockIdx.x + st * gstride;
+                if (tl < ntiles) issue_tile<NK>(ring + uint32_t(st * SLOT), w8, a.R, a.C, tl, kb_lo, lane);
+                cp_async_commit();
+            }
+            load_scales(blockIdx.x, sa, sb);
         }
-        unsigned sa[NK], sb[NK];
-        load_scales(blockIdx.x, sa, sb);
+    };
+    if (NJ == 1) issue_first();
+    pdl_wait();
+    if (NJ != 1) {
+        pdl_trigger();
+        issue_first();
+    }
+    if (int64_t(blockIdx.x) < ntiles) {  // block-uniform
         StagedB<NJ> B;
         if constexpr (Q8) {
             // q * d of the chunk's 32-column group (16-byte aligned codes)

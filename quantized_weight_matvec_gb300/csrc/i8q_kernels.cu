@@ -104,7 +104,6 @@ __global__ void __launch_bounds__(256) i8q_kernel(I8QArgs a) {
     extern __shared__ uint4 dsm[];
     int8_t *xs = reinterpret_cast<int8_t *>(dsm);
     float *ds = reinterpret_cast<float *>(xs + int64_t(B) * a.C);
-    pdl_wait();
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nchunk = a.C >> 4;
@@ -112,7 +111,8 @@ __global__ void __launch_bounds__(256) i8q_kernel(I8QArgs a) {
     const int64_t ntiles = (a.R + T - 1) / T;
     int64_t tile = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
 
-    // the first weights in flight while the codes are staged
+    // the first weights in flight before the dependency wait (they never
+    // depend on the preceding kernel) and while the codes are staged
     uint4 w[NSTEP][T];
     unsigned e[NSTEP][T];
     if (tile < ntiles) {
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(256) i8q_kernel(I8QArgs a) {
 #pragma unroll
         for (int st = 0; st < NSTEP; st++) load_rows<T>(w[st], e[st], a, tile * T, rows, lane + 32 * st, nchunk);
     }
+    pdl_wait();
     {
         const int64_t nv = (int64_t(B) * a.C) >> 4;
         const uint4 *src = reinterpret_cast<const uint4 *>(a.xq);
