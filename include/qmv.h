@@ -216,8 +216,14 @@ QMV_API qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, c
  * on the tensor cores: every finite E4M3 value is an f16, and each 64-column
  * block of x is split into f16 parts hi + lo under a power-of-two exponent,
  * which carries an element to 2^-22 of itself or 2^-39 of the block's
- * largest |x|, whichever is larger.  Non-finite results are recomputed
- * element by element, so NaN and Inf follow the formula above.
+ * largest |x|, whichever is larger.  At batch 5..8, when C is a multiple of
+ * 128 up to 4096, every scale block starts on a multiple of 128 columns and
+ * of 64 rows, and w and x are 16-byte aligned, the raw E4M3 weights go to
+ * the fifth-generation tensor cores
+ * instead, against x split per 128-column block into four E4M3 pieces
+ * (an element to 2^-16 of itself or 2^-29 of the block's largest |x|).
+ * Non-finite results are recomputed element by element, so NaN and Inf
+ * follow the formula above.
  *
  *   w      [R, C] E4M3 bytes, R >= 0, C >= 1
  *   scale  [SR, SC] E8M0 bytes, 1 <= SR <= max(R, 1), 1 <= SC <= C
@@ -498,6 +504,20 @@ QMV_API qmv_status i8_matvec_topk_sample(const int8_t *w, int64_t R, int64_t C,
                                          int64_t *top_index, float *top_value, float *top_prob,
                                          int64_t *token, void *workspace,
                                          int64_t workspace_bytes, qmv_stream stream);
+
+/*
+ * qmv_tc_wait_timeouts -- how many waits of the fifth-generation tensor-core
+ * F8 kernel (f8_matvec and its argmax / top-k forms at batch 5..8) have run
+ * out of their one-second limit on the current device since the library was
+ * loaded.  A wait that runs out ends its part of the kernel early and the
+ * outputs of that call are not valid.  None is expected; the limit exists so
+ * that a fault elsewhere cannot leave the kernel waiting forever.
+ *
+ *   count  host pointer, written
+ *
+ * Synchronous: a device-to-host copy on the legacy default stream.
+ */
+QMV_API qmv_status qmv_tc_wait_timeouts(uint64_t *count);
 
 /* Human-readable name of a status code (static storage). */
 QMV_API const char *qmv_status_string(qmv_status status);

@@ -1,0 +1,571 @@
+// f8_tc_kernels.cu -- block-scaled F8 E4M3 matvec at batch 5..8 on the
+// fifth-generation tensor cores (tcgen05.mma kind::f8f6f4, accumulators in
+// tensor memory, weights streamed by TMA), for sm_103a.
+//
+// Method: ds4f-disk issue #6 "attention + tokenizer + sampling", work item 1
+// and step 1 (the F8 E4M3 + E8M0 matvec), work item 3 (the ~246k x 4096 head)
+// and step 3 (greedy selection on the head).
+//
+//   y[v][r] = sum_c E4M3(w[r][c]) * E8M0(scale[r*SR/R][c*SC/C]) * x[v][c]
+//
+// Orientation.  A tcgen05.mma costs about the same whatever its N (16 .. 256),
+// so the weights go in as the wide operand: N = 256 weight rows of one tile,
+// read by the tensor core straight from the TMA ring as raw E4M3 bytes (no
+// decode on the CUDA cores).  The activations are the M = 128 operand, of
+// which 32 rows are used: vector v's piece p sits in row 4v + p.
+//
+// Pieces.  Per vector v and 128-column block kb, with m the largest finite |x|
+// there and E = 7 - floor(log2 m), x * 2^E lies below 256 and is split into four
+// E4M3 pieces: piece 0 = E4M3(x 2^E), and piece p + 1 = E4M3 of 16 times the
+// residual left by pieces 0..p.  Each piece keeps 4 significant bits of what is
+// left, so the four carry x to 2^-16 relative (to an absolute 2^-22 of the
+// block's scaled maximum below the E4M3 normal range), and x * 2^E = sum_p
+// piece_p * 2^-4p.  E4M3 x E4M3 products are exact in the float32 accumulator.
+//
+// Scales.  Every 128-column block must lie in one scale column block and
+// every 64-row unit in one scale row (each scale block starts on a multiple of
+// 128 columns and of 64 rows), so within a tile's unit the factor
+// 2^(s - 127) * 2^-(E + 4p) of accumulator row 4v + p and block kb is one
+// power of two.  Each block gets a fresh accumulator D (4 MMAs of K = 32); the
+// epilogue warps read D back (tcgen05.ld), multiply row 4v + p by its factor
+// and add into registers.  At the end of a tile the 4 pieces of each vector
+// (lanes 4v .. 4v + 3) are summed with two shuffles.
+//
+// Warps (512 threads, one block per SM): warp 1 issues the TMA copies (lane
+// 0), warp 2 issues the MMAs (lane 0) and owns the tensor memory, warps 0, 4,
+// 8 and 12 (the warps that may read TMEM lanes 0..31) are the epilogue, and
+// every warp but warp 1 first builds the activation pieces, block by block,
+// each block announced on its own mbarrier so the MMAs start on block 0 at
+// once.  A block's rows are 64-row units [u0, u1) of the matrix, in tiles of
+// up to four units; the TMA loads one 64-row box per unit, so a short last
+// tile costs only its own rows.
+//
+// Memory.  Shared: the pieces of all of K (32 rows x C bytes), a ring of three
+// 32 KB weight stages (256 rows x 128 bytes, 128-byte swizzle), the scale
+// column of every block, the block exponents and the barriers -- 226 KB at C =
+// 4096.  Tensor memory: two 256-column accumulators.
+//
+// Fix-up.  A result that is not finite (an E4M3 code 0x7F / 0xFF, which the
+// tensor core reads as NaN; a NaN scale; Inf or NaN in x, which marks its
+// block; an overflow) is recomputed by the exact per-element path, which gives
+// those inputs their per-element meaning.
+//
+// Waits.  Every mbarrier wait gives up after one second (%globaltimer): the
+// role then stops, its results are not valid, and the library's count of
+// abandoned waits (qmv_tc_wait_timeouts) goes up.  No wait is expected to
+// run out; the limit keeps a fault elsewhere from hanging the GPU.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "f8_common.cuh"
+
+namespace qmv {
+namespace f8 {
+
+// Waits abandoned after their time limit, summed over all calls (read by
+// qmv_tc_wait_timeouts).
+__device__ unsigned long long g_tc_timeouts = 0;
+
+namespace {
+
+constexpr int kTcThreads = 512;
+constexpr int kTcRows = 256, kTcUnit = 64, kTcChunk = 128;       // tile rows, unit rows, K-block columns
+constexpr int kTcStageBytes = kTcRows * kTcChunk;                // 32 KB: one tile x one K-block
+constexpr int kTcUnitBytes = kTcUnit * kTcChunk;                 // 8 KB: one TMA box
+constexpr int kTcStages = 3;
+constexpr int kTcND = 2;                                         // accumulators of 256 columns
+constexpr int kTcTmemCols = 512;
+constexpr int kTcPieces = 4;
+constexpr int kTcMaxJobs = 3;                                    // K-blocks per building warp
+constexpr int kTcBuildWarps = kTcThreads / 32 - 1;               // every warp but the TMA one
+constexpr int kTcMaxBlocks = kTcMaxJobs * kTcBuildWarps;         // 45 K-blocks: C <= 5760
+constexpr int kWTma = 1, kWMma = 2;                              // epilogue: warps 0, 4, 8, 12
+constexpr int kEZero = 100000, kENonFinite = 100001;             // block exponent markers
+constexpr uint64_t kWaitNs = 1000000000ull;                      // one second
+
+__host__ __device__ inline size_t tc_smem_bytes(int64_t C) {
+    const int64_t nkb = C / kTcChunk;
+    return size_t(1024                                  // alignment of the base to 1024
+                  + nkb * 4096                          // pieces: 32 rows x 128 bytes per block
+                  + int64_t(kTcStages) * kTcStageBytes  // weight ring
+                  + nkb * 4 + nkb * 32                  // scale columns, block exponents
+                  + 8 * (2 * kTcStages + 2 * kTcND + 1 + nkb) + 16);  // barriers, TMEM address
+}
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return uint32_t(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __noinline__ bool bar_wait_slow(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    while (true) {
+        for (int i = 0; i < 64; i++)
+            if (bar_try(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) {
+            atomicAdd(&g_tc_timeouts, 1ull);
+            return false;
+        }
+    }
+}
+// Waits for the phase of `bar` with this parity; false after the time limit.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+    return bar_try(bar, parity) || bar_wait_slow(bar, parity);
+}
+__device__ __forceinline__ void bar_init(uint32_t bar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+    asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+// One 64-row x 128-byte box of the weights (x = column byte, y = row).
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// D (tmem) [+]= A (smem) x B (smem), E4M3 operands, float32 accumulator.
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+// Shared-memory operand descriptors (sm_100 format: start, leading and
+// stride byte offsets >> 4, version 1 at bit 46, layout at bits 61..63).
+// Pieces: no swizzle, K-major, 8-row x 16-byte cores; K-adjacent cores 512
+// bytes apart, M-adjacent 128 bytes apart.  Rows 32..127 of the M = 128
+// operand read the next cores (unused accumulator rows).
+__device__ __forceinline__ uint64_t piece_desc(uint32_t saddr) {
+    return uint64_t((saddr & 0x3FFFF) >> 4) | (uint64_t(512 >> 4) << 16) | (uint64_t(128 >> 4) << 32) |
+           (uint64_t(1) << 46);
+}
+// Weights: 128-byte swizzle, K-major (rows of 128 bytes, 8-row groups 1024
+// bytes apart), as the TMA writes them.
+__device__ __forceinline__ uint64_t weight_desc(uint32_t saddr) {
+    return uint64_t((saddr & 0x3FFFF) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) |
+           (uint64_t(2) << 61);
+}
+// Instruction descriptor: float32 D, E4M3 A and B (both K-major), N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(256 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+
+// Two floats -> an E4M3 pair, rounded to nearest even (`a` in the low byte).
+__device__ __forceinline__ uint32_t to_e4m3x2(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+__device__ __forceinline__ float2 from_e4m3x2(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<unsigned short>(two)));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+}
+
+// 2^(s - 127) * 2^-(E + 4p) as float32 (a power of two; 0 below 2^-149, Inf
+// above float range, NaN for a NaN scale or a non-finite block).
+__device__ __forceinline__ float block_factor(unsigned s, int E, int p) {
+    if (E == kENonFinite || s == 255u) return __uint_as_float(0x7fc00000u);
+    if (E == kEZero) return 0.0f;
+    const int ex = int(s) - 127 - E - 4 * p;
+    return ex > 127 ? __uint_as_float(0x7f800000u)
+         : ex >= -126 ? __uint_as_float(uint32_t(ex + 127) << 23)
+         : ex >= -149 ? __uint_as_float(1u << (ex + 149)) : 0.0f;
+}
+
+template <bool AM>
+__global__ void __launch_bounds__(kTcThreads, 1) f8_tc_kernel(const __grid_constant__ CUtensorMap wmap, F8Args a, int batch) {
+    extern __shared__ unsigned char tc_smem[];
+    const uint32_t raw0 = smem_u32(tc_smem);
+    const uint32_t base = (raw0 + 1023u) & ~1023u;
+    unsigned char *sm = tc_smem + (base - raw0);
+    const int nkb = int(a.C / kTcChunk);
+    const uint32_t s_ring = base + uint32_t(nkb) * 4096;  // the pieces' unused rows read into it
+    int *cbk = reinterpret_cast<int *>(sm + (s_ring - base) + kTcStages * kTcStageBytes);
+    int *eb = cbk + nkb;  // [kb][8] block exponents
+    const uint32_t s_bars = (smem_u32(eb + nkb * 8) + 7u) & ~7u;
+    const uint32_t full0 = s_bars, empty0 = full0 + 8 * kTcStages, dfull0 = empty0 + 8 * kTcStages,
+                   dempty0 = dfull0 + 8 * kTcND, done_bar = dempty0 + 8 * kTcND, ready0 = done_bar + 8;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + (ready0 + 8 * nkb - base));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t units = (a.R + kTcUnit - 1) / kTcUnit;
+    const int64_t u0 = int64_t(blockIdx.x) * units / gridDim.x, u1 = int64_t(blockIdx.x + 1) * units / gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTcStages; i++) {
+            bar_init(full0 + 8 * i, 1);
+            bar_init(empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < kTcND; i++) {
+            bar_init(dfull0 + 8 * i, 1);
+            bar_init(dempty0 + 8 * i, 4);
+        }
+        bar_init(done_bar, 1);
+        for (int i = 0; i < nkb; i++) bar_init(ready0 + 8 * i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kWMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(kTcTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    for (int kb = threadIdx.x; kb < nkb; kb += blockDim.x) cbk[kb] = int((int64_t(kb) * kTcChunk * a.SC) / a.C);
+    pdl_trigger();
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = *tmem_holder;
+
+    float best_v = -INFINITY;  // argmax: the best of this thread's rows (lanes 4v of the epilogue warps)
+    int64_t best_i = INT64_MAX;
+
+    if (warp == kWTma) {
+        // ---- producer: stage g holds K-block kb of the tile's units, one box per unit.
+        // The weights are read-only for the library's calls, so the copies start
+        // before the dependency wait.
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+            uint32_t g = 0;
+            bool ok = true;
+            for (int64_t ut = u0; ut < u1 && ok; ut += 4) {
+                const int nu = int(min(int64_t(4), u1 - ut));
+                for (int kb = 0; kb < nkb; kb++, g++) {
+                    const uint32_t s = g % kTcStages, u = g / kTcStages;
+                    if (u > 0 && !bar_wait(empty0 + 8 * s, (u - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    bar_expect_tx(full0 + 8 * s, uint32_t(nu * kTcUnitBytes));
+                    for (int i = 0; i < nu; i++)
+                        tma_load(s_ring + s * kTcStageBytes + i * kTcUnitBytes, &wmap, kb * kTcChunk,
+                                 int((ut + i) * kTcUnit), full0 + 8 * s);
+                }
+            }
+            // the copies still in flight land before the block can exit
+            for (uint32_t k = g > uint32_t(kTcStages) ? g - kTcStages : 0; k < g; k++)
+                bar_wait(full0 + 8 * (k % kTcStages), (k / kTcStages) & 1);
+        }
+        __syncwarp();
+        pdl_wait();  // (the argmax completion below reads other blocks' results)
+    } else {
+        pdl_wait();
+        // ---- activation pieces, K-block by K-block: lane (v = lane % 8, q = lane / 8) of the
+        // warp that owns block kb handles its 16-column cores q and q + 4 of vector v.  Pieces
+        // of vector v go to rows 4v .. 4v + 3; vectors past the batch are zero.
+        {
+            const int wi = warp < kWTma ? warp : warp - 1;
+            const int v = lane & 7, q = lane >> 3;
+            float4 xs[kTcMaxJobs][8];
+#pragma unroll
+            for (int jj = 0; jj < kTcMaxJobs; jj++) {
+                const int kb = wi + jj * kTcBuildWarps;
+#pragma unroll
+                for (int h = 0; h < 2; h++)
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        xs[jj][4 * h + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (kb < nkb && v < batch)
+                            xs[jj][4 * h + i] = __ldg(reinterpret_cast<const float4 *>(
+                                                          a.x + int64_t(v) * a.C + int64_t(kb) * kTcChunk + (q + 4 * h) * 16) + i);
+                    }
+            }
+#pragma unroll
+            for (int jj = 0; jj < kTcMaxJobs; jj++) {
+                const int kb = wi + jj * kTcBuildWarps;
+                if (kb >= nkb) break;  // warp-uniform
+                float r[32];
+                bool fin = true;
+                float m = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const float4 t = xs[jj][i];
+                    r[4 * i] = t.x;
+                    r[4 * i + 1] = t.y;
+                    r[4 * i + 2] = t.z;
+                    r[4 * i + 3] = t.w;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    const bool f = isfinite(r[i]);
+                    fin &= f;
+                    if (!f) r[i] = 0.f;
+                    m = fmaxf(m, fabsf(r[i]));
+                }
+                m = fmaxf(m, __shfl_xor_sync(kFull, m, 8));
+                m = fmaxf(m, __shfl_xor_sync(kFull, m, 16));
+                const int E = m > 0.f ? 7 - ilogbf(m) : kEZero;  // in [-120, 156]
+                if (m > 0.f) {
+                    const int E1 = E > 127 ? 127 : E, E2 = E - E1;  // x * 2^E in two exact steps
+                    const float f1 = __uint_as_float(uint32_t(127 + E1) << 23),
+                                f2 = __uint_as_float(uint32_t(127 + E2) << 23);
+#pragma unroll
+                    for (int i = 0; i < 32; i++) r[i] = r[i] * f1 * f2;
+                }
+                const uint32_t kc0 = uint32_t(kb * 8 + q);  // the lane's first 16-column core
+#pragma unroll
+                for (int pc = 0; pc < kTcPieces; pc++) {
+                    uint32_t wv[8];
+#pragma unroll
+                    for (int i = 0; i < 16; i++) {
+                        const uint32_t two = to_e4m3x2(r[2 * i], r[2 * i + 1]);
+                        if (i & 1) wv[i >> 1] |= two << 16;
+                        else wv[i >> 1] = two;
+                        if (pc + 1 < kTcPieces) {  // the residual, times 16 (exact)
+                            const float2 qv = from_e4m3x2(two);
+                            r[2 * i] = (r[2 * i] - qv.x) * 16.f;
+                            r[2 * i + 1] = (r[2 * i + 1] - qv.y) * 16.f;
+                        }
+                    }
+                    const int mrow = 4 * v + pc;
+                    const uint32_t roff = uint32_t(mrow >> 3) * 128 + uint32_t(mrow & 7) * 16;
+                    *reinterpret_cast<uint4 *>(sm + kc0 * 512 + roff) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    *reinterpret_cast<uint4 *>(sm + (kc0 + 4) * 512 + roff) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+                }
+                const unsigned bad = __ballot_sync(kFull, !fin);  // lanes v, v+8, v+16, v+24 hold vector v
+                if (q == 0) eb[kb * 8 + v] = ((bad >> v) & 0x01010101u) ? kENonFinite : E;
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // pieces -> tensor core reads
+                __syncwarp();
+                if (lane == 0) bar_arrive(ready0 + 8 * kb);
+            }
+        }
+
+        if (warp == kWMma) {
+            // ---- MMA issuer: per stage, four K = 32 steps into a fresh accumulator
+            if (lane == 0) {
+                uint32_t g = 0;
+                bool ok = true;
+                for (int64_t ut = u0; ut < u1 && ok; ut += 4)
+                    for (int kb = 0; kb < nkb; kb++, g++) {
+                        const uint32_t s = g % kTcStages, u = g / kTcStages, d = g % kTcND, ud = g / kTcND;
+                        if ((ut == u0 && !bar_wait(ready0 + 8 * kb, 0)) || !bar_wait(full0 + 8 * s, u & 1) ||
+                            (ud > 0 && !bar_wait(dempty0 + 8 * d, (ud - 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; kk++)
+                            tc_mma(tmem + d * 256, piece_desc(base + uint32_t(kb * 8 + kk * 2) * 512),
+                                   weight_desc(s_ring + s * kTcStageBytes + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
+                        tc_commit(dfull0 + 8 * d);  // the accumulator is ready ...
+                        tc_commit(empty0 + 8 * s);  // ... and the stage free, once these MMAs are done
+                    }
+                tc_commit(done_bar);
+                bar_wait(done_bar, 0);
+            }
+            __syncwarp();
+        } else if ((warp & 3) == 0) {
+            // ---- epilogue: warp e reads accumulator columns 64e .. 64e + 63 (unit e of the tile)
+            const int e = warp >> 2;
+            const int v = lane >> 2, p = lane & 3;
+            uint32_t g = 0;
+            bool ok = true;
+            for (int64_t ut = u0; ut < u1 && ok; ut += 4) {
+                const bool mine = ut + e < u1;
+                const int64_t r0 = (ut + e) * kTcUnit;
+                const int64_t srow = mine ? (r0 * a.SR / a.R) * a.SC : 0;
+                float acc[64];
+#pragma unroll
+                for (int j = 0; j < 64; j++) acc[j] = 0.f;
+                for (int kb = 0; kb < nkb; kb++, g++) {
+                    const uint32_t d = g % kTcND, ud = g / kTcND;
+                    // every lane waits; the warp goes on only if all of them saw the phase
+                    const bool seen = bar_wait(dfull0 + 8 * d, ud & 1) && (ut != u0 || bar_wait(ready0 + 8 * kb, 0));
+                    if (!__all_sync(kFull, seen)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_after();
+                    const float fs = (mine && v < batch) ? block_factor(__ldg(a.scale + srow + cbk[kb]), eb[kb * 8 + v], p) : 0.f;
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        uint32_t dv[32];
+                        tc_ld32(tmem + d * 256 + 64 * e + 32 * h, dv);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                        for (int j = 0; j < 32; j++) acc[32 * h + j] = fmaf(__uint_as_float(dv[j]), fs, acc[32 * h + j]);
+                    }
+                    tc_before();
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(dempty0 + 8 * d);
+                }
+                if (!ok || !mine) continue;  // warp-uniform
+#pragma unroll
+                for (int j = 0; j < 64; j++) {
+                    acc[j] += __shfl_xor_sync(kFull, acc[j], 1);
+                    acc[j] += __shfl_xor_sync(kFull, acc[j], 2);
+                }
+                const bool owner = p == 0 && v < batch;
+                const int nr = int(min(int64_t(kTcUnit), a.R - r0));
+                // results that are not finite take the exact per-element path (warp-collective)
+#pragma unroll
+                for (int j = 0; j < 64; j++) {
+                    unsigned bad = __ballot_sync(kFull, owner && j < nr && !isfinite(acc[j]));
+                    while (bad) {
+                        const int bl = __ffs(bad) - 1;
+                        bad &= bad - 1;
+                        const float ex = f8_row_exact(a, r0 + j, bl >> 2, nullptr);
+                        if (lane == bl) acc[j] = ex;
+                    }
+                }
+                if (owner) {
+                    float *yr = a.y ? a.y + int64_t(v) * a.R + r0 : nullptr;
+#pragma unroll
+                    for (int j = 0; j < 64; j++) {
+                        if (j < nr) {
+                            if (yr) yr[j] = acc[j];
+                            if (AM && arg_better(acc[j], r0 + j, best_v, best_i)) {
+                                best_v = acc[j];
+                                best_i = r0 + j;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_before();
+    __syncthreads();
+    if (warp == kWMma) {
+        tc_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols));
+    }
+    if (AM) {
+        // the block's best per vector from the four epilogue warps (the ring is idle now)
+        ArgBest *wb = reinterpret_cast<ArgBest *>(sm + (s_ring - base));  // [4][8]
+        if ((warp & 3) == 0 && (lane & 3) == 0) {
+            ArgBest r;
+            r.v = best_v;
+            r.pad = 0;
+            r.i = best_i;
+            wb[(warp >> 2) * 8 + (lane >> 2)] = r;
+        }
+        __syncthreads();
+        if (int(threadIdx.x) < batch) {
+            const int k = threadIdx.x;
+            float bv = wb[k].v;
+            int64_t bi = wb[k].i;
+            for (int w2 = 1; w2 < 4; w2++)
+                if (arg_better(wb[w2 * 8 + k].v, wb[w2 * 8 + k].i, bv, bi)) {
+                    bv = wb[w2 * 8 + k].v;
+                    bi = wb[w2 * 8 + k].i;
+                }
+            ArgBest r;
+            r.v = bv;
+            r.pad = 0;
+            r.i = bi;
+            a.ws[int64_t(blockIdx.x) * batch + k] = r;
+        }
+        argmax_complete(a, batch, sm + (s_ring - base) + 1024);
+    }
+}
+
+// ---- host ---------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, fetched through the runtime (no link against the
+// driver library); NULL when the driver does not offer it.
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// The weights as a 2-D tensor of bytes [R][C], read in 64-row x 128-byte
+// boxes with the 128-byte swizzle the MMA descriptors expect.
+bool weight_map(const F8Args &a, CUtensorMap &map) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(a.C), cuuint64_t(a.R)};
+    const cuuint64_t strides[1] = {cuuint64_t(a.C)};
+    const cuuint32_t box[2] = {kTcChunk, kTcUnit};
+    const cuuint32_t elem[2] = {1, 1};
+    return enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.w), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_fits(const F8Args &a, int batch) {
+    if (batch < 5 || batch > 8 || a.R < 1 || a.R > (int64_t(1) << 31) - 1) return false;
+    if (a.C % kTcChunk != 0 || a.C / kTcChunk > kTcMaxBlocks) return false;
+    if (tc_smem_bytes(a.C) > size_t(227) * 1024) return false;
+    if (reinterpret_cast<uintptr_t>(a.w) % 16 != 0 || reinterpret_cast<uintptr_t>(a.x) % 16 != 0) return false;
+    // every 64-row unit inside one scale row, every 128-column block inside one scale column block
+    if (!chunks_uniform(a.R, a.SR, kTcUnit) || !chunks_uniform(a.C, a.SC, kTcChunk)) return false;
+    return encode_tiled() != nullptr;
+}
+
+qmv_status launch_tc(const F8Args &a, int batch, bool am, cudaStream_t s, int &blocks_out) {
+    CUtensorMap map;
+    if (!weight_map(a, map)) return QMV_ERR_CUDA;
+    const size_t smem = tc_smem_bytes(a.C);
+    const int64_t units = (a.R + kTcUnit - 1) / kTcUnit;
+    int64_t blocks = sm_count();
+    if (blocks > units) blocks = units;
+    if (am && blocks > QMV_ARGMAX_MAX_BLOCKS) blocks = QMV_ARGMAX_MAX_BLOCKS;
+    blocks_out = int(blocks);
+    if (am) {
+        auto kern = f8_tc_kernel<true>;
+        if (!allow_smem(reinterpret_cast<const void *>(kern), smem)) return QMV_ERR_CUDA;
+        return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(kTcThreads), smem, s, map, a, batch));
+    }
+    auto kern = f8_tc_kernel<false>;
+    if (!allow_smem(reinterpret_cast<const void *>(kern), smem)) return QMV_ERR_CUDA;
+    return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(kTcThreads), smem, s, map, a, batch));
+}
+
+qmv_status tc_wait_timeouts(unsigned long long *count) {
+    return from_cuda(cudaMemcpyFromSymbol(count, g_tc_timeouts, sizeof(*count)));
+}
+
+}  // namespace f8
+
+qmv_status f8_tc_wait_timeouts(unsigned long long *count) { return f8::tc_wait_timeouts(count); }
+
+}  // namespace qmv

@@ -545,4 +545,12 @@ qmv_status i8_matvec_topk_sample(const int8_t *w, int64_t R, int64_t C, const ui
                                    token, workspace, s);
 }
 
+qmv_status qmv_tc_wait_timeouts(uint64_t *count) {
+    if (!count) return QMV_ERR_NULL;
+    unsigned long long c = 0;
+    const qmv_status st = qmv::f8_tc_wait_timeouts(&c);
+    if (st == QMV_OK) *count = uint64_t(c);
+    return st;
+}
+
 }  // extern "C"

@@ -104,6 +104,8 @@ def load() -> ctypes.CDLL:
     lib.qmv_status_string.restype = ctypes.c_char_p
     lib.qmv_abi_version.argtypes = []
     lib.qmv_abi_version.restype = I32
+    lib.qmv_tc_wait_timeouts.argtypes = [P]
+    lib.qmv_tc_wait_timeouts.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -114,6 +116,14 @@ def status_string(status: int) -> str:
 
 def abi_version() -> int:
     return int(load().qmv_abi_version())
+
+
+def tc_wait_timeouts() -> int:
+    """Waits of the fifth-generation tensor-core F8 kernel that ran out of
+    their one-second limit on the current device (none, normally)."""
+    out = ctypes.c_uint64(0)
+    _check(load().qmv_tc_wait_timeouts(ctypes.addressof(out)), "qmv_tc_wait_timeouts")
+    return int(out.value)
 
 
 # --------------------------------------------------------------------------

@@ -30,7 +30,8 @@ def test_header_declares_every_entry_point():
     for n in ("cq_prepare", "cq_matvec", "cq_dequantize_row", "f8_matvec", "f8_matvec_argmax",
               "cq_matvec_multi", "cq_prepare_matvec", "i8_matvec", "hadamard_mlp",
               "topk_sample", "f8_matvec_topk_sample", "i8_matvec_topk_sample",
-              "i8_quantize_x", "i8_matvec_q8", "qmv_status_string", "qmv_abi_version"):
+              "i8_quantize_x", "i8_matvec_q8", "qmv_status_string", "qmv_abi_version",
+              "qmv_tc_wait_timeouts"):
         assert n in names
 
 
@@ -98,6 +99,11 @@ def test_cq_batch_null_align_alias():
     assert qmv.cq_dequantize_row(m, FAKE + 2, 3, FAKE + 65536) == 6
     # empty matrix: valid, nothing launched
     assert qmv.cq_matvec(_m(output=0), FAKE, 1, FAKE + 65536) == 0
+
+
+def test_tc_wait_timeouts_rejects_null():
+    # checked before any CUDA call, so it runs without a GPU
+    assert qmv.load().qmv_tc_wait_timeouts(0) == 1
 
 
 def test_f8_rejections():

@@ -1,0 +1,243 @@
+"""GPU parity of the fifth-generation tensor-core F8 kernel (batch 5..8).
+
+f8_matvec at batch 5..8 goes to tcgen05.mma kind::f8f6f4 when C is a multiple
+of 128 up to 4096, every scale block starts on a multiple of 128 columns and
+64 rows, and w and x are 16-byte aligned: the raw E4M3 weights are the wide
+MMA operand (TMA-streamed, 128-byte swizzle) and x enters as four E4M3 pieces
+per 128-column block.  The bar is the matvec tolerance of ds4f-disk issue #6
+step 1's definition, |y - y_oracle| <= 1e-4 * sum_c |w * s * x| + 1e-6, against
+the float64 oracle.
+
+Cases: every batch 5..8; a ragged last 64-row unit; 64-row scale blocks; one
+128-column block; blocks with unequal numbers of units (and short last
+tiles); activations with a wide dynamic range inside a block, huge, tiny,
+subnormal and zero; Inf / NaN in x; saturated E4M3 codes and NaN scales;
+subnormal and large scales; integer inputs, where the result is exact; the
+fused argmax and top-k forms; determinism; that this kernel is the one
+launched, that shapes outside its conditions go elsewhere, and that none of
+its waits ran out of time.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_weight_matvec_gb300 import qmv, synth
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-4, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qmv.load()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run(f, x=None):
+    x = f.x if x is None else x
+    y = qmv.f8_matvec_t(dev(f.w), dev(f.scale), dev(x))
+    torch.cuda.synchronize()
+    return y.cpu().numpy().astype(np.float64)
+
+
+def check(f, abs_tol=ABS):
+    y = run(f)
+    ref, mag = oracle.f8_matvec(f.w, f.scale, f.x, threads=8)
+    with np.errstate(invalid="ignore"):  # inf - inf where both sides are infinite
+        ok = (np.isnan(y) & np.isnan(ref)) | (y == ref) | (np.abs(y - ref) <= REL * mag + abs_tol)
+    if not ok.all():
+        i = tuple(np.argwhere(~ok)[0])
+        raise AssertionError("mismatch at %s: gpu %r oracle %r bound %r (%d bad)" % (
+            i, y[i], ref[i], REL * mag[i] + abs_tol, int((~ok).sum())))
+    return y
+
+
+def kernel_names(fn):
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    names = []
+    for _ in range(2):  # the first profiling session of a process may record nothing
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+        if names:
+            break
+    if not names:
+        pytest.skip("the profiler recorded no kernels on this box")
+    return names
+
+
+@pytest.mark.parametrize("batch", [5, 6, 7, 8])
+@pytest.mark.parametrize("R,C,SR,SC", [
+    (1000, 4096, 1, 32),     # ragged last unit (1000 = 15 * 64 + 40)
+    (1024, 2048, 8, 16),     # 128-row x 128-column scale blocks
+    (640, 1024, 10, 8),      # 64-row scale blocks: every unit its own scale row
+    (129, 128, 1, 1),        # one 128-column block, one row past a unit
+    (5000, 4096, 1, 32),     # 79 units over the grid: unequal numbers, short last tiles
+    (2112, 3968, 33, 31)])   # 31 blocks of 128 columns, 64-row scale blocks
+def test_tc_shapes(batch, R, C, SR, SC):
+    check(synth.f8_inputs(R * 5 + C + batch, R, C, SR, SC, 112, 140, batch=batch))
+
+
+def test_tc_wide_dynamic_range_inside_blocks():
+    """x spans six decades inside every 128-column block."""
+    f = synth.f8_inputs(71, 3072, 2048, 24, 16, 118, 132, batch=8)
+    rng = np.random.default_rng(71)
+    f.x = (f.x * (10.0 ** rng.uniform(-3, 3, f.x.shape))).astype(np.float32)
+    check(f)
+
+
+def test_tc_one_large_element_per_block():
+    """One element per block 2^20 times the rest: the others keep 2^-29 of it."""
+    f = synth.f8_inputs(72, 1024, 1024, 8, 8, 120, 134, batch=6)
+    f.x[:, ::128] *= np.float32(2.0 ** 20)
+    check(f)
+
+
+@pytest.mark.parametrize("mult", [1e30, 1e-30, 1e-40, 0.0])
+def test_tc_extreme_magnitudes(mult):
+    """Huge, tiny and subnormal activations, and all-zero blocks: the relative
+    bound holds without the absolute term."""
+    f = synth.f8_inputs(73, 768, 1024, 6, 8, 120, 134, batch=5)
+    f.x = (f.x * np.float32(mult)).astype(np.float32)
+    f.x[1, 128:384] = 0.0  # two all-zero column blocks
+    y = run(f)
+    ref, mag = oracle.f8_matvec(f.w, f.scale, f.x, threads=8)
+    assert np.all(np.abs(y - ref) <= REL * mag), "relative bound without the absolute term"
+    if mult == 0.0:
+        assert not y.any()
+
+
+def test_tc_subnormal_scales_and_large_exponents():
+    f = synth.f8_inputs(74, 256, 1024, 4, 8, 0, 190, batch=7)
+    check(f)
+
+
+def test_tc_nonfinite_x():
+    f = synth.f8_inputs(75, 896, 1024, 7, 8, 118, 132, batch=6)
+    f.x[0, 37] = np.inf
+    f.x[1, 700] = np.nan
+    f.x[2, 5] = -np.inf
+    f.x[2, 6] = np.inf
+    y = check(f)
+    assert np.isnan(y[1]).all()
+    assert np.isinf(y[0]).any()
+    assert not np.isfinite(y[2]).any()
+    assert np.isfinite(y[3:]).all()
+
+
+def test_tc_saturated_codes_and_nan_scale():
+    f = synth.f8_inputs(76, 512, 4096, 8, 32, 120, 130, batch=8, finite_only=False)
+    assert (f.w == 0x7F).any() and (f.w == 0xFF).any()
+    check(f)
+    f.scale[3, 5] = 255
+    y = check(f)
+    rows_with_nan = np.nonzero((np.arange(512) * 8) // 512 == 3)[0]
+    assert np.isnan(y[:, rows_with_nan]).all()
+    assert not np.isnan(np.delete(y, rows_with_nan, axis=1)).any()
+
+
+def test_tc_integer_inputs_are_exact():
+    """Integer weights (E4M3 codes of 0, +-1, +-2, 3, 4), integer x in [-8, 8]
+    and unit scales: every partial sum is an integer below 2^24 and every x
+    is exact in its first E4M3 piece, so the result equals the float64 oracle
+    exactly."""
+    rng = np.random.default_rng(77)
+    codes = np.array([0x00, 0x38, 0x40, 0x44, 0x48, 0xB8, 0xC0], np.uint8)
+    R, C = 1536, 2048
+    f = synth.F8Inputs(R, C, 4, 16, codes[rng.integers(0, len(codes), (R, C))],
+                       np.full((4, 16), 127, np.uint8),
+                       rng.integers(-8, 9, (8, C)).astype(np.float32))
+    y = run(f)
+    ref, _ = oracle.f8_matvec(f.w, f.scale, f.x, threads=8)
+    assert np.array_equal(y, ref)
+
+
+def test_tc_deterministic_and_writes_only_its_outputs():
+    f = synth.f8_inputs(78, 2049, 4096, 1, 32, 118, 132, batch=7)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    buf = torch.full((7 * 2049 + 64,), float("nan"), device="cuda")
+    buf[7 * 2049:] = 3.5
+    out = buf[:7 * 2049].view(7, 2049)
+    qmv.f8_matvec_t(w, s, x, out=out)
+    torch.cuda.synchronize()
+    a = out.clone()
+    qmv.f8_matvec_t(w, s, x, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), out.view(torch.int32))
+    assert not torch.isnan(a).any() and bool((buf[7 * 2049:] == 3.5).all())
+
+
+@pytest.mark.parametrize("batch", [5, 8])
+def test_tc_argmax_matches_its_matvec(batch):
+    """The fused greedy form: y bit for bit the plain call's, within
+    tolerance of the oracle; the index is the greedy choice over that y."""
+    f = synth.f8_inputs(79 + batch, 3000, 4096, 1, 32, 118, 132, batch=batch)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    y_buf = torch.empty((batch, f.R), dtype=torch.float32, device="cuda")
+    idx, val = qmv.f8_matvec_argmax_t(w, s, x, y=y_buf)
+    y_plain = qmv.f8_matvec_t(w, s, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y_buf.view(torch.int32), y_plain.view(torch.int32))
+    y = y_buf.cpu().numpy()
+    ref, mag = oracle.f8_matvec(f.w, f.scale, f.x, threads=8)
+    assert np.all(np.abs(y - ref) <= REL * mag + ABS)
+    idx = idx.cpu().numpy()
+    assert np.array_equal(idx, oracle.argmax_rows(y))
+    assert np.array_equal(val.cpu().numpy().view(np.uint32), y[np.arange(batch), idx].view(np.uint32))
+    # without y, the same choice
+    idx2, _ = qmv.f8_matvec_argmax_t(w, s, x)
+    assert np.array_equal(idx2.cpu().numpy(), idx)
+
+
+def test_tc_argmax_nan_and_ties():
+    """A NaN result wins the greedy choice; among equal values the lower row."""
+    f = synth.f8_inputs(81, 1024, 1024, 1, 8, 120, 128, batch=6)
+    f.x[2, 10] = np.nan
+    f.w[700] = f.w[300]
+    f.x[4] = 0.0
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    idx, _ = qmv.f8_matvec_argmax_t(w, s, x)
+    y = qmv.f8_matvec_t(w, s, x)
+    torch.cuda.synchronize()
+    idx, y = idx.cpu().numpy(), y.cpu().numpy()
+    assert np.array_equal(idx, oracle.argmax_rows(y))
+    assert idx[4] == 0  # all zero: the first row
+
+
+def test_tc_topk_sample_over_its_matvec():
+    f = synth.f8_inputs(82, 4096, 2048, 1, 16, 118, 132, batch=8)
+    u = np.random.default_rng(82).random(8).astype(np.float32)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    y, idx, val, _, _ = qmv.f8_matvec_topk_sample_t(w, s, x, 64, 1.0, dev(u))
+    y = y.cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), qmv.f8_matvec_t(w, s, x).cpu().numpy().view(np.uint32))
+    ref_idx, _, _ = oracle.topk_sample(y, 64, 1.0, u)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+
+
+def test_tc_kernel_is_the_one_launched():
+    f = synth.f8_inputs(83, 512, 1024, 1, 8, 118, 132, batch=8)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    names = kernel_names(lambda: qmv.f8_matvec_t(w, s, x))
+    assert any("f8_tc" in n for n in names), names
+    # batch 4, and rows whose scale blocks start off a 64-row boundary, stay on mma.sync
+    names = kernel_names(lambda: qmv.f8_matvec_t(w, s, x[:4]))
+    assert not any("f8_tc" in n for n in names) and any("f8_mma" in n for n in names), names
+    g = synth.f8_inputs(84, 1000, 1024, 8, 8, 118, 132, batch=8)  # scale rows of 125
+    gw, gs, gx = dev(g.w), dev(g.scale), dev(g.x)
+    names = kernel_names(lambda: qmv.f8_matvec_t(gw, gs, gx))
+    assert not any("f8_tc" in n for n in names), names
+
+
+def test_zz_no_wait_ran_out():
+    """Run last in this file: no wait of the kernel hit its time limit."""
+    assert qmv.tc_wait_timeouts() == 0
