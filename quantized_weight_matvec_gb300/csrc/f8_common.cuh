@@ -251,7 +251,8 @@ inline bool chunks_uniform(int64_t C, int64_t SC, int64_t width = 16) {
 }
 
 
-// The tensor-core kernels (f8_mma_kernels.cu).  mma_fits: whether they take
+// The mma.sync tensor-core kernels (f8_mma_kernels.cu), for the batch 2..8
+// calls the fifth-generation kernel does not take.  mma_fits: whether they take
 // this call (batch >= 2, C % 64 == 0, C >= 256, 16-byte aligned w and x,
 // 64-column-aligned scale blocks, shared memory in reach); launch_mma runs
 // them (with the argmax epilogue when `am`), setting the grid size used.
@@ -259,9 +260,9 @@ bool mma_fits(const F8Args &a, int batch);
 qmv_status launch_mma(const F8Args &a, int batch, bool am, cudaStream_t s, int &blocks_out);
 
 // The fifth-generation tensor-core kernel (f8_tc_kernels.cu).  tc_fits:
-// whether it takes this call (batch 5..8, C % 128 == 0 with C <= 4096, 16-byte
-// aligned w and x, every scale block starting on a multiple of 64 rows and of
-// 128 columns); launch_tc runs it.  tc_wait_timeouts
+// whether it takes this call (batch 2..8, C % 128 == 0 with C <= 4096, at
+// least 8 64-row units per SM, 16-byte aligned w and x, every scale block
+// starting on a multiple of 64 rows and of 128 columns); launch_tc runs it.  tc_wait_timeouts
 // reads how many of its waits have ever run out of time (none, normally).
 bool tc_fits(const F8Args &a, int batch);
 qmv_status launch_tc(const F8Args &a, int batch, bool am, cudaStream_t s, int &blocks_out);

@@ -2,8 +2,8 @@
 
 f8_matvec at batch >= 2 on C % 64 == 0 with 64-column-aligned scale blocks
 runs on mma.sync (f16 operands, float32 accumulation) unless the tcgen05
-kernel takes it (batch 5..8 with 128-column, 64-row aligned scale blocks;
-tests/test_gpu_f8_tc.py): E4M3 weights decode
+kernel takes it (large matrices with 128-column, 64-row aligned scale blocks;
+tests/test_gpu_f8_tc.py); the shapes here are all below its size threshold: E4M3 weights decode
 exactly to f16, and each 64-column block of every activation vector is split
 into f16 hi + lo parts under a per-block power-of-two exponent.  The bar is the
 matvec tolerance of ds4f-disk issue #6 step 1's definition,
@@ -156,8 +156,8 @@ def test_mma_deterministic_and_writes_only_its_outputs():
 
 
 def test_mma_kernel_is_the_one_launched():
-    # scale rows of 125 weight rows: not on a 64-row boundary, so batch 8 stays
-    # on this kernel rather than the tcgen05 one
+    # a small matrix with scale rows of 125 weight rows: batch 8 stays on this
+    # kernel rather than the tcgen05 one
     from torch.profiler import ProfilerActivity, profile
     f = synth.f8_inputs(68, 500, 1024, 4, 8, 118, 132, batch=8)
     w, s, x = dev(f.w), dev(f.scale), dev(f.x)
