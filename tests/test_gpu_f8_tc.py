@@ -277,6 +277,75 @@ def test_tc_kernel_is_the_one_launched():
     assert not any("f8_tc" in n for n in names) and any("f8_mma" in n for n in names), names
 
 
+def test_tc_reads_activations_a_preceding_kernel_wrote():
+    """The kernel streams weights before its dependency wait and reads x only
+    after it.  Chain: a small F8 call (mma.sync, which lets its dependents
+    launch early) writes a [8, 4096] result; the large call takes it as x at
+    once, on the same stream, eagerly, on a side stream and inside a CUDA
+    graph.  Each time y is bit for bit the call on the settled x."""
+    g = synth.f8_inputs(90, 4096, 4096, 32, 32, 118, 132, batch=8)
+    f = synth.f8_inputs(91, r0() + 64, 4096, 1, 32, 118, 132, batch=8)
+    gw, gs, gx = dev(g.w), dev(g.scale), dev(g.x)
+    fw, fs = dev(f.w), dev(f.scale)
+    mid = qmv.f8_matvec_t(gw, gs, gx)
+    torch.cuda.synchronize()
+    want = qmv.f8_matvec_t(fw, fs, mid.clone())
+    torch.cuda.synchronize()
+    want = want.cpu()
+
+    def chain(stream=None):
+        m = torch.full((8, 4096), float("nan"), device="cuda")
+        y = torch.full((8, f.R), float("nan"), device="cuda")
+        qmv.f8_matvec_t(gw, gs, gx, out=m, stream=stream)
+        qmv.f8_matvec_t(fw, fs, m, out=y, stream=stream)
+        return y
+
+    y = chain()
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu().view(torch.int32), want.view(torch.int32))
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        y = chain(st)
+    st.synchronize()
+    assert torch.equal(y.cpu().view(torch.int32), want.view(torch.int32))
+    m = torch.full((8, 4096), float("nan"), device="cuda")
+    y = torch.full((8, f.R), float("nan"), device="cuda")
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        qmv.f8_matvec_t(gw, gs, gx, out=m, stream=cs)  # (warm the launch path outside capture)
+        cs.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            qmv.f8_matvec_t(gw, gs, gx, out=m, stream=cs)
+            qmv.f8_matvec_t(fw, fs, m, out=y, stream=cs)
+    m.fill_(float("nan"))
+    y.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y.cpu().view(torch.int32), want.view(torch.int32))
+
+
+def test_tc_back_to_back_calls_keep_their_own_inputs():
+    """Three consecutive calls on one stream with different x and y: each
+    result is the one its own x gives (the next call's early weight loads do
+    not disturb the previous call)."""
+    f = synth.f8_inputs(92, r0(), 2048, 1, 16, 118, 132, batch=6)
+    w, s = dev(f.w), dev(f.scale)
+    rng = np.random.default_rng(92)
+    xs = [dev(rng.standard_normal(f.x.shape).astype(np.float32)) for _ in range(3)]
+    singles = []
+    for x in xs:
+        singles.append(qmv.f8_matvec_t(w, s, x))
+        torch.cuda.synchronize()
+    ys = [torch.empty((6, f.R), device="cuda") for _ in range(3)]
+    for x, y in zip(xs, ys):
+        qmv.f8_matvec_t(w, s, x, out=y)
+    torch.cuda.synchronize()
+    for a, b in zip(ys, singles):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
 def test_zz_no_wait_ran_out():
     """Run last in this file: no wait of the kernel hit its time limit."""
     assert qmv.tc_wait_timeouts() == 0
