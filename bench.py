@@ -449,6 +449,26 @@ def run_ours(args):
     barrier(d)
     f8_alone_ms = h0.elapsed_time(h1) / nh
 
+    # the same head at batch 8 (the tcgen05 kernel: raw E4M3 weights by TMA as
+    # the MMA's wide operand), seeded activations, back-to-back launches
+    x8 = torch.from_numpy(np.random.default_rng(55).standard_normal((8, f8.C)).astype(np.float32)).to(dev)
+    head8 = torch.empty((8, f8.R), dtype=torch.float32, device=dev)
+    n8 = min(args.steps, 20)
+    for _ in range(3):
+        check(qmv.f8_matvec(w5.data_ptr(), f8.R, f8.C, s5.data_ptr(), f8.SR, f8.SC, x8.data_ptr(), 8,
+                            head8.data_ptr(), sh), names[3])
+    torch.cuda.synchronize()
+    h0.record(stream)
+    for _ in range(n8):
+        check(qmv.f8_matvec(w5.data_ptr(), f8.R, f8.C, s5.data_ptr(), f8.SR, f8.SC, x8.data_ptr(), 8,
+                            head8.data_ptr(), sh), names[3])
+    h1.record(stream)
+    torch.cuda.synchronize()
+    barrier(d)
+    f8_b8_ms = h0.elapsed_time(h1) / n8
+    assert torch.isfinite(head8).all()
+    del head8, x8
+
     # the CQ vocabulary projection alone: back-to-back cq_matvec calls over
     # distinct copies of the matrix totalling more than twice the L2 (each
     # call L2-cold), captured in a CUDA graph and replayed, since at ~us per
@@ -485,6 +505,7 @@ def run_ours(args):
     elapsed_s = max_over_ranks(elapsed_ms / 1e3, d)
     e2e_s = max_over_ranks(e2e_ms / 1e3, d)
     f8_s = max_over_ranks(f8_alone_ms / 1e3, d)
+    f8_b8_s = max_over_ranks(f8_b8_ms / 1e3, d)
     cq_s = max_over_ranks(cq_alone_us / 1e6, d)
     cpu = cpu_baseline(cq, f8) if (rank == 0 and world == 1) else None
     if rank != 0:
@@ -493,6 +514,8 @@ def run_ours(args):
         return
     peak, peak_kind = measured_hbm_gbs()
     f8_achieved = nbytes["f8_matvec"] / f8_s / 1e9
+    b8_bytes = f8_bytes(f8.R, f8.C, f8.SR, f8.SC, 8)
+    b8_achieved = b8_bytes / f8_b8_s / 1e9
     cq_achieved = nbytes["cq_matvec"] / cq_s / 1e9
     value = world * total_bytes * args.steps / elapsed_s / 1e9
     line = {
@@ -533,6 +556,16 @@ def run_ours(args):
                         "frac": round(cq_achieved / peak, 4), "traffic": None,
                         "us_per_call": round(cq_s * 1e6, 3),
                         "algorithmic_bytes": nbytes["cq_matvec"]},
+        "roofline_head_b8": {"kernel": "f8_matvec (245760x4096, batch 8: tcgen05 kind::f8f6f4, weights by TMA)",
+                             "bound": "hbm",
+                             "timing": "%d back-to-back launches between one event pair" % n8,
+                             "achieved": round(b8_achieved, 1), "peak": peak,
+                             "peak_kind": peak_kind + " copy bandwidth", "unit": "GB/s",
+                             "frac": round(b8_achieved / peak, 4), "traffic": None,
+                             "us_per_call": round(f8_b8_s * 1e6, 2),
+                             "algorithmic_bytes": b8_bytes,
+                             "ncu": "profiles/f8_tc_head_b8.md (131072 rows: DRAM reads 1.000x the weights, "
+                                    "tensor pipe 16%)"},
         "cpu_baseline": cpu,
         "context": {"pages_cpu_figures": PAGES_CPU_CONTEXT,
                     "this_run_head_s_per_token": round(f8_s, 6)},
