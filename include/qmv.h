@@ -216,14 +216,14 @@ QMV_API qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, c
  * on the tensor cores: every finite E4M3 value is an f16, and each 64-column
  * block of x is split into f16 parts hi + lo under a power-of-two exponent,
  * which carries an element to 2^-22 of itself or 2^-39 of the block's
- * largest |x|, whichever is larger.  When C is a multiple of 128 up to 4096,
- * R is at least 512 rows per SM, every scale block starts on a multiple of
- * 128 columns and of 64 rows, and w and x are 16-byte aligned, the raw E4M3
- * weights go to the fifth-generation tensor cores instead, against x split
- * per 128-column block into eight E4M3 pieces (an element to 2^-16 of itself
- * or 2^-45 of the block's largest |x|, whichever is larger).  At batch 5..8
- * that path keeps partial sums in y between two passes, so the argmax form
- * without y runs the mma.sync kernel there.
+ * largest |x|, whichever is larger.  At batch 5..8, when C is a multiple of
+ * 128 up to 4096, R is at least 192 rows per SM, every scale block starts on
+ * a multiple of 128 columns and of 64 rows, and w and x are 16-byte aligned,
+ * the raw E4M3 weights go to the fifth-generation tensor cores instead,
+ * against x split per 128-column block into eight E4M3 pieces (an element to
+ * 2^-16 of itself or 2^-45 of the block's largest |x|, whichever is larger).
+ * That path keeps partial sums in y between two passes over K, so the argmax
+ * form without y runs the batch 2..8 kernel above.
  * Non-finite results are recomputed element by element, so NaN and Inf
  * follow the formula above.
  *
@@ -509,7 +509,7 @@ QMV_API qmv_status i8_matvec_topk_sample(const int8_t *w, int64_t R, int64_t C,
 
 /*
  * qmv_tc_wait_timeouts -- how many waits of the fifth-generation tensor-core
- * F8 kernel (f8_matvec and its argmax / top-k forms at batch 2..8) have run
+ * F8 kernel (f8_matvec and its argmax / top-k forms at batch 5..8) have run
  * out of their one-second limit on the current device since the library was
  * loaded.  A wait that runs out ends its part of the kernel early and the
  * outputs of that call are not valid.  None is expected; the limit exists so

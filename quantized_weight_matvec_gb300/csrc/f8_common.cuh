@@ -260,9 +260,10 @@ bool mma_fits(const F8Args &a, int batch);
 qmv_status launch_mma(const F8Args &a, int batch, bool am, cudaStream_t s, int &blocks_out);
 
 // The fifth-generation tensor-core kernel (f8_tc_kernels.cu).  tc_fits:
-// whether it takes this call (batch 2..8, C % 128 == 0 with C <= 4096, at
-// least 8 64-row units per SM, 16-byte aligned w and x, every scale block
-// starting on a multiple of 64 rows and of 128 columns); launch_tc runs it.  tc_wait_timeouts
+// whether it takes this call (batch 5..8, C % 128 == 0 with C <= 4096, at
+// least 3 64-row units per SM, 16-byte aligned w and x, every scale block
+// starting on a multiple of 64 rows and of 128 columns, y given); launch_tc
+// runs it.  tc_wait_timeouts
 // reads how many of its waits have ever run out of time (none, normally).
 bool tc_fits(const F8Args &a, int batch);
 qmv_status launch_tc(const F8Args &a, int batch, bool am, cudaStream_t s, int &blocks_out);

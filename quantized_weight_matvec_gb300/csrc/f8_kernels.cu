@@ -474,7 +474,7 @@ qmv_status launch_any(const F8Args &a, int batch, cudaStream_t s, int &blocks) {
     const bool fast = (a.C % 16 == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0) &&
                       (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) && (a.C / 16) * 4 <= 200 * 1024 &&
                       chunks_uniform(a.C, a.SC);
-    if (tc_fits(a, batch)) return launch_tc(a, batch, AM, s, blocks);    // batch 2..8: tcgen05, weights by TMA
+    if (tc_fits(a, batch)) return launch_tc(a, batch, AM, s, blocks);    // batch 5..8: tcgen05, weights by TMA
     if (mma_fits(a, batch)) return launch_mma(a, batch, AM, s, blocks);  // batch 2..8: mma.sync
     if (fast) {
         switch (batch) {

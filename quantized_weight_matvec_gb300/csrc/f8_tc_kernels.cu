@@ -1,4 +1,4 @@
-// f8_tc_kernels.cu -- block-scaled F8 E4M3 matvec at batch 2..8 on the
+// f8_tc_kernels.cu -- block-scaled F8 E4M3 matvec at batch 5..8 on the
 // fifth-generation tensor cores (tcgen05.mma kind::f8f6f4, accumulators in
 // tensor memory, weights streamed by TMA), for sm_103a.
 //
@@ -24,8 +24,8 @@
 // within 2^-21 of the largest are split exactly.  E4M3 x E4M3 products are
 // exact in the float32 accumulator.
 //
-// Passes.  Up to 4 vectors (32 piece rows, batch 2..4) the pieces of all of K
-// take 128 KB of shared memory; 5..8 vectors (64 rows) take twice that, so the
+// Passes.  Up to 4 vectors (32 piece rows) the pieces of all of K take 128 KB
+// of shared memory; 5..8 vectors (64 rows) take twice that, so the
 // K range runs in two passes of half the blocks each, the second adding onto
 // the partial sums the first stored in y (the same thread reads back what it
 // wrote, so the result is deterministic).
@@ -94,7 +94,7 @@ constexpr int kTcMaxJobs = 4;                                    // K-blocks per
 constexpr int kWTma = 2, kWMma = 3;                              // (warps 0, 1 mod 4 may be epilogue)
 constexpr int kEZero = 100000, kENonFinite = 100001;             // block exponent markers
 constexpr uint64_t kWaitNs = 1000000000ull;                      // one second
-constexpr int kTcMinUnitsPerSm = 8;                              // smaller matrices: the mma.sync kernel
+constexpr int kTcMinUnitsPerSm = 3;                              // smaller matrices: the mma.sync kernel
 
 // Vector slots (rows 8v + p of the pieces): 4 at batch <= 4, else 8; the K
 // range then runs in one pass or two, so the pieces of one pass fit 128 KB.
@@ -693,7 +693,9 @@ bool weight_map(const F8Args &a, CUtensorMap &map) {
 }  // namespace
 
 bool tc_fits(const F8Args &a, int batch) {
-    if (batch < 2 || batch > 8 || a.R < 1 || a.R > (int64_t(1) << 31) - 1) return false;
+    // batch 5..8: at 2..4 vectors the mma.sync kernels measured as fast or
+    // faster (the layout below serves them, but is not routed to)
+    if (batch < 5 || batch > 8 || a.R < 1 || a.R > (int64_t(1) << 31) - 1) return false;
     // enough rows for every block to stream a while: the activation pieces are
     // built once per block, which smaller matrices do not repay
     if ((a.R + kTcUnit - 1) / kTcUnit < int64_t(kTcMinUnitsPerSm) * sm_count()) return false;

@@ -2,8 +2,9 @@
 
 f8_matvec at batch >= 2 on C % 64 == 0 with 64-column-aligned scale blocks
 runs on mma.sync (f16 operands, float32 accumulation) unless the tcgen05
-kernel takes it (large matrices with 128-column, 64-row aligned scale blocks;
-tests/test_gpu_f8_tc.py); the shapes here are all below its size threshold: E4M3 weights decode
+kernel takes it (batch 5..8 on large matrices with 128-column, 64-row
+aligned scale blocks; tests/test_gpu_f8_tc.py); the shapes here are all below
+its size threshold: E4M3 weights decode
 exactly to f16, and each 64-column block of every activation vector is split
 into f16 hi + lo parts under a per-block power-of-two exponent.  The bar is the
 matvec tolerance of ds4f-disk issue #6 step 1's definition,

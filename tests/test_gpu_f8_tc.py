@@ -1,16 +1,16 @@
-"""GPU parity of the fifth-generation tensor-core F8 kernel (batch 2..8).
+"""GPU parity of the fifth-generation tensor-core F8 kernel (batch 5..8).
 
-f8_matvec at batch 2..8 goes to tcgen05.mma kind::f8f6f4 when C is a
-multiple of 128 up to 4096, the matrix has at least 8 64-row units per SM,
+f8_matvec at batch 5..8 goes to tcgen05.mma kind::f8f6f4 when C is a
+multiple of 128 up to 4096, the matrix has at least 3 64-row units per SM,
 every scale block starts on a multiple of 128 columns and 64 rows, and w and
 x are 16-byte aligned: the raw E4M3 weights are the wide MMA operand
 (TMA-streamed, 128-byte swizzle) and x enters as four E4M3 pieces per
 128-column block.  The bar is the matvec tolerance of ds4f-disk issue #6
 step 1's definition, |y - y_oracle| <= 1e-4 * sum_c |w * s * x| + 1e-6,
 against the float64 oracle.  The row counts here start at that size
-threshold, R0 = 8 * 64 * (SMs of the device).
+threshold, R0 = 3 * 64 * (SMs of the device).
 
-Cases: every batch 2..8; a ragged last 64-row unit; 64-row and 128-row
+Cases: every batch 5..8; a ragged last 64-row unit; 64-row and 128-row
 scale blocks; one 128-column block; blocks with unequal numbers of units
 (and short last tiles); activations with a wide dynamic range inside a
 block, huge, tiny, subnormal and zero; Inf / NaN in x; saturated E4M3 codes
@@ -39,8 +39,8 @@ def _gpu():
 
 
 def r0():
-    """The fewest rows the kernel takes: 8 64-row units per SM."""
-    return 8 * 64 * torch.cuda.get_device_properties(0).multi_processor_count
+    """The fewest rows the kernel takes: 3 64-row units per SM."""
+    return 3 * 64 * torch.cuda.get_device_properties(0).multi_processor_count
 
 
 def dev(a):
@@ -82,17 +82,17 @@ def kernel_names(fn):
     return names
 
 
-@pytest.mark.parametrize("batch", [2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("batch", [5, 6, 7, 8])
 def test_tc_every_batch_ragged_last_unit(batch):
     R = r0() + 40  # the last 64-row unit holds 40 rows
     check(synth.f8_inputs(100 + batch, R, 1024, 1, 8, 112, 140, batch=batch))
 
 
 @pytest.mark.parametrize("batch,shape", [
-    (3, ("r0", 2048, 128, 16)),        # 128-row x 128-column scale blocks
+    (5, ("r0", 2048, 128, 16)),        # 128-row x 128-column scale blocks
     (8, ("r0", 2048, 128, 16)),
     (5, ("r0+320", 1024, 64, 8)),      # 64-row scale blocks: every unit its own scale row
-    (2, ("r0+1", 128, 0, 1)),          # one 128-column block, one row past a unit
+    (6, ("r0+1", 128, 0, 1)),          # one 128-column block, one row past a unit
     (8, ("r0+1", 128, 0, 1)),
     (8, ("2r0+273", 4096, 0, 32)),     # units split unevenly over the grid, short last tiles
     (6, ("r0", 3968, 64, 31))])        # 31 blocks of 128 columns, 64-row scale blocks
@@ -195,13 +195,12 @@ def test_tc_deterministic_and_writes_only_its_outputs():
     assert not torch.isnan(a).any() and bool((buf[7 * R:] == 3.5).all())
 
 
-@pytest.mark.parametrize("batch", [2, 5, 8])
+@pytest.mark.parametrize("batch", [5, 8])
 def test_tc_argmax_matches_its_matvec(batch):
     """The fused greedy form: y bit for bit the plain call's, within
     tolerance of the oracle; the index is the greedy choice over that y.
-    Without y, batch 2..4 runs the same kernel (the same choice); batch 5..8
-    runs the mma.sync kernel, whose choice must be a greedy one within the
-    tolerance of the oracle's values."""
+    Without y the mma.sync kernel runs, whose choice must be a greedy one
+    within the tolerance of the oracle's values."""
     f = synth.f8_inputs(79 + batch, r0() + 700, 2048, 1, 16, 118, 132, batch=batch)
     w, s, x = dev(f.w), dev(f.scale), dev(f.x)
     y_buf = torch.empty((batch, f.R), dtype=torch.float32, device="cuda")
@@ -217,12 +216,9 @@ def test_tc_argmax_matches_its_matvec(batch):
     assert np.array_equal(val.cpu().numpy().view(np.uint32), y[np.arange(batch), idx].view(np.uint32))
     idx2, _ = qmv.f8_matvec_argmax_t(w, s, x)
     idx2 = idx2.cpu().numpy()
-    if batch <= 4:
-        assert np.array_equal(idx2, idx)
-    else:
-        for k in range(batch):
-            tol = 2 * (REL * mag[k] + ABS)
-            assert ref[k, idx2[k]] >= (ref[k] - tol).max() - tol[idx2[k]]
+    for k in range(batch):
+        tol = 2 * (REL * mag[k] + ABS)
+        assert ref[k, idx2[k]] >= (ref[k] - tol).max() - tol[idx2[k]]
 
 
 def test_tc_argmax_nan_and_ties():
@@ -232,11 +228,12 @@ def test_tc_argmax_nan_and_ties():
     f.w[700] = f.w[300]
     f.x[4] = 0.0
     w, s, x = dev(f.w), dev(f.scale), dev(f.x)
-    idx, _ = qmv.f8_matvec_argmax_t(w, s, x)
-    y = qmv.f8_matvec_t(w, s, x)
+    yb = torch.empty((6, f.R), dtype=torch.float32, device="cuda")
+    idx, _ = qmv.f8_matvec_argmax_t(w, s, x, y=yb)
     torch.cuda.synchronize()
-    idx, y = idx.cpu().numpy(), y.cpu().numpy()
+    idx, y = idx.cpu().numpy(), yb.cpu().numpy()
     assert np.array_equal(idx, oracle.argmax_rows(y))
+    assert np.isnan(y[2]).all() and idx[2] == 0  # NaN everywhere: the first row
     assert idx[4] == 0  # all zero: the first row
 
 
@@ -254,17 +251,19 @@ def test_tc_topk_sample_over_its_matvec():
 def test_tc_kernel_is_the_one_launched():
     f = synth.f8_inputs(83, r0(), 1024, 1, 8, 118, 132, batch=8)
     w, s, x = dev(f.w), dev(f.scale), dev(f.x)
-    for b in (2, 8):
+    for b in (5, 8):
         names = kernel_names(lambda: qmv.f8_matvec_t(w, s, x[:b]))
         assert any("f8_tc" in n for n in names), names
+    # at 2..4 vectors the mma.sync kernel runs
+    names = kernel_names(lambda: qmv.f8_matvec_t(w, s, x[:4]))
+    assert any("f8_mma" in n for n in names) and not any("f8_tc" in n for n in names), names
     # the argmax form: with y on this kernel; without y, at 5..8 vectors, on mma.sync
     yb = torch.empty((8, f.R), dtype=torch.float32, device="cuda")
     names = kernel_names(lambda: qmv.f8_matvec_argmax_t(w, s, x, y=yb))
     assert any("f8_tc" in n for n in names), names
     names = kernel_names(lambda: qmv.f8_matvec_argmax_t(w, s, x))
     assert any("f8_mma" in n for n in names) and not any("f8_tc" in n for n in names), names
-    names = kernel_names(lambda: qmv.f8_matvec_argmax_t(w, s, x[:3]))
-    assert any("f8_tc" in n for n in names), names
+
     # below the size threshold, and with scale rows that start off a 64-row
     # boundary, batch 8 stays on the mma.sync kernel
     g = synth.f8_inputs(84, r0() - 64, 1024, 1, 8, 118, 132, batch=8)

@@ -308,7 +308,7 @@ def head_ref(head):
 def test_f8_head_full_size_every_row(head, head_ref, batch):
     """All 245760 rows of the 245760 x 4096 head (ds4f-disk issue #6, work
     item 3) against the oracle, at each batch the head runs: batch 1 on the
-    streaming kernel, 2-8 on the tcgen05 one."""
+    streaming kernel, 2-4 on the mma.sync kernel, 5-8 on the tcgen05 one."""
     f, w_dev, s_dev = head
     y = host(qmv.f8_matvec_t(w_dev, s_dev, dev(f.x[:batch])))
     ref, mag = head_ref
