@@ -971,6 +971,16 @@ def run_configs(args):
                 med, best = _graph_time(torch, acalls, reps=10)
                 emit(name, batch, "f8_matvec_argmax", nb - 4 * batch * f.R + 12 * batch, med,
                      best, k, call=acalls[0])
+                if batch > 1:  # logits stored too: the batch 5..8 head then runs on tcgen05
+                    ycalls = [(lambda wi: lambda sh: qmv.f8_matvec_argmax(
+                        wi.data_ptr(), f.R, f.C, s5.data_ptr(), f.SR, f.SC, x.data_ptr(), batch,
+                        y.data_ptr(), oi.data_ptr(), ov.data_ptr(), wsp.data_ptr(), wsp.numel(),
+                        sh))(wi) for wi in ws]
+                    if k == 1:
+                        ycalls = ycalls * 8
+                    med, best = _graph_time(torch, ycalls, reps=10)
+                    emit(name, batch, "f8_matvec_argmax(y stored)", nb + 12 * batch, med, best, k,
+                         call=ycalls[0])
                 # head + top-64 temperature sampling (logits stored)
                 tk = 64
                 wst = torch.empty(qmv.TOPK_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)

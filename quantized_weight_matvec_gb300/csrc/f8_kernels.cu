@@ -431,6 +431,127 @@ __global__ void __launch_bounds__(256) f8_rows_kernel(F8Args a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Split-row kernel (batch 1, C from 4096 to 16384 columns, few rows): a block
+// of 8 warps takes a tile of T rows and every warp a share of its columns --
+// lane l of warp w reads the chunks l + 32 (w + 8 s), s < NS, of each row --
+// so the block requests the tile's T * C bytes with all 256 threads at once,
+// and a matrix of up to (resident blocks) x T rows goes out in one wave of
+// loads, issued before the dependency wait.  The warps' row sums meet in
+// shared memory and are added in warp order; warp t finishes row t (NaN
+// fix-up, store, argmax offer).  NS * T = 8 chunks in flight per thread.
+// ---------------------------------------------------------------------------
+constexpr int kSplitWarps = 8;
+
+template <int T, int NS, bool AM>
+__global__ void __launch_bounds__(256, 4) f8_split_kernel(F8Args a) {
+    static_assert(T <= kSplitWarps, "warp t finishes row t");
+    extern __shared__ int chunk_cb[];
+    __shared__ float part[kSplitWarps][T];
+    pdl_trigger();
+    const int64_t nchunk = a.C >> 4;
+    for (int64_t ch = threadIdx.x; ch < nchunk; ch += blockDim.x)
+        chunk_cb[ch] = int((ch * 16 * a.SC) / a.C);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // one tile per block (the launcher makes the grid cover every tile)
+    const int64_t r0 = int64_t(blockIdx.x) * T;
+    const int rows = int(min(int64_t(T), a.R - r0));
+    uint4 d[NS][T];
+#pragma unroll
+    for (int st = 0; st < NS; st++)  // weights only: before the wait
+        load_step<T>(d[st], a, r0, rows, lane + 32 * (warp + kSplitWarps * st), nchunk);
+    pdl_wait();
+    __syncthreads();
+
+    const uint8_t *srow0;
+    uint32_t dpack;
+    const bool uniform = setup_scale<T>(a, r0, rows, srow0, dpack);
+    float acc[T][1];
+#pragma unroll
+    for (int t = 0; t < T; t++) acc[t][0] = 0.0f;
+#pragma unroll
+    for (int st = 0; st < NS; st++) {
+        const int64_t ch = lane + 32 * (warp + kSplitWarps * st);
+        if (ch < nchunk) {
+            if (uniform)
+                compute_step<1, T, true>(acc, d[st], a, srow0, dpack, chunk_cb[ch], ch);
+            else
+                compute_step<1, T, false>(acc, d[st], a, srow0, dpack, chunk_cb[ch], ch);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        const float pv = warp_sum(acc[t][0]);
+        if (lane == 0) part[warp][t] = pv;
+    }
+    __syncthreads();
+    WarpBest<1> best;
+    best.init();
+    if (warp < rows) {  // warp-uniform
+        float val = part[0][warp];
+#pragma unroll
+        for (int w2 = 1; w2 < kSplitWarps; w2++) val += part[w2][warp];
+        if (isnan(val)) val = f8_row_exact(a, r0 + warp, 0, nullptr);
+        if (AM) best.offer(0, val, r0 + warp);
+        if (lane == 0 && (!AM || a.y)) a.y[r0 + warp] = val;
+    }
+    if (AM) {
+        __shared__ __align__(16) unsigned char arg_scratch[sizeof(ArgScratch)];
+        block_best_store<1>(best, a.ws);
+        argmax_complete(a, 1, arg_scratch);
+    }
+}
+
+// Steps per thread of the split kernel for C columns: 1, 2 or 4 (0: not taken).
+inline int split_steps(int64_t C) {
+    const int64_t nchunk = C >> 4;
+    if (nchunk < 32 * kSplitWarps) return 0;
+    for (int ns = 1; ns <= 4; ns *= 2)
+        if (nchunk <= int64_t(32) * kSplitWarps * ns) return ns;
+    return 0;
+}
+
+template <int T, int NS, bool AM>
+int split_capacity(size_t smem) {
+    const void *kp = reinterpret_cast<const void *>(f8_split_kernel<T, NS, AM>);
+    if (!allow_smem(kp, smem)) return 0;
+    return occupancy(kp, 256, smem) * sm_count();
+}
+
+// Whether the split kernel takes this batch-1 call (the fast kernel's
+// requirements hold): C in [4096, 16384] and every tile resident at once.
+template <bool AM>
+bool split_fits(const F8Args &a) {
+    const int ns = split_steps(a.C);
+    if (ns == 0) return false;
+    const size_t smem = size_t(a.C >> 4) * sizeof(int);
+    const int T = 8 / ns;
+    const int cap = ns == 1 ? split_capacity<8, 1, AM>(smem)
+                  : ns == 2 ? split_capacity<4, 2, AM>(smem)
+                            : split_capacity<2, 4, AM>(smem);
+    return (a.R + T - 1) / T <= int64_t(cap);
+}
+
+template <int T, int NS, bool AM>
+qmv_status launch_split_t(const F8Args &a, cudaStream_t s, int &blocks_out) {
+    const size_t smem = size_t(a.C >> 4) * sizeof(int);
+    auto kern = f8_split_kernel<T, NS, AM>;
+    if (!allow_smem(reinterpret_cast<const void *>(kern), smem)) return QMV_ERR_CUDA;
+    const int64_t blocks = (a.R + T - 1) / T;  // one per tile (split_fits: all resident)
+    if (AM && blocks > QMV_ARGMAX_MAX_BLOCKS) return QMV_ERR_SHAPE;
+    blocks_out = int(blocks);
+    return from_cuda(launch_pdl(kern, dim3(unsigned(blocks)), dim3(256), smem, s, a));
+}
+
+template <bool AM>
+qmv_status launch_split(const F8Args &a, cudaStream_t s, int &blocks_out) {
+    switch (split_steps(a.C)) {
+        case 1: return launch_split_t<8, 1, AM>(a, s, blocks_out);
+        case 2: return launch_split_t<4, 2, AM>(a, s, blocks_out);
+        default: return launch_split_t<2, 4, AM>(a, s, blocks_out);
+    }
+}
+
 template <int B, bool AM, int T = (B <= 2) ? 8 : 4, bool PF = false, bool GS = true>
 qmv_status launch_fast(const F8Args &a, cudaStream_t s, int &blocks_out) {
     const size_t smem = size_t(a.C >> 4) * sizeof(int);
@@ -478,7 +599,8 @@ qmv_status launch_any(const F8Args &a, int batch, cudaStream_t s, int &blocks) {
     if (mma_fits(a, batch)) return launch_mma(a, batch, AM, s, blocks);  // batch 2..8: mma.sync
     if (fast) {
         switch (batch) {
-            case 1: return launch_fast<1, AM>(a, s, blocks);
+            case 1:  // few rows of 4096..16384 columns: one wave, columns split over warps
+                return split_fits<AM>(a) ? launch_split<AM>(a, s, blocks) : launch_fast<1, AM>(a, s, blocks);
             case 2: return launch_fast<2, AM>(a, s, blocks);
             case 3: return launch_fast<3, AM>(a, s, blocks);
             case 4: return launch_fast<4, AM>(a, s, blocks);

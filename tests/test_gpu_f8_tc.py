@@ -4,7 +4,7 @@ f8_matvec at batch 5..8 goes to tcgen05.mma kind::f8f6f4 when C is a
 multiple of 128 up to 4096, the matrix has at least 3 64-row units per SM,
 every scale block starts on a multiple of 128 columns and 64 rows, and w and
 x are 16-byte aligned: the raw E4M3 weights are the wide MMA operand
-(TMA-streamed, 128-byte swizzle) and x enters as four E4M3 pieces per
+(TMA-streamed, 128-byte swizzle) and x enters as eight E4M3 pieces per
 128-column block.  The bar is the matvec tolerance of ds4f-disk issue #6
 step 1's definition, |y - y_oracle| <= 1e-4 * sum_c |w * s * x| + 1e-6,
 against the float64 oracle.  The row counts here start at that size
