@@ -241,6 +241,84 @@ __global__ void __launch_bounds__(256) i8_rows_kernel(I8Args a) {
 }
 
 // ---------------------------------------------------------------------------
+// Split-row kernel (batch 1, 4096..16384 columns, few rows): a block of 8
+// warps takes a tile of T rows and every warp a share of its columns --
+// lane l of warp w reads the chunks l + 32 (w + 8 s), s < NS -- so the
+// tile's T * C bytes (and their scale bytes) are requested by all 256
+// threads at once, before the dependency wait, and every tile of the matrix
+// is in flight in one wave.  The warps' row sums are added in shared memory
+// in warp order; warp t stores row t.
+// ---------------------------------------------------------------------------
+constexpr int kSplitWarps = 8;
+
+template <int T, int NS>
+__global__ void __launch_bounds__(256, 4) i8_split_kernel(I8Args a) {
+    static_assert(T <= kSplitWarps, "warp t stores row t");
+    __shared__ float part[kSplitWarps][T];
+    pdl_trigger();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t nchunk = a.C >> 4;
+    const int64_t r0 = int64_t(blockIdx.x) * T;  // one tile per block
+    const int rows = int(min(int64_t(T), a.R - r0));
+    uint4 d[NS][T];
+    unsigned e[NS][T];
+#pragma unroll
+    for (int st = 0; st < NS; st++)  // weights and their scales: before the wait
+        load_step<T>(d[st], e[st], a, r0, rows, lane + 32 * (warp + kSplitWarps * st), nchunk);
+    pdl_wait();
+    float acc[T][1];
+#pragma unroll
+    for (int t = 0; t < T; t++) acc[t][0] = 0.0f;
+#pragma unroll
+    for (int st = 0; st < NS; st++) {
+        const int64_t ch = lane + 32 * (warp + kSplitWarps * st);
+        if (ch < nchunk) compute_step<1, T>(acc, d[st], e[st], a, ch);
+    }
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        const float pv = warp_sum(acc[t][0]);
+        if (lane == 0) part[warp][t] = pv;
+    }
+    __syncthreads();
+    if (warp < rows && lane == 0) {
+        float val = part[0][warp];
+#pragma unroll
+        for (int w2 = 1; w2 < kSplitWarps; w2++) val += part[w2][warp];
+        a.y[r0 + warp] = val;
+    }
+}
+
+// Chunk steps per thread of the split kernel for C columns: 1, 2 or 4 (0:
+// outside its range).
+inline int split_steps(int64_t C) {
+    const int64_t nchunk = C >> 4;
+    if (nchunk < 32 * kSplitWarps) return 0;
+    for (int ns = 1; ns <= 4; ns *= 2)
+        if (nchunk <= int64_t(32) * kSplitWarps * ns) return ns;
+    return 0;
+}
+
+template <int T, int NS>
+qmv_status launch_i8_split_t(const I8Args &a, cudaStream_t s, bool &taken) {
+    const void *kp = reinterpret_cast<const void *>(i8_split_kernel<T, NS>);
+    const int64_t tiles = (a.R + T - 1) / T;
+    taken = tiles <= int64_t(occupancy(kp, 256, 0)) * sm_count();  // every tile resident
+    if (!taken) return QMV_OK;
+    return from_cuda(launch_pdl(i8_split_kernel<T, NS>, dim3(unsigned(tiles)), dim3(256), 0, s, a));
+}
+
+// Runs the split kernel when it takes the call (batch 1, C % 16 == 0 and
+// aligned pointers checked by the caller); `taken` says whether it did.
+qmv_status launch_i8_split(const I8Args &a, cudaStream_t s, bool &taken) {
+    switch (split_steps(a.C)) {
+        case 1: return launch_i8_split_t<8, 1>(a, s, taken);
+        case 2: return launch_i8_split_t<4, 2>(a, s, taken);
+        case 4: return launch_i8_split_t<2, 4>(a, s, taken);
+        default: taken = false; return QMV_OK;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // General kernel: any C and alignment.  One warp per row, one element per
 // lane step: (w * scale) * x in a float32 FMA.
 // ---------------------------------------------------------------------------
@@ -703,6 +781,12 @@ qmv_status launch_i8(const I8Args &a, cudaStream_t s) {
     if (B >= 2 && a.C >= 256) {
         const int nk = mma::staged_nk(a.C, B);
         if (nk) return launch_i8_mma_any<(B + 3) / 4>(a, B, nk, s);
+    }
+    // Batch 1, few rows of 4096..16384 columns: one wave, columns split over warps
+    if (B == 1) {
+        bool taken = false;
+        const qmv_status st = launch_i8_split(a, s, taken);
+        if (taken) return st;
     }
     // Too few tiles to keep a streaming grid busy: the small-matrix kernel
     // (at 4096 rows it also beats converting x in every block).

@@ -4,7 +4,8 @@ per-16 E8M0 group scales) against the float64 oracle.
 Matrices with many rows run on the streaming kernels: up to batch 4 the
 integer-dot kernel (x in fixed-point limbs per 16-column group, exact int32
 sums), above it the float32 kernel; small matrices run on the small-matrix
-kernel.  The tests below cover each route."""
+kernel (batch 1 at 4096..16384 columns: the split-row kernel).  The tests
+below cover each route."""
 import os
 
 import numpy as np
@@ -146,3 +147,67 @@ def test_i8_streaming_extreme_scales():
     f.scale[7, 3] = 255
     y = check(f)
     assert np.isnan(y[:, 7]).all()
+
+
+# ---------------------------------------------------------------------------
+# Split-row kernel: batch 1, 4096..16384 columns, every T-row tile (T = 8, 4,
+# 2 for up to 4096, 8192, 16384 columns) resident at once
+# ---------------------------------------------------------------------------
+
+def kernel_names(fn):
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    names = []
+    for _ in range(2):  # the first profiling session of a process may record nothing
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+        if names:
+            break
+    if not names:
+        pytest.skip("the profiler recorded no kernels on this box")
+    return names
+
+
+@pytest.mark.parametrize("R,C", [(1, 4096), (7, 4096), (9, 4096), (4100, 4096), (1001, 8192),
+                                 (3, 12288), (611, 16384), (5, 4080), (4, 16400)])
+def test_i8_split_shapes(R, C):
+    check(synth.i8_inputs(R * 3 + C, R, C, 100, 130, batch=1))
+
+
+def test_i8_split_nonfinite_x_and_nan_scale():
+    f = synth.i8_inputs(44, 300, 8192, 110, 124, batch=1)
+    f.scale[5, 100] = 255
+    y = check(f)
+    assert np.isnan(y[0, 5]) and not np.isnan(np.delete(y, 5, axis=1)).any()
+    f.x[0, 3000] = np.inf
+    y = check(f)
+    assert not np.isfinite(y).all()
+
+
+def test_i8_split_sees_activations_written_just_before():
+    """Weights and scales are loaded before the dependency wait, x after it."""
+    f = synth.i8_inputs(45, 4096, 4096, 110, 124, batch=4)
+    w, s, src = dev(f.w), dev(f.scale), dev(f.x)
+    x = torch.zeros((1, 4096), device="cuda")
+    ys = []
+    for v in range(4):
+        x.copy_(src[v:v + 1])  # a kernel on the same stream
+        ys.append(qmv.i8_matvec_t(w, s, x))
+    torch.cuda.synchronize()
+    ref, mag = oracle.i8_matvec(f.w, f.scale, f.x, threads=8)
+    for v in range(4):
+        y = ys[v].cpu().numpy()[0].astype(np.float64)
+        assert (np.abs(y - ref[v]) <= REL * mag[v] + ABS).all()
+
+
+@pytest.mark.parametrize("R,C,batch,expect", [
+    (4096, 4096, 1, True), (611, 16384, 1, True), (1000, 2048, 1, False), (4, 16400, 1, False),
+    (4096, 4096, 2, False), (65536, 4096, 1, False)])
+def test_i8_split_kernel_is_the_one_launched(R, C, batch, expect):
+    w = torch.zeros((R, C), dtype=torch.int8, device="cuda")
+    s = torch.full((R, C // 16), 127, dtype=torch.uint8, device="cuda")
+    x = torch.ones((batch, C), device="cuda")
+    names = kernel_names(lambda: qmv.i8_matvec_t(w, s, x))
+    assert any("i8_split_kernel" in n for n in names) == expect, names
