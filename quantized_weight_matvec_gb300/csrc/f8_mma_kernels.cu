@@ -313,8 +313,9 @@ __device__ __forceinline__ int64_t scale_row_offset(const F8Args &a, int64_t r, 
     return q * a.SC;
 }
 
-template <int NJ, int NK, bool AM>
+template <int NJ, int NK, bool AM, bool EARLY>
 __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int batch, int div32) {
+    constexpr bool kEarly = NJ == 1 || EARLY;  // first tiles issued before the dependency wait
     extern __shared__ __align__(16) unsigned char st_smem[];
     constexpr int NCH = 4 * NK;                 // 16-byte chunks per row and warp
     constexpr int SLOT = 16 * NCH * 16;         // bytes per warp and stage
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
 
     // scale column of every K-block (depends only on shapes)
     int *cb64 = reinterpret_cast<int *>(red + 2 * NW * NJ * 32 * 2);
-    if (NJ == 1) pdl_trigger();
+    if (kEarly) pdl_trigger();
     for (int kb = threadIdx.x; kb < NW * NK; kb += blockDim.x) cb64[kb] = int((int64_t(kb) * 64 * a.SC) / a.C);
 
     const int64_t ntiles = (a.R + 15) >> 4;
@@ -336,9 +337,10 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
     // At batch 2-4 (NJ = 1) the first kRing - 1 tiles of weights go out
     // before the dependency wait (they never depend on the preceding kernel).
     // At batch 5-8 (NJ = 2), where the kernel sits at its register limit,
-    // they go out after the barrier below: issued earlier, the head ran 236
-    // against 211 us at batch 8.
-    if (NJ == 1 && int64_t(blockIdx.x) < ntiles) {  // block-uniform
+    // only for matrices of a few tiles per block (EARLY): issued early on the
+    // head, its batch-8 argmax ran 209 against 203 us, while 4096 x 4096
+    // went from 12.1 to 10.8 us.  Otherwise they go out after the barrier.
+    if (kEarly && int64_t(blockIdx.x) < ntiles) {  // block-uniform
 #pragma unroll
         for (int st = 0; st < kRing - 1; st++) {
             const int64_t tl = blockIdx.x + st * gstride;
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
         }
     }
     pdl_wait();
-    if (NJ != 1) pdl_trigger();
+    if (!kEarly) pdl_trigger();
     __syncthreads();
     float best_v = -INFINITY;
     int64_t best_i = INT64_MAX;
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
         }
     };
     if (int64_t(blockIdx.x) < ntiles) {  // block-uniform
-        if (NJ != 1) {
+        if (!kEarly) {
             // the first kRing - 1 tiles go out before the B fragments are built
 #pragma unroll
             for (int st = 0; st < kRing - 1; st++) {
@@ -455,6 +457,9 @@ __global__ void __launch_bounds__(512, 1) f8_mma_staged_kernel(F8Args a, int bat
 // 16-byte aligned w and x, every 64-column block inside one scale block, and
 // its shared memory in reach.
 constexpr size_t kMmaSmemMax = 200 * 1024;
+// Batch 5-8 matrices of at most this many 16-row tiles per block issue their
+// first tiles before the dependency wait (EARLY).
+constexpr int64_t kEarlyTilesPerBlock = 8;
 bool mma_fits_impl(const F8Args &a, int batch) {
     if (batch < 2 || a.C % 64 != 0 || a.C < 256) return false;
     if (reinterpret_cast<uintptr_t>(a.w) % 16 != 0 || reinterpret_cast<uintptr_t>(a.x) % 16 != 0) return false;
@@ -464,17 +469,20 @@ bool mma_fits_impl(const F8Args &a, int batch) {
     return chunks_uniform(a.C, a.SC, 64);
 }
 
-template <int NJ, int NK, bool AM>
+template <int NJ, int NK, bool AM, bool EARLY = false>
 qmv_status launch_mma_staged(const F8Args &a, int batch, cudaStream_t s, int &blocks_out) {
     const int NW = int(a.C / 64 / NK);
     const size_t smem = mma::staged_smem_bytes(NW, NK, NJ, size_t(NW) * NK * 4);  // + scale columns
-    auto kern = f8_mma_staged_kernel<NJ, NK, AM>;
+    auto kern = f8_mma_staged_kernel<NJ, NK, AM, EARLY>;
     const void *kp = reinterpret_cast<const void *>(kern);
     if (!allow_smem(kp, smem)) return QMV_ERR_CUDA;
     const int64_t ntiles = (a.R + 15) / 16;
     int64_t blocks = int64_t(occupancy(kp, 32 * NW, smem)) * sm_count();
     if (blocks > ntiles) blocks = ntiles;
     if (AM && blocks > QMV_ARGMAX_MAX_BLOCKS) blocks = QMV_ARGMAX_MAX_BLOCKS;
+    if constexpr (NJ == 2 && !EARLY) {
+        if (ntiles <= kEarlyTilesPerBlock * blocks) return launch_mma_staged<NJ, NK, AM, true>(a, batch, s, blocks_out);
+    }
     blocks_out = int(blocks);
     // R * SR < 2^32: the scale-row index takes a 32-bit division
     const int div32 = (a.R < (int64_t(1) << 32) && a.SR <= (int64_t(0xffffffff) / a.R)) ? 1 : 0;
