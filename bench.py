@@ -971,6 +971,19 @@ def run_configs(args):
                 med, best = _graph_time(torch, acalls, reps=10)
                 emit(name, batch, "f8_matvec_argmax", nb - 4 * batch * f.R + 12 * batch, med,
                      best, k, call=acalls[0])
+                if batch > 4:  # no y, but room for the logits in the workspace (tcgen05 at 5..8)
+                    wbig = torch.zeros(qmv.f8_argmax_workspace_bytes(batch, f.R), dtype=torch.uint8,
+                                       device=dev)
+                    bcalls = [(lambda wi: lambda sh: qmv.f8_matvec_argmax(
+                        wi.data_ptr(), f.R, f.C, s5.data_ptr(), f.SR, f.SC, x.data_ptr(), batch, 0,
+                        oi.data_ptr(), ov.data_ptr(), wbig.data_ptr(), wbig.numel(), sh))(wi)
+                        for wi in ws]
+                    if k == 1:
+                        bcalls = bcalls * 8
+                    med, best = _graph_time(torch, bcalls, reps=10)
+                    emit(name, batch, "f8_matvec_argmax(logits in workspace)", nb + 12 * batch, med,
+                         best, k, call=bcalls[0])
+                    del wbig
                 if batch > 1:  # logits stored too: the batch 5..8 head then runs on tcgen05
                     ycalls = [(lambda wi: lambda sh: qmv.f8_matvec_argmax(
                         wi.data_ptr(), f.R, f.C, s5.data_ptr(), f.SR, f.SC, x.data_ptr(), batch,

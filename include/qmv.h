@@ -223,7 +223,8 @@ QMV_API qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, c
  * against x split per 128-column block into eight E4M3 pieces (an element to
  * 2^-16 of itself or 2^-45 of the block's largest |x|, whichever is larger).
  * That path keeps partial sums in y between two passes over K, so the argmax
- * form without y runs the batch 2..8 kernel above.
+ * form without y runs the batch 2..8 kernel above unless its workspace has
+ * room for the logits (QMV_F8_ARGMAX_WORKSPACE_TC_BYTES).
  * Non-finite results are recomputed element by element, so NaN and Inf
  * follow the formula above.
  *
@@ -358,6 +359,13 @@ QMV_API qmv_status hadamard_mlp(const float *x, int64_t n, int64_t D, const floa
 #define QMV_ARGMAX_COUNTER_BYTES 16
 #define QMV_F8_ARGMAX_WORKSPACE_BYTES(batch) \
     ((int64_t)QMV_ARGMAX_COUNTER_BYTES + (int64_t)QMV_ARGMAX_MAX_BLOCKS * (int64_t)(batch) * 16)
+/* Bytes of workspace with which a call without y also keeps its batch x R
+ * logits in the workspace (behind the partials, from the next 256-byte
+ * boundary), so that batch 5..8 calls can run on the tcgen05 kernel; with less
+ * they run on the batch 2..8 kernel. */
+#define QMV_F8_ARGMAX_LOGITS_OFFSET(batch) ((QMV_F8_ARGMAX_WORKSPACE_BYTES(batch) + 255) / 256 * 256)
+#define QMV_F8_ARGMAX_WORKSPACE_TC_BYTES(batch, R) \
+    (QMV_F8_ARGMAX_LOGITS_OFFSET(batch) + (int64_t)(batch) * (int64_t)(R) * 4)
 
 /*
  * f8_matvec_argmax -- the head matvec followed by greedy selection, fused.
@@ -384,7 +392,12 @@ QMV_API qmv_status hadamard_mlp(const float *x, int64_t n, int64_t D, const floa
  *              one launch): fill them with zeros once before the workspace's
  *              first use; every call leaves them zero again.  The rest is
  *              scratch, its contents on entry ignored.  Calls that overlap
- *              on the GPU must not share a workspace.
+ *              on the GPU must not share a workspace.  With y NULL and
+ *              workspace_bytes >= QMV_F8_ARGMAX_WORKSPACE_TC_BYTES(batch, R),
+ *              the logits are written to the workspace from byte
+ *              QMV_F8_ARGMAX_LOGITS_OFFSET(batch) on, as [batch, R] float32,
+ *              when that lets a batch 5..8 call run on the tcgen05 kernel
+ *              (the results are those of the same call with y given).
  * R >= 1.  Other arguments and errors as f8_matvec.
  */
 QMV_API qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,

@@ -634,11 +634,20 @@ qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_
 
 qmv_status launch_f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale, int64_t SR,
                                    int64_t SC, const float *x, int batch, float *y, int64_t *out_index,
-                                   float *out_value, void *workspace, cudaStream_t s) {
+                                   float *out_value, void *workspace, int64_t workspace_bytes,
+                                   cudaStream_t s) {
     // workspace: the arrival counter in its first 16 bytes, then the partials
     unsigned char *base = static_cast<unsigned char *>(workspace);
     f8::F8Args a{w,     scale, x, y, R, C, SR, SC, reinterpret_cast<f8::ArgBest *>(base + QMV_ARGMAX_COUNTER_BYTES),
                  reinterpret_cast<unsigned *>(base), out_index, out_value};
+    // No y, but room behind the partials for the batch's logits: keep them
+    // there when that lets the call run on the tcgen05 kernel (which needs y).
+    const int64_t off = QMV_F8_ARGMAX_LOGITS_OFFSET(batch);
+    if (!y && workspace_bytes - off >= int64_t(batch) * R * 4) {
+        f8::F8Args t = a;
+        t.y = reinterpret_cast<float *>(base + off);
+        if (f8::tc_fits(t, batch)) a.y = t.y;
+    }
     int blocks = 0;
     return f8::launch_any<true>(a, batch, s, blocks);
 }

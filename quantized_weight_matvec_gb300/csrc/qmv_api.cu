@@ -375,7 +375,7 @@ qmv_status f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_
             if (overlaps(outs[i], outb[i], outs[j], outb[j])) return QMV_ERR_ALIAS;
     }
     return qmv::launch_f8_matvec_argmax(w, R, C, scale, SR, SC, x, batch, y, out_index, out_value,
-                                        workspace, reinterpret_cast<cudaStream_t>(stream));
+                                        workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 qmv_status i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale, const float *x,

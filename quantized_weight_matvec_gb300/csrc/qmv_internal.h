@@ -110,7 +110,7 @@ qmv_status launch_f8_matvec(const uint8_t *w, int64_t R, int64_t C, const uint8_
 qmv_status launch_f8_matvec_argmax(const uint8_t *w, int64_t R, int64_t C, const uint8_t *scale,
                                    int64_t SR, int64_t SC, const float *x, int batch, float *y,
                                    int64_t *out_index, float *out_value, void *workspace,
-                                   cudaStream_t s);
+                                   int64_t workspace_bytes, cudaStream_t s);
 // Waits of the fifth-generation tensor-core F8 kernel that ran out of time
 // (f8_tc_kernels.cu).
 qmv_status f8_tc_wait_timeouts(unsigned long long *count);

@@ -32,10 +32,20 @@ TOPK_WORKSPACE_BYTES = TOPK_MAX_SLICES * MAX_TOPK * 8
 ARGMAX_COUNTER_BYTES = 16
 
 
-def f8_argmax_workspace_bytes(batch: int) -> int:
+def f8_argmax_workspace_bytes(batch: int, R: int = 0) -> int:
     """QMV_F8_ARGMAX_WORKSPACE_BYTES(batch): the arrival counter, then the
-    per-block partial results."""
-    return ARGMAX_COUNTER_BYTES + ARGMAX_MAX_BLOCKS * int(batch) * 16
+    per-block partial results; with R, QMV_F8_ARGMAX_WORKSPACE_TC_BYTES(batch,
+    R): room behind them for the batch x R logits of a call without y."""
+    base = ARGMAX_COUNTER_BYTES + ARGMAX_MAX_BLOCKS * int(batch) * 16
+    if not R:
+        return base
+    return f8_argmax_logits_offset(batch) + 4 * int(batch) * int(R)
+
+
+def f8_argmax_logits_offset(batch: int) -> int:
+    """QMV_F8_ARGMAX_LOGITS_OFFSET(batch): where a large workspace keeps the
+    logits of a call without y."""
+    return (f8_argmax_workspace_bytes(batch) + 255) // 256 * 256
 
 
 class QmvError(RuntimeError):

@@ -129,6 +129,8 @@ def test_f8_argmax_rejections():
     I, V, K = FAKE + (1 << 33), FAKE + (1 << 34), FAKE + (1 << 35)
     need = qmv.f8_argmax_workspace_bytes(2)
     assert need == 16 + 2048 * 2 * 16
+    assert qmv.f8_argmax_logits_offset(2) == 65792  # need rounded up to 256 bytes
+    assert qmv.f8_argmax_workspace_bytes(2, 1000) == 65792 + 2 * 1000 * 4  # ..._TC_BYTES(2, 1000)
     a = qmv.f8_matvec_argmax
     assert a(W, 0, 16, S, 1, 1, X, 2, Y, I, V, K, need) == 2          # R >= 1
     assert a(W, 16, 16, S, 1, 1, X, 2, Y, I, V, K, need - 1) == 2     # workspace too small

@@ -221,6 +221,33 @@ def test_tc_argmax_matches_its_matvec(batch):
         assert ref[k, idx2[k]] >= (ref[k] - tol).max() - tol[idx2[k]]
 
 
+@pytest.mark.parametrize("batch", [5, 8])
+def test_tc_argmax_without_y_keeps_logits_in_a_large_workspace(batch):
+    """Without y, a workspace of QMV_F8_ARGMAX_WORKSPACE_TC_BYTES(batch, R)
+    holds the logits behind the partials, so the call runs on this kernel:
+    index and value bit for bit those of the same call with y, and the
+    workspace's counter left zero.  One byte less and the mma.sync kernel
+    runs."""
+    R = r0() + 300
+    f = synth.f8_inputs(86 + batch, R, 2048, 1, 16, 118, 132, batch=batch)
+    w, s, x = dev(f.w), dev(f.scale), dev(f.x)
+    yb = torch.empty((batch, R), dtype=torch.float32, device="cuda")
+    idx, val = qmv.f8_matvec_argmax_t(w, s, x, y=yb)
+    big = torch.zeros(qmv.f8_argmax_workspace_bytes(batch, R), dtype=torch.uint8, device="cuda")
+    idx2, val2 = qmv.f8_matvec_argmax_t(w, s, x, workspace=big)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2)
+    assert torch.equal(val.view(torch.int32), val2.view(torch.int32))
+    assert int(big[:16].count_nonzero()) == 0
+    tail = big[qmv.f8_argmax_logits_offset(batch):].view(torch.float32).view(batch, R)
+    assert torch.equal(tail.view(torch.int32), yb.view(torch.int32))
+    names = kernel_names(lambda: qmv.f8_matvec_argmax_t(w, s, x, workspace=big))
+    assert any("f8_tc" in n for n in names), names
+    short = big[:big.numel() - 1]
+    names = kernel_names(lambda: qmv.f8_matvec_argmax_t(w, s, x, workspace=short))
+    assert any("f8_mma" in n for n in names) and not any("f8_tc" in n for n in names), names
+
+
 def test_tc_argmax_nan_and_ties():
     """A NaN result wins the greedy choice; among equal values the lower row."""
     f = synth.f8_inputs(81, r0(), 1024, 1, 8, 120, 128, batch=6)
@@ -257,7 +284,8 @@ def test_tc_kernel_is_the_one_launched():
     # at 2..4 vectors the mma.sync kernel runs
     names = kernel_names(lambda: qmv.f8_matvec_t(w, s, x[:4]))
     assert any("f8_mma" in n for n in names) and not any("f8_tc" in n for n in names), names
-    # the argmax form: with y on this kernel; without y, at 5..8 vectors, on mma.sync
+    # the argmax form: with y on this kernel; without y (and a workspace of
+    # partials only), at 5..8 vectors, on mma.sync
     yb = torch.empty((8, f.R), dtype=torch.float32, device="cuda")
     names = kernel_names(lambda: qmv.f8_matvec_argmax_t(w, s, x, y=yb))
     assert any("f8_tc" in n for n in names), names
