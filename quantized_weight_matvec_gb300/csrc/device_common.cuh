@@ -37,5 +37,16 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return d;
 }
 
+// cp.async: a 16-byte global -> shared copy that holds no registers (L2
+// only), its commit, and a wait for all but the N most recent groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 }  // namespace dev
 }  // namespace qmv

@@ -17,20 +17,17 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "device_common.cuh"
+
 namespace qmv {
 namespace mma {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRing = 3;  // tiles per warp in the cp.async ring
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+using dev::cp_async16;
+using dev::cp_async_commit;
+using dev::cp_async_wait;
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
