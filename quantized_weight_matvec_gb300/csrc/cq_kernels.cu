@@ -391,7 +391,8 @@ __global__ void __launch_bounds__(256) cq_matvec_general_kernel(CqSet c) {
 // evenly over the blocks and, inside a block, warp w takes units w, w + 16,
 // ....  The first kCq2Pre units of every warp are loaded into registers
 // before the dependency wait -- while the preceding call is still running --
-// and the block lets its dependents launch at once.  After the wait: the
+// and the block lets its dependents launch at once (on grids of at most half
+// the SMs, only after the wait).  After the wait: the
 // prepared vector and codebook, the table build, the lookups.
 //
 // Shared memory: 64*P bytes (4 KB per chunk) plus 4*P for the prepared vector
@@ -416,14 +417,14 @@ constexpr int kCq2Warps = kCq2Threads / 32;
 constexpr int kCq2Pre = 4;  // units per warp loaded before the dependency wait
 
 template <int CPR, bool FUSED>
-__global__ void __launch_bounds__(kCq2Threads, FUSED ? 1 : 2) cq2_table_kernel(CqSet c, int64_t upb) {
+__global__ void __launch_bounds__(kCq2Threads, FUSED ? 1 : 2) cq2_table_kernel(CqSet c, int64_t upb, int late_trigger) {
     constexpr int RPW = 32 / CPR;
     constexpr int P = CPR * 64;
     extern __shared__ __align__(16) unsigned char table_raw[];
     float *table = reinterpret_cast<float *>(table_raw);
     float *sp = reinterpret_cast<float *>(table_raw + 64 * P);  // FUSED: prepared vector
 
-    pdl_trigger();
+    if (!late_trigger) pdl_trigger();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int rho = lane / CPR, q = lane % CPR;
     const int g = (q * 64) / int(c.G);
@@ -451,6 +452,7 @@ __global__ void __launch_bounds__(kCq2Threads, FUSED ? 1 : 2) cq2_table_kernel(C
         }
     }
     pdl_wait();
+    if (late_trigger) pdl_trigger();
 
     const float *pv = c.p;
     if (FUSED) {
@@ -568,7 +570,11 @@ qmv_status launch_cq2_table(CqSet c, cudaStream_t s) {
     if (blocks > sm_count()) blocks = sm_count();
     if (blocks < 1) blocks = 1;
     const int64_t upb = (nunits + blocks - 1) / blocks;
-    return from_cuda(launch_pdl(cq2_table_kernel<CPR, FUSED>, dim3(unsigned(blocks)), dim3(kCq2Threads), smem, s, c, upb));
+    // Dependents launch at entry, except on grids of at most half the SMs,
+    // where they are let in after the wait: 2048 x 512 ran 1.57 against 1.70
+    // us per call in chains, while 32768 x 512 ran 3.30 against 2.96.
+    const int late = 2 * blocks <= sm_count() ? 1 : 0;
+    return from_cuda(launch_pdl(cq2_table_kernel<CPR, FUSED>, dim3(unsigned(blocks)), dim3(kCq2Threads), smem, s, c, upb, late));
 }
 
 template <int B, bool FUSED>
@@ -617,11 +623,47 @@ __global__ void __launch_bounds__(256) cq_vec_kernel(CqSet c) {
     // them), then [B][P/16][17] padded
     extern __shared__ __align__(16) float vec_smem[];
     float *spad = vec_smem + (FUSED ? int64_t(B) * c.P : 0);
-    pdl_wait();
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t P = c.P;
     const int nch = int(P >> 4);
+    const int lg = __ffsll(c.G) - 1;
+    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    const int steps = (nch + 31) >> 5;
+    const int64_t nunits = c.first[c.nmats];
+    // chunk ch of row r of matrix mi: its 16 codes and its group's norm
+    auto load_chunk = [&](int mi, int64_t r, int ch, uint64_t &lo, uint32_t &hi, float &n) {
+        lo = 0;
+        hi = 0;
+        n = 0.0f;
+        if (ch < nch) {
+            const uint16_t *src = reinterpret_cast<const uint16_t *>(c.packed[mi] + r * c.row_bytes) + ch * BITS;
+#pragma unroll
+            for (int i = 0; i < BITS; i++) {
+                const uint64_t h = __ldg(src + i);
+                if (i < 4)
+                    lo |= h << (16 * i);
+                else
+                    hi = uint32_t(h);
+            }
+            n = half_bits_to_float(__ldg(c.norms[mi] + r * c.nG + ((int64_t(ch) << 4) >> lg)));
+        }
+    };
+    // this warp's first row, first chunk step, and the codebook: loaded
+    // before the dependency wait (the matrices are read-only model data).
+    // Dependents are let in only after the wait: triggered at entry, chains
+    // of these short calls ran slower (3-5-bit 2048 x 512: 3.5 against 2.1 us).
+    int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    int mi = 0;
+    uint64_t lo0 = 0;
+    uint32_t hi0 = 0;
+    float n0 = 0.0f;
+    if (u < nunits) {
+        mi = set_matrix(c, u, 0);
+        load_chunk(mi, u - c.first[mi], lane, lo0, hi0, n0);
+    }
+    const float cb_lane = lane < (1 << BITS) ? __ldg(c.codebook + lane) : 0.0f;
+    pdl_wait();
+    pdl_trigger();
     const float *psrc = c.p;
     if (FUSED) {
         block_prepare(c, B, vec_smem);
@@ -632,37 +674,26 @@ __global__ void __launch_bounds__(256) cq_vec_kernel(CqSet c) {
         const int64_t v = i / P, k = i - v * P;
         spad[(v * nch + (k >> 4)) * 17 + (k & 15)] = FUSED ? psrc[i] : __ldg(psrc + i);
     }
-    const float cb_lane = lane < (1 << BITS) ? __ldg(c.codebook + lane) : 0.0f;
     __syncthreads();
-    const int lg = __ffsll(c.G) - 1;
-    const int64_t nwarps = int64_t(gridDim.x) * (blockDim.x >> 5);
-    const int steps = (nch + 31) >> 5;
-    int mi = 0;
-    for (int64_t u = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; u < c.first[c.nmats]; u += nwarps) {
+    bool first = true;
+    for (; u < nunits; u += nwarps) {
         mi = set_matrix(c, u, mi);
         const int64_t r = u - c.first[mi];
-        const uint16_t *row = reinterpret_cast<const uint16_t *>(c.packed[mi] + r * c.row_bytes);
-        const uint16_t *nrow = c.norms[mi] + r * c.nG;
         float acc[B];
 #pragma unroll
         for (int v = 0; v < B; v++) acc[v] = 0.0f;
         for (int j = 0; j < steps; j++) {  // warp-uniform trip count: every lane shuffles
             const int ch = lane + 32 * j;
             const bool valid = ch < nch;
-            uint64_t lo = 0;
-            uint32_t hi = 0;
-            float n = 0.0f;
-            if (valid) {
-                const uint16_t *src = row + ch * BITS;
-#pragma unroll
-                for (int i = 0; i < BITS; i++) {
-                    const uint64_t h = __ldg(src + i);
-                    if (i < 4)
-                        lo |= h << (16 * i);
-                    else
-                        hi = uint32_t(h);
-                }
-                n = half_bits_to_float(__ldg(nrow + ((int64_t(ch) << 4) >> lg)));
+            uint64_t lo;
+            uint32_t hi;
+            float n;
+            if (first && j == 0) {
+                lo = lo0;
+                hi = hi0;
+                n = n0;
+            } else {
+                load_chunk(mi, r, ch, lo, hi, n);
             }
             const float *pp = spad + (valid ? ch : 0) * 17;
             float part[B];
@@ -684,6 +715,7 @@ __global__ void __launch_bounds__(256) cq_vec_kernel(CqSet c) {
                 for (int v = 0; v < B; v++) acc[v] = fmaf(part[v], n, acc[v]);
             }
         }
+        first = false;
 #pragma unroll
         for (int v = 0; v < B; v++) {
 #pragma unroll
@@ -788,6 +820,15 @@ qmv_status launch_cq_dequantize_row(const qmv_cq_matrix &m, const int32_t *rows,
 
 bool cq_fused_fits(const qmv_cq_matrix &m, int batch) {
     return m.group <= 1024 && int64_t(batch) * m.input_padded * 4 <= 96 * 1024;
+}
+
+bool cq_set_uses_table(const qmv_cq_matrix *mats, int nmats, int batch) {
+    const int64_t P = mats[0].input_padded;
+    if (mats[0].bits != 2 || batch != 1 || mats[0].group < 64) return false;
+    if (P != 256 && P != 512 && P != 1024 && P != 2048) return false;
+    for (int i = 0; i < nmats; i++)
+        if (reinterpret_cast<uintptr_t>(mats[i].packed) % 16 != 0) return false;  // as launch_cq_set
+    return true;
 }
 
 qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, const float *x,

@@ -40,10 +40,9 @@ inline int grid_blocks(const void *kernel, int threads, size_t smem, int64_t war
 // back-to-back calls of a decode step.  Every kernel of the library reads
 // activations and writes outputs only after pdl_wait(), so stream order holds
 // for them whatever the preceding kernel is.  The matrices are model
-// weights, read-only for the library's calls: the CQ 2-bit table kernel
-// loads its first rows before pdl_wait() (and triggers its dependents at
-// once), so a matrix must not be written by kernels still queued ahead of a
-// call on its stream (see qmv.h).
+// weights, read-only for the library's calls: most matvec kernels (CQ, F8,
+// I8) load their first weights before pdl_wait(), so a matrix must not be
+// written by kernels still queued ahead of a call on its stream (see qmv.h).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
@@ -80,6 +79,9 @@ qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, c
                          float *prepared_out, int batch, float *const *ys, cudaStream_t s);
 // Whether cq_prepare_matvec can prepare on chip (else it runs two launches).
 bool cq_fused_fits(const qmv_cq_matrix &m, int batch);
+// Whether a set call runs on the 2-bit table kernel (the fused prepare pays
+// there; elsewhere the separate prepare launch measured faster).
+bool cq_set_uses_table(const qmv_cq_matrix *mats, int nmats, int batch);
 
 // ---- I8 ------------------------------------------------------------------
 qmv_status launch_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,

@@ -103,3 +103,38 @@ def test_wide_groups_run_as_two_launches():
     with pytest.raises(qmv.QmvError) as e:  # two launches need the prepared buffer
         qmv.cq_prepare_matvec_t(mats, x)
     assert e.value.status == 1
+
+
+def launches(fn):
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    names = []
+    for _ in range(2):  # the first profiling session of a process may record nothing
+        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+        if names:
+            break
+    if not names:
+        pytest.skip("the profiler recorded no kernels on this box")
+    return names
+
+
+def test_prepared_buffer_picks_the_faster_form():
+    """With a prepared buffer, a set off the 2-bit table kernel runs as two
+    launches (prepare, then the set); without one, or on the table kernel,
+    as one fused launch.  Results are the same bits either way."""
+    cs, mats, x = make_set((2048, 2048, 2048), 512, 64, 4, 1, seed=17)
+    p, ref = separate(mats, x)
+    prepared = torch.empty_like(p)
+    assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x, prepared=prepared))) == 2
+    assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x))) == 1
+    ys = qmv.cq_prepare_matvec_t(mats, x, prepared=prepared)
+    ys2 = qmv.cq_prepare_matvec_t(mats, x)
+    torch.cuda.synchronize()
+    for y, y2, r in zip(ys, ys2, ref):
+        assert bits_eq(y, r) and bits_eq(y2, r)
+    cs, mats, x = make_set((2048, 2048, 2048), 512, 64, 2, 1, seed=18)
+    prepared = torch.empty((1, 512), device="cuda")
+    assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x, prepared=prepared))) == 1
