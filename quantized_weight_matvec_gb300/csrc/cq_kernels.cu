@@ -51,7 +51,7 @@ enum class GMode { Prepare, Gather };
 struct GroupArgs {
     int64_t input, P, G, nG;
     int64_t njobs;  // vectors (prepare) or ids (gather)
-    double s;       // RN64(1/sqrt(G))
+    Scale s;        // RN64(1/sqrt(G)), and its float32 split
     float *out;
     // prepare
     const float *x;
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(256) group_small_kernel(GroupArgs a) {
     float v[1];
     v[0] = group_load<M>(a, j, col, valid, codebook_lane<M>(a, lane), bad);
     fwht_warp<1>(v, int(a.G), lane);
-    if (valid) group_store<M>(a, j, col, scale_f64(v[0], a.s), bad);
+    if (valid) group_store<M>(a, j, col, scale_rn(v[0], a.s), bad);
 }
 
 // 64 <= G <= 1024: one warp per group job, E = G/32 elements per lane.
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) group_warp_kernel(GroupArgs a) {
     for (int e = 0; e < E; e++) v[e] = group_load<M>(a, j, col0 + e, true, cbl, bad);
     fwht_warp<E>(v, int(a.G), lane);
 #pragma unroll
-    for (int e = 0; e < E; e++) group_store<M>(a, j, col0 + e, scale_f64(v[e], a.s), bad);
+    for (int e = 0; e < E; e++) group_store<M>(a, j, col0 + e, scale_rn(v[e], a.s), bad);
 }
 
 // G > 1024: one block per group job, the group staged in shared memory and
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(1024) group_block_kernel(GroupArgs a) {
     }
     __syncthreads();
     for (int i = threadIdx.x; i < G; i += blockDim.x)
-        group_store<M>(a, j, g * a.G + i, scale_f64(sm[i], a.s), bad);
+        group_store<M>(a, j, g * a.G + i, scale_rn(sm[i], a.s), bad);
 }
 
 template <GMode M>
@@ -215,7 +215,7 @@ GroupArgs group_args(const qmv_cq_matrix &m) {
     a.P = m.input_padded;
     a.G = m.group;
     a.nG = m.input_padded / m.group;
-    a.s = 1.0 / sqrt(double(m.group));
+    a.s = make_scale(1.0 / sqrt(double(m.group)));
     a.packed = m.packed;
     a.norms = m.norms;
     a.codebook = m.codebook;
@@ -248,7 +248,7 @@ struct CqSet {
     const float *p;        // prepared activation [B, P] (not FUSED)
     const float *x;        // raw activation [B, input] (FUSED)
     float *prepared_out;   // FUSED: block 0 also stores the prepared vector (may be NULL)
-    double s;              // RN64(1/sqrt(G))
+    Scale s;               // RN64(1/sqrt(G)), and its float32 split
 };
 
 // Matrix of unit u, scanning on from matrix i (units of a warp only grow).
@@ -275,7 +275,7 @@ __device__ __forceinline__ void prep_warp_jobs(const CqSet &c, int B, float *sp)
         fwht_warp<E>(val, int(c.G), lane);
 #pragma unroll
         for (int e = 0; e < E; e++) {
-            const float o = scale_f64(val[e], c.s);
+            const float o = scale_rn(val[e], c.s);
             sp[v * c.P + col0 + e] = o;
             if (store) c.prepared_out[v * c.P + col0 + e] = o;
         }
@@ -295,7 +295,7 @@ __device__ __forceinline__ void prep_small(const CqSet &c, int B, float *sp) {
         val[0] = (valid && col < c.input) ? __ldg(c.x + v * c.input + col) : 0.0f;
         fwht_warp<1>(val, int(c.G), lane);
         if (valid) {
-            const float o = scale_f64(val[0], c.s);
+            const float o = scale_rn(val[0], c.s);
             sp[flat] = o;
             if (store) c.prepared_out[flat] = o;
         }
@@ -843,7 +843,7 @@ qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, c
     c.nG = m0.input_padded / m0.group;
     c.row_bytes = m0.row_bytes;
     c.codebook = m0.codebook;
-    c.s = 1.0 / sqrt(double(m0.group));
+    c.s = make_scale(1.0 / sqrt(double(m0.group)));
     c.p = p;
     c.x = x;
     c.prepared_out = prepared_out;

@@ -9,6 +9,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <math.h>
 
 namespace qmv {
 namespace {
@@ -17,6 +18,55 @@ namespace {
 // 1/sqrt(group) and stores the product into float32.
 __device__ __forceinline__ float scale_f64(float v, double s) {
     return __double2float_rn(__dmul_rn(double(v), s));
+}
+
+// The same value without float64 arithmetic (GB300 issues about two
+// float64 multiplies per clock per SM).  s = s1 + s2 + s3 exactly, each a
+// float32; then p = RN32(v s1), its exact error e = v s1 - p (one FMA),
+// t = RN32(RN32(v s2 + e) + v s3) by two FMAs, and the result RN32(p + t).
+// For s = RN64(1/sqrt 2) * 2^-k (group or dimension an odd power of two)
+// this equals RN32(RN64(v * s)) for every float32 mantissa, both signs
+// (checked exhaustively on the host against the definition), as long as no
+// step leaves the normal range; for s = 2^-k it is v * s exactly.  Other s,
+// and |v| outside [2^-60, 2^100] (zero, tiny, huge, Inf, NaN), take
+// the float64 product.
+struct Scale {
+    double s;           // RN64(1/sqrt(n))
+    float s1, s2, s3;   // s = s1 + s2 + s3
+    int fast;           // s is 2^-k or RN64(1/sqrt 2) * 2^-k
+};
+
+inline Scale make_scale(double s) {
+    Scale k;
+    k.s = s;
+    k.s1 = float(s);
+    const double r = s - double(k.s1);
+    k.s2 = float(r);
+    k.s3 = float(r - double(k.s2));
+    int e1 = 0, e2 = 0;
+    const double m1 = frexp(s, &e1);                     // s = m1 * 2^e1, m1 in [0.5, 1)
+    const double m2 = frexp(s / (1.0 / sqrt(2.0)), &e2);  // exact when s = that constant * 2^-k
+    const bool exact_split = double(k.s1) + double(k.s2) + double(k.s3) == s;
+    k.fast = exact_split && s > 0.0 && (m1 == 0.5 || (m2 == 0.5 && s == ldexp(1.0 / sqrt(2.0), e2 - 1)))
+                 ? 1
+                 : 0;
+    return k;
+}
+
+// (out of line, so that the compiler does not predicate the float64
+// multiply into the common path)
+__device__ __noinline__ float scale_f64_rare(float v, double s) { return scale_f64(v, s); }
+
+__device__ __forceinline__ float scale_rn(float v, const Scale &k) {
+    const float av = fabsf(v);
+    if (__builtin_expect(k.fast && av >= 0x1p-60f && av <= 0x1p100f, 1)) {
+        const float p = __fmul_rn(v, k.s1);
+        const float e = __fmaf_rn(v, k.s1, -p);
+        float t = __fmaf_rn(v, k.s2, e);
+        t = __fmaf_rn(v, k.s3, t);
+        return __fadd_rn(p, t);
+    }
+    return scale_f64_rare(v, k.s);
 }
 
 // Unnormalised FWHT of one group spread over a warp.  For G >= 32 each lane

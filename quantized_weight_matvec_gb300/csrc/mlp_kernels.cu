@@ -33,7 +33,7 @@ struct MlpArgs {
     float *out;
     int64_t n;
     int D;
-    double s;  // RN64(1/sqrt(D))
+    Scale s;  // RN64(1/sqrt(D)), and its float32 split
 };
 
 // Whole-vector FWHT: v holds elements tid*E .. tid*E+E-1 of the D values.
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(1024) hadamard_mlp_kernel(MlpArgs a) {
 #pragma unroll
     for (int e = 0; e < E; e++) {
         const float d2e = PRE ? g2[e] : (live ? __ldg(a.d2 + i0 + e) : 0.0f);
-        v[e] = silu32(__fmul_rn(d2e, scale_f64(v[e], a.s)));
+        v[e] = silu32(__fmul_rn(d2e, scale_rn(v[e], a.s)));
     }
     fwht_block<E>(v, sm, a.D, tid, nt);
     float *ov = a.out + j * a.n;
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(1024) hadamard_mlp_kernel(MlpArgs a) {
         const int i = i0 + e;
         if (!live || i >= a.n) continue;
         const float d3e = PRE ? g3[e] : __ldg(a.d3 + i);
-        float o = __fmul_rn(scale_f64(v[e], a.s), d3e);
+        float o = __fmul_rn(scale_rn(v[e], a.s), d3e);
         if (rv) o = __fadd_rn(PRE ? rr[e] : __ldg(rv + i), o);
         if (uv) o = __fsub_rn(o, PRE ? uu[e] : __ldg(uv + i));
         ov[i] = o;
@@ -128,7 +128,7 @@ qmv_status launch_mlp(const MlpArgs &a, int batch, cudaStream_t s) {
 qmv_status launch_hadamard_mlp(const float *x, int64_t n, int D, const float *d1, const float *d2,
                                const float *d3, const float *residual, const float *u, int batch,
                                float *out, double s, cudaStream_t stream) {
-    const MlpArgs a{x, d1, d2, d3, residual, u, out, n, D, s};
+    const MlpArgs a{x, d1, d2, d3, residual, u, out, n, D, make_scale(s)};
     // E values per thread: one warp up to D = 256, then 8 per thread up to
     // 1024 threads (D = 8192), then 16 and 32.
     if (D <= 32) return launch_mlp<1>(a, batch, stream);

@@ -89,6 +89,31 @@ def test_prepare_scale_rounding_case():
     assert got[0] == got[1] == np.float32(float.fromhex("0x1.d81934p-1"))
 
 
+@pytest.mark.parametrize("binade,full", [(0, True), (-60, True), (99, True), (-61, False),
+                                         (100, False), (-130, False)])
+def test_prepare_scale_every_mantissa(binade, full):
+    """Group 2, pairs (v, 0): both outputs must be RN32(RN64(v * RN64(1/sqrt 2))).
+    Every float32 mantissa of the binade [2^b, 2^(b+1)), both signs (a 2^16
+    sample outside the range where the kernels use their float32 form of the
+    product: there they take the float64 one; b = -130 is subnormal)."""
+    if binade >= -126:
+        m = np.arange(1 << 23, dtype=np.uint32)
+        v = ((np.uint32(127 + binade) << 23) | m).view(np.float32)
+    else:  # subnormal: exponent field 0, value m * 2^-149
+        v = np.arange(1 << (binade + 149), 1 << (binade + 150), dtype=np.uint32).view(np.float32)
+    if not full:
+        v = np.random.default_rng(abs(binade)).choice(v, 1 << 16, replace=False)
+    v = np.concatenate([v, -v])
+    x = np.zeros((1, 2 * v.size), np.float32)
+    x[0, 0::2] = v
+    c = synth.cq_inputs(2, 1, x.shape[1], 2, 2)
+    mat = qmv.CQMatrix.from_numpy(c)
+    got = host(qmv.cq_prepare_t(mat, dev(x)))[0]
+    s = 1.0 / np.sqrt(np.float64(2.0))
+    want = (v.astype(np.float64) * s).astype(np.float32)
+    assert bits_equal(got[0::2], want) and bits_equal(got[1::2], want)
+
+
 # ---------------------------------------------------------------------------
 # cq_dequantize_row: bit-exact, out-of-range ids
 # ---------------------------------------------------------------------------

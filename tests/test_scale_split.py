@@ -1,0 +1,65 @@
+"""The float32 form of the normalisation product used by the CQ prepare,
+row gather and Hadamard MLP kernels (needle.js "part 2", sections 1-2:
+1/sqrt(n) in float64, the product taken in float64 and stored as float32).
+
+The kernels avoid float64 arithmetic: with s = RN64(1/sqrt n) split exactly
+into three float32 terms s1 + s2 + s3, they form p = RN32(v s1), its exact
+error e = v s1 - p, t = RN32(RN32(v s2 + e) + v s3) and RN32(p + t).  This
+test replays those steps on the host with exact intermediate arithmetic
+(float64 / long double where each step's exact value fits) for every
+float32 mantissa, both signs, at the binades that bound the kernels' range
+for this form ([2^-60, 2^100]), and checks the result against the
+definition RN32(RN64(v * s)).  s = RN64(1/sqrt 2) covers every odd power of
+two n (the other values differ by a power of two); for even powers s is a
+power of two and the product is exact.
+"""
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.skipif(np.finfo(np.longdouble).nmant < 63,
+                                reason="needs an 80-bit long double for the exact replay")
+
+
+def split(s):
+    s1 = np.float32(s)
+    r = s - np.float64(s1)
+    s2 = np.float32(r)
+    s3 = np.float32(r - np.float64(s2))
+    assert np.float64(s1) + np.float64(s2) + np.float64(s3) == s
+    return s1, s2, s3
+
+
+def replay(v, s1, s2, s3):
+    """The kernel's steps on float32 v, each rounded exactly as the GPU does."""
+    p = v * s1                                                     # RN32
+    e64 = v.astype(np.float64) * np.float64(s1) - p.astype(np.float64)
+    e = e64.astype(np.float32)
+    assert np.array_equal(e.astype(np.float64), e64)               # the error is exact
+    t1x = v.astype(np.longdouble) * np.longdouble(s2) + e.astype(np.longdouble)
+    t1 = t1x.astype(np.float32)                                    # one FMA, one rounding
+    t2x = v.astype(np.longdouble) * np.longdouble(s3) + t1.astype(np.longdouble)
+    t2 = t2x.astype(np.float32)
+    return (p.astype(np.float64) + t2.astype(np.float64)).astype(np.float32)
+
+
+@pytest.mark.parametrize("k", [0, 3, 14])        # n = 2, 2^7, 2^29
+@pytest.mark.parametrize("binade", [0, -60, 99])
+def test_three_term_product_matches_float64_rounding(k, binade):
+    s = 1.0 / np.sqrt(np.float64(2.0)) / np.float64(2.0 ** k)   # RN64(1/sqrt(2^(2k+1)))
+    assert s == 1.0 / np.sqrt(np.float64(2.0 ** (2 * k + 1)))
+    s1, s2, s3 = split(s)
+    m = np.arange(1 << 23, dtype=np.uint32)
+    for sign in (1, -1):
+        v = ((np.uint32(127 + binade) << 23) | m).view(np.float32)
+        if sign < 0:
+            v = -v
+        want = (v.astype(np.float64) * s).astype(np.float32)
+        got = replay(v, s1, s2, s3)
+        bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
+        assert bad.size == 0, (k, binade, sign, v[bad[:3]], got[bad[:3]], want[bad[:3]])
+
+
+def test_powers_of_two_are_exact():
+    s = 1.0 / np.sqrt(np.float64(64.0))
+    s1, s2, s3 = split(s)
+    assert s1 == np.float32(0.125) and s2 == 0 and s3 == 0
