@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(256) group_small_kernel(GroupArgs a) {
     float v[1];
     v[0] = group_load<M>(a, j, col, valid, codebook_lane<M>(a, lane), bad);
     fwht_warp<1>(v, int(a.G), lane);
-    if (valid) group_store<M>(a, j, col, scale_rn(v[0], a.s), bad);
+    scale_rn_all<1>(v, a.s);
+    if (valid) group_store<M>(a, j, col, v[0], bad);
 }
 
 // 64 <= G <= 1024: one warp per group job, E = G/32 elements per lane.
@@ -146,8 +147,9 @@ __global__ void __launch_bounds__(256) group_warp_kernel(GroupArgs a) {
 #pragma unroll
     for (int e = 0; e < E; e++) v[e] = group_load<M>(a, j, col0 + e, true, cbl, bad);
     fwht_warp<E>(v, int(a.G), lane);
+    scale_rn_all<E>(v, a.s);
 #pragma unroll
-    for (int e = 0; e < E; e++) group_store<M>(a, j, col0 + e, scale_rn(v[e], a.s), bad);
+    for (int e = 0; e < E; e++) group_store<M>(a, j, col0 + e, v[e], bad);
 }
 
 // G > 1024: one block per group job, the group staged in shared memory and
@@ -273,9 +275,10 @@ __device__ __forceinline__ void prep_warp_jobs(const CqSet &c, int B, float *sp)
             val[e] = col < c.input ? __ldg(c.x + v * c.input + col) : 0.0f;
         }
         fwht_warp<E>(val, int(c.G), lane);
+        scale_rn_all<E>(val, c.s);
 #pragma unroll
         for (int e = 0; e < E; e++) {
-            const float o = scale_rn(val[e], c.s);
+            const float o = val[e];
             sp[v * c.P + col0 + e] = o;
             if (store) c.prepared_out[v * c.P + col0 + e] = o;
         }
@@ -294,8 +297,9 @@ __device__ __forceinline__ void prep_small(const CqSet &c, int B, float *sp) {
         float val[1];
         val[0] = (valid && col < c.input) ? __ldg(c.x + v * c.input + col) : 0.0f;
         fwht_warp<1>(val, int(c.G), lane);
+        scale_rn_all<1>(val, c.s);
         if (valid) {
-            const float o = scale_rn(val[0], c.s);
+            const float o = val[0];
             sp[flat] = o;
             if (store) c.prepared_out[flat] = o;
         }

@@ -28,8 +28,8 @@ __device__ __forceinline__ float scale_f64(float v, double s) {
 // this equals RN32(RN64(v * s)) for every float32 mantissa, both signs
 // (checked exhaustively on the host against the definition), as long as no
 // step leaves the normal range; for s = 2^-k it is v * s exactly.  Other s,
-// and |v| outside [2^-60, 2^100] (zero, tiny, huge, Inf, NaN), take
-// the float64 product.
+// and nonzero |v| outside [2^-60, 2^100] (tiny, huge, Inf, NaN), take the
+// float64 product.
 struct Scale {
     double s;           // RN64(1/sqrt(n))
     float s1, s2, s3;   // s = s1 + s2 + s3
@@ -57,16 +57,42 @@ inline Scale make_scale(double s) {
 // multiply into the common path)
 __device__ __noinline__ float scale_f64_rare(float v, double s) { return scale_f64(v, s); }
 
-__device__ __forceinline__ float scale_rn(float v, const Scale &k) {
+// Whether v takes the float32 form: zero, or |v| in [2^-60, 2^100].
+__device__ __forceinline__ bool scale_in_range(float v) {
     const float av = fabsf(v);
-    if (__builtin_expect(k.fast && av >= 0x1p-60f && av <= 0x1p100f, 1)) {
-        const float p = __fmul_rn(v, k.s1);
-        const float e = __fmaf_rn(v, k.s1, -p);
-        float t = __fmaf_rn(v, k.s2, e);
-        t = __fmaf_rn(v, k.s3, t);
-        return __fadd_rn(p, t);
-    }
+    return av == 0.0f || (av >= 0x1p-60f && av <= 0x1p100f);
+}
+
+// The float32 form.  copysign keeps the sign of a zero product (p + t would
+// give +0 for v = -0); for every other v in range |t| < |p| / 2, so it
+// changes nothing.
+__device__ __forceinline__ float scale_f32(float v, const Scale &k) {
+    const float p = __fmul_rn(v, k.s1);
+    const float e = __fmaf_rn(v, k.s1, -p);
+    float t = __fmaf_rn(v, k.s2, e);
+    t = __fmaf_rn(v, k.s3, t);
+    return copysignf(__fadd_rn(p, t), p);
+}
+
+__device__ __forceinline__ float scale_rn(float v, const Scale &k) {
+    if (__builtin_expect(k.fast && scale_in_range(v), 1)) return scale_f32(v, k);
     return scale_f64_rare(v, k.s);
+}
+
+// scale_rn of E values with one test for all of them (one branch per
+// group of values, not one per value).
+template <int E>
+__device__ __forceinline__ void scale_rn_all(float (&v)[E], const Scale &k) {
+    bool ok = k.fast != 0;
+#pragma unroll
+    for (int e = 0; e < E; e++) ok = ok && scale_in_range(v[e]);
+    if (__builtin_expect(ok, 1)) {
+#pragma unroll
+        for (int e = 0; e < E; e++) v[e] = scale_f32(v[e], k);
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; e++) v[e] = scale_rn(v[e], k);
+    }
 }
 
 // Unnormalised FWHT of one group spread over a warp.  For G >= 32 each lane

@@ -94,19 +94,21 @@ __global__ void __launch_bounds__(1024) hadamard_mlp_kernel(MlpArgs a) {
         }
     }
     fwht_block<E>(v, sm, a.D, tid, nt);
+    scale_rn_all<E>(v, a.s);
 #pragma unroll
     for (int e = 0; e < E; e++) {
         const float d2e = PRE ? g2[e] : (live ? __ldg(a.d2 + i0 + e) : 0.0f);
-        v[e] = silu32(__fmul_rn(d2e, scale_rn(v[e], a.s)));
+        v[e] = silu32(__fmul_rn(d2e, v[e]));
     }
     fwht_block<E>(v, sm, a.D, tid, nt);
+    scale_rn_all<E>(v, a.s);
     float *ov = a.out + j * a.n;
 #pragma unroll
     for (int e = 0; e < E; e++) {
         const int i = i0 + e;
         if (!live || i >= a.n) continue;
         const float d3e = PRE ? g3[e] : __ldg(a.d3 + i);
-        float o = __fmul_rn(scale_rn(v[e], a.s), d3e);
+        float o = __fmul_rn(v[e], d3e);
         if (rv) o = __fadd_rn(PRE ? rr[e] : __ldg(rv + i), o);
         if (uv) o = __fsub_rn(o, PRE ? uu[e] : __ldg(uv + i));
         ov[i] = o;

@@ -114,6 +114,28 @@ def test_prepare_scale_every_mantissa(binade, full):
     assert bits_equal(got[0::2], want) and bits_equal(got[1::2], want)
 
 
+def test_prepare_power_of_two_scale_edges():
+    """Group 4, x = (v, 0, 0, 0): all four outputs are RN32(RN64(v / 2)), the
+    power-of-two case (one float32 multiply): subnormal v (halving rounds),
+    the smallest normals, huge values, +-Inf and NaN."""
+    rng = np.random.default_rng(4)
+    sub = rng.integers(1, 1 << 23, 4096, dtype=np.uint32).view(np.float32)
+    v = np.concatenate([sub, -sub, np.array([np.finfo(np.float32).tiny, np.finfo(np.float32).max,
+                                             -np.finfo(np.float32).max, np.inf, -np.inf,
+                                             np.float32(1.5e-45), 0.0], np.float32)])
+    x = np.zeros((1, 4 * v.size), np.float32)
+    x[0, 0::4] = v
+    c = synth.cq_inputs(3, 1, x.shape[1], 4, 2)
+    got = host(qmv.cq_prepare_t(qmv.CQMatrix.from_numpy(c), dev(x)))[0].reshape(-1, 4)
+    want = (v.astype(np.float64) * 0.5).astype(np.float32)
+    for j in range(4):
+        assert bits_equal(got[:, j], want)
+    xn = np.zeros((1, 4), np.float32)
+    xn[0, 0] = np.nan
+    gn = host(qmv.cq_prepare_t(qmv.CQMatrix.from_numpy(synth.cq_inputs(3, 1, 4, 4, 2)), dev(xn)))[0]
+    assert np.isnan(gn).all()
+
+
 # ---------------------------------------------------------------------------
 # cq_dequantize_row: bit-exact, out-of-range ids
 # ---------------------------------------------------------------------------

@@ -8,8 +8,8 @@ error e = v s1 - p, t = RN32(RN32(v s2 + e) + v s3) and RN32(p + t).  This
 test replays those steps on the host with exact intermediate arithmetic
 (float64 / long double where each step's exact value fits) for every
 float32 mantissa, both signs, at the binades that bound the kernels' range
-for this form ([2^-60, 2^100]), and checks the result against the
-definition RN32(RN64(v * s)).  s = RN64(1/sqrt 2) covers every odd power of
+for this form ([2^-60, 2^100], and signed zeros), and checks the result
+against the definition RN32(RN64(v * s)).  s = RN64(1/sqrt 2) covers every odd power of
 two n (the other values differ by a power of two); for even powers s is a
 power of two and the product is exact.
 """
@@ -39,7 +39,8 @@ def replay(v, s1, s2, s3):
     t1 = t1x.astype(np.float32)                                    # one FMA, one rounding
     t2x = v.astype(np.longdouble) * np.longdouble(s3) + t1.astype(np.longdouble)
     t2 = t2x.astype(np.float32)
-    return (p.astype(np.float64) + t2.astype(np.float64)).astype(np.float32)
+    r = (p.astype(np.float64) + t2.astype(np.float64)).astype(np.float32)
+    return np.copysign(r, p)  # (the kernels keep the sign of a zero product)
 
 
 @pytest.mark.parametrize("k", [0, 3, 14])        # n = 2, 2^7, 2^29
@@ -57,6 +58,14 @@ def test_three_term_product_matches_float64_rounding(k, binade):
         got = replay(v, s1, s2, s3)
         bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
         assert bad.size == 0, (k, binade, sign, v[bad[:3]], got[bad[:3]], want[bad[:3]])
+
+
+def test_signed_zeros_keep_their_sign():
+    s = 1.0 / np.sqrt(np.float64(2.0))
+    s1, s2, s3 = split(s)
+    v = np.array([0.0, -0.0], np.float32)
+    got = replay(v, s1, s2, s3)
+    assert np.array_equal(got.view(np.uint32), (v.astype(np.float64) * s).astype(np.float32).view(np.uint32))
 
 
 def test_powers_of_two_are_exact():
