@@ -828,14 +828,9 @@ def run_configs(args):
         def fused(ms):
             return lambda sh: qmv.cq_prepare_matvec([m.struct for m in ms], x.data_ptr(), 1, 0, yp, sh)
 
-        def fused_p(ms):  # prepared buffer given: off the 2-bit table kernel, two launches
-            return lambda sh: qmv.cq_prepare_matvec([m.struct for m in ms], x.data_ptr(), 1,
-                                                    p.data_ptr(), yp, sh)
-
         tag = "%s/%dbit" % (label, bits)
         for op, mk in (("prepare+cq_matvec x%d" % len(cs), sep),
-                       ("prepare+cq_matvec_multi", multi), ("cq_prepare_matvec", fused),
-                       ("cq_prepare_matvec(prepared given)", fused_p)):
+                       ("prepare+cq_matvec_multi", multi), ("cq_prepare_matvec", fused)):
             med, best = _graph_time(torch, [mk(ms) for ms in sets])
             emit(tag, 1, op, nb, med, best, k)
         del packs, norms, sets

@@ -196,11 +196,7 @@ QMV_API qmv_status cq_matvec_multi(const qmv_cq_matrix *mats, int32_t nmats, con
  * activation [batch, input_padded] is also written there.  When
  * batch * input_padded floats do not fit on chip (over 96 KiB) or
  * group > 1024, the call runs cq_prepare and cq_matvec_multi as two
- * launches instead (same results; `prepared` must then be given).  With
- * `prepared` given it also does so for every set that does not run on the
- * 2-bit table kernel (bits 2 at batch 1, group >= 64, input_padded 256, 512,
- * 1024 or 2048, 16-byte aligned packed rows), where the separate prepare is
- * faster; the results are the same either way.
+ * launches instead (same results; `prepared` must then be given).
  */
 QMV_API qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, const float *x,
                                      int32_t batch, float *prepared, float *const *ys,

@@ -826,15 +826,6 @@ bool cq_fused_fits(const qmv_cq_matrix &m, int batch) {
     return m.group <= 1024 && int64_t(batch) * m.input_padded * 4 <= 96 * 1024;
 }
 
-bool cq_set_uses_table(const qmv_cq_matrix *mats, int nmats, int batch) {
-    const int64_t P = mats[0].input_padded;
-    if (mats[0].bits != 2 || batch != 1 || mats[0].group < 64) return false;
-    if (P != 256 && P != 512 && P != 1024 && P != 2048) return false;
-    for (int i = 0; i < nmats; i++)
-        if (reinterpret_cast<uintptr_t>(mats[i].packed) % 16 != 0) return false;  // as launch_cq_set
-    return true;
-}
-
 qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, const float *x,
                          float *prepared_out, int batch, float *const *ys, cudaStream_t s) {
     CqSet c = {};

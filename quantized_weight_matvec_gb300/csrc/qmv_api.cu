@@ -306,21 +306,14 @@ qmv_status cq_prepare_matvec(const qmv_cq_matrix *mats, int32_t nmats, const flo
     qmv_status st = check_cq_set(mats, nmats, batch, ys, x, xb, prepared, prepared ? pb : 0);
     if (st != QMV_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // With a prepared buffer, sets off the 2-bit table kernel take the two
-    // launches: there every block of the fused kernel repeats the prepare's
-    // latency chain, and the separate prepare measured faster (3 x 2048 x 512,
-    // 4-bit: 4.8 against 5.5 us per call).
-    const bool fuse = qmv::cq_fused_fits(mats[0], batch) &&
-                      !(prepared && !qmv::cq_set_uses_table(mats, nmats, batch));
-    if (fuse) {
+    if (qmv::cq_fused_fits(mats[0], batch)) {
         if (cq_set_rows(mats, nmats) == 0) {
             // no matrix rows: the prepared activation is still produced on request
             return prepared ? qmv::launch_cq_prepare(mats[0], x, batch, prepared, s) : QMV_OK;
         }
         return qmv::launch_cq_set(mats, nmats, nullptr, x, prepared, batch, ys, s);
     }
-    // two launches through the prepared vector (needed when too wide to
-    // prepare on chip)
+    // too wide to prepare on chip: two launches through the prepared vector
     if (!prepared) return QMV_ERR_NULL;
     st = qmv::launch_cq_prepare(mats[0], x, batch, prepared, s);
     if (st != QMV_OK || cq_set_rows(mats, nmats) == 0) return st;

@@ -79,9 +79,6 @@ qmv_status launch_cq_set(const qmv_cq_matrix *mats, int nmats, const float *p, c
                          float *prepared_out, int batch, float *const *ys, cudaStream_t s);
 // Whether cq_prepare_matvec can prepare on chip (else it runs two launches).
 bool cq_fused_fits(const qmv_cq_matrix &m, int batch);
-// Whether a set call runs on the 2-bit table kernel (the fused prepare pays
-// there; elsewhere the separate prepare launch measured faster).
-bool cq_set_uses_table(const qmv_cq_matrix *mats, int nmats, int batch);
 
 // ---- I8 ------------------------------------------------------------------
 qmv_status launch_i8_matvec(const int8_t *w, int64_t R, int64_t C, const uint8_t *scale,

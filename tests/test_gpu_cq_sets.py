@@ -121,20 +121,19 @@ def launches(fn):
     return names
 
 
-def test_prepared_buffer_picks_the_faster_form():
-    """With a prepared buffer, a set off the 2-bit table kernel runs as two
-    launches (prepare, then the set); without one, or on the table kernel,
-    as one fused launch.  Results are the same bits either way."""
-    cs, mats, x = make_set((2048, 2048, 2048), 512, 64, 4, 1, seed=17)
-    p, ref = separate(mats, x)
-    prepared = torch.empty_like(p)
-    assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x, prepared=prepared))) == 2
-    assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x))) == 1
-    ys = qmv.cq_prepare_matvec_t(mats, x, prepared=prepared)
-    ys2 = qmv.cq_prepare_matvec_t(mats, x)
-    torch.cuda.synchronize()
-    for y, y2, r in zip(ys, ys2, ref):
-        assert bits_eq(y, r) and bits_eq(y2, r)
-    cs, mats, x = make_set((2048, 2048, 2048), 512, 64, 2, 1, seed=18)
-    prepared = torch.empty((1, 512), device="cuda")
-    assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x, prepared=prepared))) == 1
+def test_fused_prepare_is_one_launch_with_or_without_a_buffer():
+    """Wherever the activation fits on chip, cq_prepare_matvec is one launch,
+    whether or not the prepared vector is also stored; the results are the
+    same bits as prepare + one call per matrix."""
+    for bits, seed in ((4, 17), (2, 18)):
+        cs, mats, x = make_set((2048, 2048, 2048), 512, 64, bits, 1, seed=seed)
+        p, ref = separate(mats, x)
+        prepared = torch.empty_like(p)
+        assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x, prepared=prepared))) == 1
+        assert len(launches(lambda: qmv.cq_prepare_matvec_t(mats, x))) == 1
+        ys = qmv.cq_prepare_matvec_t(mats, x, prepared=prepared)
+        ys2 = qmv.cq_prepare_matvec_t(mats, x)
+        torch.cuda.synchronize()
+        assert bits_eq(prepared, p)
+        for y, y2, r in zip(ys, ys2, ref):
+            assert bits_eq(y, r) and bits_eq(y2, r)
