@@ -72,3 +72,42 @@ def test_powers_of_two_are_exact():
     s = 1.0 / np.sqrt(np.float64(64.0))
     s1, s2, s3 = split(s)
     assert s1 == np.float32(0.125) and s2 == 0 and s3 == 0
+
+
+def test_host_split_of_every_power_of_two(tmp_path):
+    """The library's host code (make_scale) splits s = RN64(1/sqrt n) for
+    every power of two n up to 2^30: the split is exact, the float32 form is
+    enabled, and for odd powers the three terms are those of n = 2 scaled by
+    a power of two, so the replay above covers every group and dimension."""
+    import os
+    import shutil
+    import subprocess
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "split.cu"
+    src.write_text(
+        '#include <cstdio>\n#include "fwht_device.cuh"\n'
+        "int main() {\n"
+        "  for (int b = 0; b <= 30; b++) {\n"
+        "    qmv::Scale k = qmv::make_scale(1.0 / sqrt(double(1LL << b)));\n"
+        '    printf("%d %d %a %a %a %a\\n", b, k.fast, k.s, (double)k.s1, (double)k.s2, (double)k.s3);\n'
+        "  }\n}\n")
+    exe = tmp_path / "split"
+    subprocess.run([nvcc, "-std=c++17", "-I", os.path.join(root, "quantized_weight_matvec_gb300", "csrc"),
+                    "-o", str(exe), str(src)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    base = split(1.0 / np.sqrt(np.float64(2.0)))
+    for line in filter(None, out):
+        b, fast, s, s1, s2, s3 = line.split()
+        b = int(b)
+        s, s1, s2, s3 = (float.fromhex(t) for t in (s, s1, s2, s3))
+        assert int(fast) == 1, b
+        assert s == 1.0 / np.sqrt(np.float64(2.0 ** b))
+        assert s1 + s2 + s3 == s and np.float32(s1) == s1 and np.float32(s2) == s2 and np.float32(s3) == s3
+        if b % 2:
+            f = 2.0 ** -(b // 2)
+            assert (s1, s2, s3) == (float(base[0]) * f, float(base[1]) * f, float(base[2]) * f), b
+        else:
+            assert s1 == 2.0 ** -(b // 2) and s2 == 0 and s3 == 0, b
