@@ -651,9 +651,9 @@ def run_reference(args):
         "ms_per_step": round(total_t * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD, "batch": 1, "sample_fraction": frac},
+        "config": {"workload": WORKLOAD, "batch": 1},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "sample_fraction": frac},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
