@@ -15,7 +15,8 @@ scale blocks; one 128-column block; blocks with unequal numbers of units
 (and short last tiles); activations with a wide dynamic range inside a
 block, huge, tiny, subnormal and zero; Inf / NaN in x; saturated E4M3 codes
 and NaN scales; subnormal and large scales; integer inputs, where the result
-is exact; the fused argmax and top-k forms; determinism; that this kernel is
+is exact; the fused argmax and top-k forms (the argmax without y keeping its
+logits in a large workspace); determinism; that this kernel is
 the one launched, that shapes outside its conditions go elsewhere, and that
 none of its waits ran out of time.
 """
